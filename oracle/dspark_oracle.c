@@ -1,0 +1,460 @@
+/*
+ * dspark_oracle.c -- plain, slow CPU oracle for the DSpark per-round sampling path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library calls, links or
+ * loads this file.  It is used by tests/, by __graft_entry__.smoke() and by
+ * the cpu_baseline / reference leg of bench.py.  It shares no code, header,
+ * table or helper with the CUDA path under speculative_decoding_draft_05_gb300/csrc.
+ *
+ * Everything is written as plain loops in double precision, in the order the
+ * pages state the method.  The few places where a floating-point value decides
+ * an integer (a Gumbel argmax, the accept test, the scheduler's stop test)
+ * take that decision in the kernel's precision (fp32 keys, fixed-point tau,
+ * fp64 theta), as the comments say at each place.
+ *
+ * Sources (page title, section):
+ *   [P1] "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+ *        Generation 요약 설명" (greeksharifa.github.io): summary bullets (standard
+ *        rejection sampling preserves the target distribution), §3 (latency
+ *        L = (T_draft + T_verify)/tau, tau includes the bonus token), §3.1 (local
+ *        normalisation, Markov head B = W1 W2 conditioned on the previous token,
+ *        left-to-right sampling), §3.2.1 (soft label c* = 1 - 1/2 |p^d - p^t|_1),
+ *        §3.2.2 (prefix survival, B, tau, Theta, Algorithm 1), Appendix A.
+ *   [P2] "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+ *        Generation" (notes-ybman-uk.pages.dev): "DSpark 핵심 기술 1" -- the draft
+ *        distribution p_k(v | x0, x<k) = softmax(U_k(v) + B_k(x0, x<k, v));
+ *        "배경" -- accept the longest prefix by rejection sampling.
+ *   Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+ *        as 1, 2, 3", SC'11.
+ *   Rejection rule (the textbook form the pages call "standard rejection
+ *        sampling"): Leviathan, Kalman, Matias, "Fast Inference from Transformers
+ *        via Speculative Decoding", ICML 2023; Chen et al., "Accelerating Large
+ *        Language Model Decoding with Speculative Sampling", 2023.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_PURPOSE_DRAFT 0u
+#define ORACLE_PURPOSE_ACCEPT 1u
+#define ORACLE_PURPOSE_RESAMPLE 2u
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 (SC'11).  One round maps (c0,c1,c2,c3) with key (k0,k1) to   */
+/* (hi(M1*c2)^c1^k0, lo(M1*c2), hi(M0*c0)^c3^k1, lo(M0*c0)); the key is       */
+/* bumped by the Weyl constants (W0,W1) before every round after the first.  */
+/* ------------------------------------------------------------------------- */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k0 += W0;
+      k1 += W1;
+    }
+    uint64_t p0 = (uint64_t)M0 * (uint64_t)c0;
+    uint64_t p1 = (uint64_t)M1 * (uint64_t)c2;
+    uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    uint32_t n1 = (uint32_t)p1;
+    uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    uint32_t n3 = (uint32_t)p0;
+    c0 = n0;
+    c1 = n1;
+    c2 = n2;
+    c3 = n3;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+/* The random word for (seed, request, position, purpose, vocab id):
+ * counter = (v >> 2, position, request, purpose), key = (seed lo, seed hi),
+ * and the word is output number (v & 3). */
+uint32_t oracle_rng_word(uint64_t seed, uint32_t request, uint32_t position, uint32_t purpose,
+                         uint32_t v) {
+  uint32_t ctr[4] = {v >> 2, position, request, purpose};
+  uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  return out[v & 3u];
+}
+
+/* Uniform on the open interval (0,1): u = (2*(w >> 9) + 1) * 2^-24.  Never 0
+ * or 1, and exactly representable in fp32 as well as fp64. */
+double oracle_uniform(uint32_t w) { return ((double)(w >> 9) * 2.0 + 1.0) * 0x1p-24; }
+
+/* Standard Gumbel variate G = -ln(-ln u). */
+double oracle_gumbel(uint32_t w) { return -log(-log(oracle_uniform(w))); }
+
+/* ------------------------------------------------------------------------- */
+/* Markov head bias, [P1] §3.1: B = W1 W2 of rank r, conditioned on the       */
+/* immediately previous token: B(v) = sum_i W1[prev, i] * W2[i, v].           */
+/* ------------------------------------------------------------------------- */
+void oracle_markov_bias(const double* W1, const double* W2, int V, int r, int32_t prev,
+                        double* out /* [V] */) {
+  for (int v = 0; v < V; ++v) out[v] = 0.0;
+  const double* w1row = W1 + (size_t)prev * r;
+  for (int i = 0; i < r; ++i) {
+    const double a = w1row[i];
+    const double* w2row = W2 + (size_t)i * V;
+    for (int v = 0; v < V; ++v) out[v] += a * w2row[v];
+  }
+}
+
+void oracle_markov_bias_rows(const double* W1, const double* W2, int V, int r, const int32_t* prev,
+                             int n, double* out /* [n, V] */) {
+  for (int i = 0; i < n; ++i) oracle_markov_bias(W1, W2, V, r, prev[i], out + (size_t)i * V);
+}
+
+/* log(sum_v exp(x_v)) with the maximum taken out first. */
+static double logsumexp(const double* x, int n) {
+  double m = -INFINITY;
+  for (int i = 0; i < n; ++i)
+    if (x[i] > m) m = x[i];
+  double s = 0.0;
+  for (int i = 0; i < n; ++i) s += exp(x[i] - m);
+  return m + log(s);
+}
+
+/* argmax of fp32-rounded keys, lowest index on ties; also the fp64 gap between
+ * the chosen key and the best other key (the decision's margin). */
+static int argmax_fp32(const double* key, int n, double* margin) {
+  int best = -1;
+  float bf = -INFINITY;
+  for (int v = 0; v < n; ++v) {
+    if (isnan(key[v])) continue;
+    float f = (float)key[v];
+    if (best < 0 || f > bf) {
+      bf = f;
+      best = v;
+    }
+  }
+  if (margin) {
+    double other = -INFINITY;
+    for (int v = 0; v < n; ++v)
+      if (v != best && !isnan(key[v]) && key[v] > other) other = key[v];
+    *margin = (best >= 0) ? key[best] - other : 0.0;
+  }
+  return best;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Draft step, [P1] §3.1 and [P2] "DSpark 핵심 기술 1":                         */
+/*   for k = 1..gamma (left to right):                                        */
+/*     s_k(v)  = (U_k(v) + B_k(v)) / T,   B_k = W1[x_{k-1}] W2, x_0 = anchor   */
+/*     lse_k   = log sum_v exp(s_k(v))    (local normalisation)                */
+/*     x_k     = argmax_v s_k(v) + G(seed, request, k, DRAFT, v)  (Gumbel-max) */
+/*     logp_k  = s_k(x_k) - lse_k                                             */
+/* The argmax compares fp32-rounded keys (the kernel's precision).            */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int n_req, gamma, V, r;
+  double T;
+  uint64_t seed;
+  const int32_t* req_ids;
+  const double *U, *W1, *W2;
+  const int32_t* x0;
+  int32_t* x;
+  double *logp, *lse, *scores, *margin;
+} draft_job;
+
+static void draft_one(const draft_job* J, int i, double* s, double* key) {
+  const int g = J->gamma, V = J->V;
+  const uint32_t req = (uint32_t)J->req_ids[i];
+  int32_t prev = J->x0[i];
+  for (int k = 1; k <= g; ++k) {
+    const double* Uk = J->U + ((size_t)i * g + (k - 1)) * V;
+    oracle_markov_bias(J->W1, J->W2, V, J->r, prev, s);
+    for (int v = 0; v < V; ++v) s[v] = (Uk[v] + s[v]) / J->T;
+    const double lse = logsumexp(s, V);
+    for (int v = 0; v < V; ++v)
+      key[v] = s[v] + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)k,
+                                                    ORACLE_PURPOSE_DRAFT, (uint32_t)v));
+    double margin = 0.0;
+    const int xk = argmax_fp32(key, V, &margin);
+    const size_t o = (size_t)i * g + (k - 1);
+    J->x[o] = xk;
+    J->logp[o] = s[xk] - lse;
+    J->lse[o] = lse;
+    if (J->margin) J->margin[o] = margin;
+    if (J->scores) memcpy(J->scores + o * V, s, sizeof(double) * (size_t)V);
+    prev = xk;
+  }
+}
+
+typedef struct {
+  const void* job;
+  int n, nthreads, tid;
+  void (*fn)(const void*, int, double*, double*);
+  size_t scratch;
+} worker_arg;
+
+static void* worker(void* p) {
+  worker_arg* w = (worker_arg*)p;
+  double* a = (double*)malloc(sizeof(double) * w->scratch);
+  double* b = (double*)malloc(sizeof(double) * w->scratch);
+  for (int i = w->tid; i < w->n; i += w->nthreads) w->fn(w->job, i, a, b);
+  free(a);
+  free(b);
+  return NULL;
+}
+
+static void run_parallel(const void* job, int n, int nthreads, size_t scratch,
+                         void (*fn)(const void*, int, double*, double*)) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > n) nthreads = n > 0 ? n : 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+  worker_arg* args = (worker_arg*)malloc(sizeof(worker_arg) * nthreads);
+  for (int t = 0; t < nthreads; ++t) {
+    args[t].job = job;
+    args[t].n = n;
+    args[t].nthreads = nthreads;
+    args[t].tid = t;
+    args[t].fn = fn;
+    args[t].scratch = scratch;
+    pthread_create(&th[t], NULL, worker, &args[t]);
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+  free(th);
+  free(args);
+}
+
+static void draft_fn(const void* job, int i, double* a, double* b) {
+  draft_one((const draft_job*)job, i, a, b);
+}
+
+int oracle_draft(int n_req, const int32_t* req_ids, int gamma, int V, int r, double T,
+                 uint64_t seed, const double* U, const double* W1, const double* W2,
+                 const int32_t* x0, int32_t* x, double* logp, double* lse, double* scores,
+                 double* margin, int nthreads) {
+  if (n_req < 0 || gamma < 1 || V < 1 || r < 1 || !(T > 0.0)) return 1;
+  for (int i = 0; i < n_req; ++i)
+    if (x0[i] < 0 || x0[i] >= V) return 2;
+  draft_job J = {n_req, gamma, V, r, T, seed, req_ids, U, W1, W2, x0, x, logp, lse, scores, margin};
+  run_parallel(&J, n_req, nthreads, (size_t)V, draft_fn);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Hardware-aware prefix scheduler, [P1] §3.2.2 (Algorithm 1):                */
+/*   a_{r,j} = prod_{i<=j} c_{r,i}; candidates sorted by survival (ties:      */
+/*   smaller j, then smaller r); start with l = 0 for all, B = R, tau = R,    */
+/*   Theta_0 = tau * SPS(B); take candidates in order, B += 1, tau += a,      */
+/*   Theta = tau * SPS(B); stop at the first candidate whose Theta does not   */
+/*   strictly improve; l_r = number of taken candidates of request r.         */
+/* Precision (the kernel's, since these values decide integers): a is the    */
+/* sequential fp32 product; tau is held exactly in 2^-48 fixed point, each a */
+/* rounded to nearest (ties to even); Theta is fp64:                         */
+/*   Theta = ((double)tau_fixed * 2^-48) * SPS[B].                            */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  float a;
+  int j, r;
+} cand;
+
+static int cand_cmp(const void* pa, const void* pb) {
+  const cand* x = (const cand*)pa;
+  const cand* y = (const cand*)pb;
+  if (x->a > y->a) return -1;
+  if (x->a < y->a) return 1;
+  if (x->j != y->j) return x->j < y->j ? -1 : 1;
+  if (x->r != y->r) return x->r < y->r ? -1 : 1;
+  return 0;
+}
+
+int oracle_schedule(int R, int gamma, const float* c, const double* sps, int sps_len, int32_t* ell,
+                    double* diag /* [4]: B*, tau*, Theta*, n* (may be NULL) */,
+                    float* a_out /* [R, gamma] (may be NULL) */) {
+  if (R < 1 || gamma < 1) return 1;
+  if (sps_len < R * (1 + gamma) + 1) return 1;
+  const int n = R * gamma;
+  cand* cs = (cand*)malloc(sizeof(cand) * (size_t)n);
+  for (int r = 0; r < R; ++r) {
+    float a = 1.0f;
+    for (int j = 0; j < gamma; ++j) {
+      float cj = c[(size_t)r * gamma + j];
+      if (!(cj >= 0.0f)) cj = 0.0f; /* NaN or negative: no survival */
+      if (cj > 1.0f) cj = 1.0f;
+      a = (j == 0) ? cj : a * cj;
+      float av = a;
+      if (av == 0.0f) av = 0.0f; /* canonical +0 */
+      cs[(size_t)r * gamma + j].a = av;
+      cs[(size_t)r * gamma + j].j = j;
+      cs[(size_t)r * gamma + j].r = r;
+      if (a_out) a_out[(size_t)r * gamma + j] = av;
+    }
+  }
+  qsort(cs, (size_t)n, sizeof(cand), cand_cmp);
+  for (int r = 0; r < R; ++r) ell[r] = 0;
+  int64_t tau = (int64_t)R << 48;
+  int B = R;
+  double theta_prev = ((double)tau * 0x1p-48) * sps[B];
+  int taken = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t q = (int64_t)nearbyint((double)cs[i].a * 0x1p48);
+    const int64_t tau_i = tau + q;
+    const double theta = ((double)tau_i * 0x1p-48) * sps[B + 1];
+    if (!(theta > theta_prev)) break;
+    tau = tau_i;
+    B += 1;
+    theta_prev = theta;
+    ell[cs[i].r] += 1;
+    taken += 1;
+  }
+  if (diag) {
+    diag[0] = (double)B;
+    diag[1] = (double)tau * 0x1p-48;
+    diag[2] = theta_prev;
+    diag[3] = (double)taken;
+  }
+  free(cs);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Verification: standard rejection sampling over the scheduled prefix       */
+/* ([P1] summary, §3; [P2] "배경"), plus the soft label of [P1] §3.2.1.       */
+/*   p^t_j = softmax(Z_j / T) (target), p^d_j = exp(s_j - lse_j) (draft).     */
+/*   For j = 1..l: c*_j = sum_v min(p^d_j(v), p^t_j(v)).                     */
+/*   Accept x_j iff u_j < p^t_j(x_j) / p^d_j(x_j), tested as                  */
+/*     ln u_j < (Z_j[x_j]/T - LSE^t_j) - logp_j    (fp32 decision),          */
+/*   u_j = U01(seed, request, j, ACCEPT, 0).  n = number of leading accepts.  */
+/*   n < l: the token at row n+1 is drawn from norm(max(0, p^t - p^d)) by     */
+/*   Gumbel-max with G(seed, request, n+1, RESAMPLE, v); if that residual is  */
+/*   identically zero it is drawn from p^t instead.                           */
+/*   n = l: the bonus token at row l+1 is drawn from p^t by Gumbel-max.       */
+/*   Emitted: x_1..x_n then that token; n_emit = n + 1 ([P1] §3: tau counts   */
+/*   the bonus token).  c*_j for j > l and LSE^t_j for j > l are NaN.         */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  int n_req, gamma, V;
+  double T;
+  uint64_t seed;
+  const int32_t* req_ids;
+  const int32_t* x;
+  const double *logp, *lse, *scores, *Z;
+  const int32_t* ell;
+  int32_t *n_acc, *tokens, *n_emit, *stop_kind;
+  double *cstar, *lse_t, *acc_margin, *res_margin;
+} verify_job;
+
+static void verify_one(const verify_job* J, int i, double* buf, double* key) {
+  const int g = J->gamma, V = J->V;
+  const uint32_t req = (uint32_t)J->req_ids[i];
+  int L = J->ell[i];
+  if (L < 0) L = 0;
+  if (L > g) L = g;
+  const double* Zi = J->Z + (size_t)i * (g + 1) * V;
+  const double* Si = J->scores + (size_t)i * g * V;
+  double lse_t[1024];
+  for (int j = 1; j <= g + 1; ++j) {
+    double val = NAN;
+    if (j <= L) {
+      const double* z = Zi + (size_t)(j - 1) * V;
+      for (int v = 0; v < V; ++v) buf[v] = z[v] / J->T;
+      val = logsumexp(buf, V);
+    }
+    if (j <= 1023) lse_t[j] = val;
+    if (J->lse_t) J->lse_t[(size_t)i * (g + 1) + (j - 1)] = val;
+  }
+  for (int j = 1; j <= g; ++j) {
+    double cs = NAN;
+    if (j <= L) {
+      const double* z = Zi + (size_t)(j - 1) * V;
+      const double* s = Si + (size_t)(j - 1) * V;
+      const double ld = J->lse[(size_t)i * g + (j - 1)];
+      cs = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double pd = exp(s[v] - ld);
+        const double pt = exp(z[v] / J->T - lse_t[j]);
+        cs += pd < pt ? pd : pt;
+      }
+    }
+    J->cstar[(size_t)i * g + (j - 1)] = cs;
+  }
+  int n = 0;
+  for (int j = 1; j <= g; ++j) {
+    if (J->acc_margin) J->acc_margin[(size_t)i * g + (j - 1)] = NAN;
+  }
+  for (int j = 1; j <= L; ++j) {
+    const int32_t xj = J->x[(size_t)i * g + (j - 1)];
+    const double* z = Zi + (size_t)(j - 1) * V;
+    const double u = oracle_uniform(oracle_rng_word(J->seed, req, (uint32_t)j,
+                                                    ORACLE_PURPOSE_ACCEPT, 0u));
+    const double lhs = log(u);
+    const double rhs = (z[xj] / J->T - lse_t[j]) - J->logp[(size_t)i * g + (j - 1)];
+    if (J->acc_margin) J->acc_margin[(size_t)i * g + (j - 1)] = fabs(lhs - rhs);
+    if (!((float)lhs < (float)rhs)) break;
+    n += 1;
+  }
+  int tok = -1, kind = 0;
+  double margin = 0.0;
+  if (n < L) {
+    const int row = n + 1;
+    const double* z = Zi + (size_t)(row - 1) * V;
+    const double* s = Si + (size_t)(row - 1) * V;
+    const double ld = J->lse[(size_t)i * g + (row - 1)];
+    int any = 0;
+    for (int v = 0; v < V; ++v) {
+      const double pt = exp(z[v] / J->T - lse_t[row]);
+      const double pd = exp(s[v] - ld);
+      const double res = pt - pd;
+      if (res > 0.0) {
+        any = 1;
+        key[v] = log(res) + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)row,
+                                                          ORACLE_PURPOSE_RESAMPLE, (uint32_t)v));
+      } else {
+        key[v] = NAN;
+      }
+    }
+    kind = 1;
+    if (!any) {
+      kind = 2;
+      for (int v = 0; v < V; ++v)
+        key[v] = z[v] / J->T + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)row,
+                                                             ORACLE_PURPOSE_RESAMPLE, (uint32_t)v));
+    }
+    tok = argmax_fp32(key, V, &margin);
+  } else {
+    const int row = L + 1;
+    const double* z = Zi + (size_t)(row - 1) * V;
+    for (int v = 0; v < V; ++v)
+      key[v] = z[v] / J->T + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)row,
+                                                           ORACLE_PURPOSE_RESAMPLE, (uint32_t)v));
+    tok = argmax_fp32(key, V, &margin);
+  }
+  int32_t* t = J->tokens + (size_t)i * (g + 1);
+  for (int j = 0; j < g + 1; ++j) t[j] = -1;
+  for (int j = 0; j < n; ++j) t[j] = J->x[(size_t)i * g + j];
+  t[n] = tok;
+  J->n_acc[i] = n;
+  J->n_emit[i] = n + 1;
+  if (J->stop_kind) J->stop_kind[i] = kind;
+  if (J->res_margin) J->res_margin[i] = margin;
+}
+
+static void verify_fn(const void* job, int i, double* a, double* b) {
+  verify_one((const verify_job*)job, i, a, b);
+}
+
+int oracle_verify(int n_req, const int32_t* req_ids, int gamma, int V, double T, uint64_t seed,
+                  const int32_t* x, const double* logp, const double* lse, const double* scores,
+                  const double* Z, const int32_t* ell, int32_t* n_acc, int32_t* tokens,
+                  int32_t* n_emit, double* cstar, double* lse_t, double* acc_margin,
+                  double* res_margin, int32_t* stop_kind, int nthreads) {
+  if (n_req < 0 || gamma < 1 || gamma > 1022 || V < 1 || !(T > 0.0)) return 1;
+  for (int i = 0; i < n_req; ++i)
+    for (int j = 0; j < gamma && j < ell[i]; ++j)
+      if (x[(size_t)i * gamma + j] < 0 || x[(size_t)i * gamma + j] >= V) return 2;
+  verify_job J = {n_req,  gamma, V,    T,     seed,      req_ids, x,         logp,
+                  lse,    scores, Z,   ell,   n_acc,     tokens,  n_emit,    stop_kind,
+                  cstar,  lse_t, acc_margin, res_margin};
+  run_parallel(&J, n_req, nthreads, (size_t)V, verify_fn);
+  return 0;
+}
