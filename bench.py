@@ -1,0 +1,512 @@
+#!/usr/bin/env python
+"""Benchmark of the DSpark per-round sampling path on GB300.
+
+One step = one full round (dspark_draft_sample -> dspark_schedule ->
+dspark_verify) over one batch of synthetic input already resident in HBM.
+Metric: draft+verify positions/s = R * gamma / round time (whole job over all
+ranks).  Default workload: R = 512 requests, gamma = 16, V = 151936, r = 256,
+bf16 inputs (verify_r512_g16_v151936).
+
+Also reported on the same JSON line:
+  roofline      the dominant kernel (the draft contraction + epilogue) timed with
+                CUDA events on its own launch stream during the timed region,
+                algorithmic bytes per launch / average launch time vs the measured
+                HBM copy bandwidth;
+  e2e           the same metric through the C-ABI with pinned HOST buffers: every
+                step copies that step's inputs host->device and reads the result
+                (tokens, counts, c*, l) back;
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload on
+                this host's cores (rank 0, N = 1 only);
+  clocks        nvidia-smi SM clocks and throttle reasons sampled during the
+                timed region.
+
+--impl reference times the CPU oracle as the reference arm (rank 0 only).
+Multi-GPU (torchrun): every rank runs an independent replica (the path has no
+data-path collective); time = max over ranks; value = all ranks' positions / time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from speculative_decoding_draft_05_gb300 import workload  # noqa: E402
+
+METRIC = "draft+verify positions/s"
+DEFAULT_WORKLOAD = "verify_r512_g16_v151936"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+DRAFT_TILE_SOURCES = ["speculative_decoding_draft_05_gb300/csrc/draft.cu",
+                      "speculative_decoding_draft_05_gb300/csrc/draft_tc.cu"]
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in DRAFT_TILE_SOURCES + ["speculative_decoding_draft_05_gb300/csrc/common.cuh"]:
+        p = os.path.join(ROOT, rel)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """dram bytes per draft-tile launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "draft_tile_dram.txt")
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_digest") != source_digest():
+        return None
+    if fields.get("workload") != workload_name:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in [("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")]:
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- the round
+class Round:
+    """Device buffers of one round and the three C-ABI calls on one stream."""
+
+    def __init__(self, w: workload.Workload, seed: int, device):
+        import speculative_decoding_draft_05_gb300 as dspark
+
+        self.dspark = dspark
+        self.w, self.seed, self.device = w, seed, device
+        inp = workload.generate(w, seed=seed, device=device)
+        self.inp = inp
+        R, g, V = w.R, w.gamma, w.V
+        f32, i32 = torch.float32, torch.int32
+        self.x = torch.empty(R, g, dtype=i32, device=device)
+        self.logp = torch.empty(R, g, dtype=f32, device=device)
+        self.lse = torch.empty(R, g, dtype=f32, device=device)
+        self.scores = torch.empty(R, g, V, dtype=f32, device=device)
+        self.ell = torch.empty(R, dtype=i32, device=device)
+        self.diag = torch.empty(4, dtype=torch.float64, device=device)
+        self.n_acc = torch.empty(R, dtype=i32, device=device)
+        self.tokens = torch.empty(R, g + 1, dtype=i32, device=device)
+        self.n_emit = torch.empty(R, dtype=i32, device=device)
+        self.cstar = torch.empty(R, g, dtype=f32, device=device)
+        self.lse_t = torch.empty(R, g + 1, dtype=f32, device=device)
+        u8 = torch.uint8
+        self.ws_d = torch.empty(dspark.draft_workspace_bytes(R, g, V, w.r, w.torch_dtype), dtype=u8,
+                                device=device)
+        self.ws_s = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
+        self.ws_v = torch.empty(dspark.verify_workspace_bytes(R, g, V), dtype=u8, device=device)
+        # Target logits: the workload's target stand-in carries the Markov bias
+        # along the draft's own tokens; run the (deterministic) draft once, untimed.
+        self.draft()
+        torch.cuda.synchronize(device)
+        self.Z = self._target_logits()
+        torch.cuda.synchronize(device)
+
+    def _target_logits(self):
+        w, inp = self.w, self.inp
+        if not w.z_bias:
+            return workload.target_logits(w, inp["U"], self.seed)
+        W1f = inp["W1"].float()
+        W2f = inp["W2"].float()
+        x0, x = inp["x0"], self.x
+
+        def bias_rows(i):
+            prev = torch.cat([x0[i:i + 1].long(), x[i].long()])
+            return W1f[prev] @ W2f
+
+        return workload.target_logits(w, inp["U"], self.seed, bias_rows=bias_rows)
+
+    def draft(self, seed=None):
+        i = self.inp
+        seed = self.seed if seed is None else seed
+        self.dspark.dspark_draft_sample(i["U"], i["W1"], i["W2"], i["x0"], self.w.T, seed,
+                                        x=self.x, logp=self.logp, lse=self.lse, scores=self.scores,
+                                        workspace=self.ws_d)
+
+    def step(self, seed=None):
+        """One round; `seed` keys the round's Philox draws (default: the input seed)."""
+        i = self.inp
+        d = self.dspark
+        seed = self.seed if seed is None else seed
+        self.draft(seed)
+        d.dspark_schedule(i["conf"], i["sps"], ell=self.ell, diag=self.diag, workspace=self.ws_s)
+        d.dspark_verify(self.x, self.logp, self.lse, self.scores, self.Z, self.ell, self.w.T, seed,
+                        n_acc=self.n_acc, tokens=self.tokens, n_emit=self.n_emit, cstar=self.cstar,
+                        lse_t=self.lse_t, workspace=self.ws_v)
+
+    def input_tensors(self):
+        i = self.inp
+        return [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"], self.Z]
+
+    def result_tensors(self):
+        return [self.tokens, self.n_emit, self.n_acc, self.cstar, self.ell]
+
+
+def draft_tile_bytes(w: workload.Workload) -> int:
+    """Algorithmic bytes of one draft-contraction launch (one position k):
+    U_k read (R*V*e) + scores write (R*V*4) + W2 read (r*V*e) + A_k read (R*r*e)."""
+    e = 4 if w.dtype == "f32" else 2
+    return w.R * w.V * (e + 4) + w.r * w.V * e + w.R * w.r * e
+
+
+def draft_tile_flops(w: workload.Workload) -> int:
+    return 2 * w.R * w.r * w.V
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample_round(w, inp_cpu, req, seed, nthreads):
+    """Time one oracle round on the requests `req` (draft + full schedule + verify)."""
+    import oracle
+
+    f64 = lambda t: t.to(torch.float64).numpy()
+    W1, W2 = inp_cpu["W1_64"], inp_cpu["W2_64"]
+    x0 = inp_cpu["x0"].numpy()[req]
+    t0 = time.perf_counter()
+    od = oracle.draft(f64(inp_cpu["U"][req]), W1, W2, x0, w.T, seed, req_ids=req, nthreads=nthreads)
+    t_draft = time.perf_counter() - t0
+    # target stand-in for the sampled requests, from the oracle's own draft (untimed)
+    if w.z_bias:
+        prev = np.concatenate([x0[:, None], od["x"]], axis=1)
+        bias = oracle.markov_bias(W1, W2, prev.reshape(-1)).reshape(len(req), w.gamma + 1, w.V)
+        Z = workload.target_logits(w, inp_cpu["U"][req], seed,
+                                   bias_rows=lambda i: torch.from_numpy(bias[i]), requests=req)
+    else:
+        Z = workload.target_logits(w, inp_cpu["U"][req], seed, requests=req)
+    t0 = time.perf_counter()
+    os_ = oracle.schedule(inp_cpu["conf"].numpy(), inp_cpu["sps"].numpy())
+    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), os_["ell"][req], w.T, seed,
+                       req_ids=req, nthreads=nthreads)
+    t_rest = time.perf_counter() - t0
+    return t_draft + t_rest, int(ov["n_emit"].sum())
+
+
+def oracle_inputs(w, seed, device):
+    inp = workload.generate(w, seed=seed, device=device)
+    cpu = {k: v.cpu() for k, v in inp.items()}
+    cpu["W1_64"] = cpu["W1"].to(torch.float64).numpy()
+    cpu["W2_64"] = cpu["W2"].to(torch.float64).numpy()
+    return cpu
+
+
+def sample_size(w, nthreads, target_s=12.0):
+    """Requests per oracle sample: about target_s seconds of work on nthreads."""
+    per_req = 2.0 * w.r * w.V * w.gamma * 1.2e-9 + w.gamma * w.V * 4e-7  # ~s per request, one core
+    n = int(max(1, min(w.R, round(target_s * nthreads / max(per_req, 1e-6)))))
+    return n
+
+
+def cpu_baseline(w, seed, device, nthreads):
+    import oracle
+
+    oracle.build()
+    inp = oracle_inputs(w, seed, device)
+    n = sample_size(w, nthreads)
+    req = list(range(n))
+    t, _ = oracle_sample_round(w, inp, req, seed, nthreads)
+    return {"value": n * w.gamma / t, "unit": "positions/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{n} of {w.R} requests (all {w.gamma} positions, full V) + the full schedule; "
+                      f"{t:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, w, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    inp = oracle_inputs(w, args.seed, device)
+    n = max(1, sample_size(w, nthreads, target_s=120.0 / max(1, args.steps + args.warmup)))
+    req = list(range(n))
+    for _ in range(args.warmup):
+        oracle_sample_round(w, inp, req, args.seed, nthreads)
+    times = []
+    emitted = 0
+    for _ in range(args.steps):
+        t, e = oracle_sample_round(w, inp, req, args.seed, nthreads)
+        times.append(t)
+        emitted += e
+    tot = sum(times)
+    value = n * w.gamma * args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(workload.describe(w), seed=args.seed, sample_requests=n),
+            "cpu_baseline": {"value": value, "unit": "positions/s", "cores": nthreads,
+                             "kind": "oracle",
+                             "sample": f"{n} of {w.R} requests per step (all positions, full V) "
+                                       f"+ the full schedule"},
+            "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "accepted_tokens_per_s": emitted / tot}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, local):
+    import speculative_decoding_draft_05_gb300 as dspark
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the library has no CPU path")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    dspark.binding.load()
+    stream = torch.cuda.current_stream(device)
+    rnd = Round(w, args.seed, device)
+    seeds = [args.seed + i for i in range(args.steps)]  # one Philox key per round
+    for i in range(args.warmup):
+        rnd.step(args.seed + i)
+    torch.cuda.synchronize(device)
+    assert dspark.dspark_read_device_status(rnd.ws_d) == 0
+
+    # ---- device-timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        dspark.dspark_profile_start()
+        ev0.record(stream)
+        for sd in seeds:
+            rnd.step(sd)
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        prof = dspark.dspark_profile_stop()
+        barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world, device)
+    positions = w.R * w.gamma * args.steps * world
+    value = positions / (ms_max / 1e3)
+    # tokens emitted by those rounds (deterministic: replay the same seeds, untimed)
+    emitted = 0
+    for sd in seeds:
+        rnd.step(sd)
+        emitted += int(rnd.n_emit.sum().item())
+    accepted = sum_over_ranks(float(emitted), world, device) / (ms_max / 1e3)
+
+    # ---- e2e through the C-ABI with pinned host buffers
+    host_in = [t.cpu().pin_memory() for t in rnd.input_tensors()]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in rnd.result_tensors()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for sd in seeds[:e2e_steps]:
+        for dst, src in zip(rnd.input_tensors(), host_in):
+            dst.copy_(src, non_blocking=True)
+        rnd.step(sd)
+        for dst, src in zip(host_out, rnd.result_tensors()):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    e2e_ms = max(e0.elapsed_time(e1), 1e3 * wall)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e_value = w.R * w.gamma * e2e_steps * world / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant kernel (draft contraction + fused epilogue)
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    tile_ms, tile_n = prof["draft_tile"]
+    avg_tile_s = tile_ms / max(1, tile_n) / 1e3
+    achieved = draft_tile_bytes(w) / avg_tile_s / 1e9
+    roofline = {"bound": "hbm", "kernel": "draft_tile", "achieved": achieved, "peak": hbm_peak,
+                "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_src,
+                "traffic": recorded_traffic(w.name),
+                "algorithmic_bytes_per_launch": draft_tile_bytes(w),
+                "avg_launch_ms": avg_tile_s * 1e3,
+                "tensor": {"achieved_tflops": draft_tile_flops(w) / avg_tile_s / 1e12,
+                           "peak_tflops": bf16_peak,
+                           "frac": draft_tile_flops(w) / avg_tile_s / 1e12 / bf16_peak}}
+    kernels = {k: {"ms_per_launch": v[0] / max(1, v[1]), "launches": v[1],
+                   "share": v[0] / max(1e-9, sum(x[0] for kk, x in prof.items() if not kk.startswith("_")))}
+               for k, v in prof.items() if not k.startswith("_")}
+    launches = sum(v[1] for k, v in prof.items() if not k.startswith("_"))
+
+    out = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out = cpu_baseline(w, args.seed, device, os.cpu_count() or 1)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+                if w.dtype == "bf16" else "f32", "data": "synthetic",
+                "config": dict(workload.describe(w), seed=args.seed,
+                               parallelism="replicas" if world > 1 else "single",
+                               l2="inputs larger than L2 (U %.2f GB, scores %.2f GB, Z %.2f GB > 129 MB)" % (
+                                   w.R * w.gamma * w.V * (2 if w.dtype == "bf16" else 4) / 1e9,
+                                   w.R * w.gamma * w.V * 4 / 1e9,
+                                   w.R * (w.gamma + 1) * w.V * (2 if w.dtype == "bf16" else 4) / 1e9)),
+                "roofline": roofline, "cpu_baseline": out,
+                "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "gpu_launches": launches, "clocks": clocks.summary(),
+                "accepted_tokens_per_s": accepted, "mean_ell": float(rnd.ell.float().mean().item()),
+                "mean_emitted": float(rnd.n_emit.float().mean().item()), "kernels": kernels}
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workload.ORDER)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_info()
+    w = workload.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    run_ours(args, w, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

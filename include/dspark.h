@@ -1,0 +1,203 @@
+/*
+ * dspark.h -- C-ABI of the DSpark per-round sampling library (libdspark.so).
+ *
+ * Three calls make one speculative-decoding round on one GPU, in stream order:
+ *
+ *   dspark_draft_sample -> dspark_schedule -> dspark_verify
+ *
+ * Sources (page title, section):
+ *   "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+ *    Generation 요약 설명" (greeksharifa.github.io) -- cited below as [summary]:
+ *    opening bullets (draft proposes a block, the target verifies the accepted
+ *    prefix by rejection sampling, which keeps the target distribution),
+ *    §3 (tau counts the bonus token), §3.1 (semi-autoregressive draft, Markov
+ *    head B = W1 W2), §3.2.1 (soft label c*), §3.2.2 (prefix scheduler,
+ *    Algorithm 1).
+ *   "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+ *    Generation" (notes-ybman-uk.pages.dev) -- cited as [notes]: "DSpark 핵심
+ *    기술 1" (p_k = softmax(U_k + B_k)), "배경" (accept the longest prefix).
+ *
+ * Conventions shared by all calls
+ * -------------------------------
+ * - Every pointer except `stream`, `diag`-less NULLs and the host-side
+ *   `out` of dspark_read_device_status is a DEVICE pointer on the current
+ *   device.  The caller allocates and owns every buffer (inputs, outputs,
+ *   workspace).  The library never allocates or frees memory and keeps no
+ *   state between calls.  Inputs are read-only, outputs write-only; no
+ *   output may alias an input or another output.
+ * - Arrays are dense, row-major, with the layouts stated per argument.
+ *   Request r, draft position k (1-based) lives at index [r][k-1].
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  All calls only
+ *   enqueue work and return; none synchronises.  Results are ready when the
+ *   stream reaches them.
+ * - Randomness is Philox4x32-10 (Salmon et al., SC'11), keyed by the 64-bit
+ *   `seed` (key = (seed & 0xffffffff, seed >> 32)).  The draw for
+ *   (request r, position p, purpose q, vocab id v) uses counter
+ *   (v >> 2, p, r, q) and output word (v & 3).  Purposes: DRAFT = 0 (draft
+ *   Gumbel noise, p = k), ACCEPT = 1 (accept uniform, p = j, v = 0),
+ *   RESAMPLE = 2 (residual or bonus Gumbel noise, p = row).  A word w maps to
+ *   u = (2 (w >> 9) + 1) 2^-24 in (0,1); Gumbel noise is G = -ln(-ln u).
+ *   Argmax ties go to the lowest vocab id.
+ * - Return value: a dspark_status.  Host-side argument errors are returned
+ *   before anything is enqueued.  Errors found on the device (bad token ids,
+ *   l_r outside [0, gamma], confidence outside [0,1]) set bits in a status
+ *   word at the start of the call's workspace; the kernels clamp the bad value
+ *   and finish.  dspark_read_device_status() reads that word.
+ *
+ * Limits: 1 <= R, 1 <= gamma <= 64, 8 <= V < 2^31 with V % 8 == 0,
+ *   R * gamma <= 16384 for dspark_schedule, 16 <= r <= 256 with r % 16 == 0
+ *   (r % 64 == 0 for BF16), 0 < temperature < inf.  Beyond these:
+ *   DSPARK_ERR_UNSUPPORTED.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, bad temperature, bad dtype */
+  DSPARK_ERR_UNSUPPORTED = 2,  /* outside the limits above */
+  DSPARK_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than the *_workspace_bytes query */
+  DSPARK_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed: dspark_last_error() */
+  DSPARK_ERR_DEVICE_INPUT = 5, /* (device status) an input value was out of range */
+  DSPARK_ERR_TIMEOUT = 6       /* (device status) a bounded device-side wait gave up */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+enum { DSPARK_PURPOSE_DRAFT = 0, DSPARK_PURPOSE_ACCEPT = 1, DSPARK_PURPOSE_RESAMPLE = 2 };
+
+/* Device status word bits (OR-ed together). */
+enum { DSPARK_DEV_BAD_INPUT = 1, DSPARK_DEV_TIMEOUT = 2 };
+
+/* Text of a status code; static storage. */
+const char* dspark_status_string(int status);
+/* Text of the last CUDA error seen by this thread's calls (empty if none). */
+const char* dspark_last_error(void);
+/* 10000 * major + 100 * minor + patch. */
+int dspark_version(void);
+
+/* ------------------------------------------------------------------------
+ * dspark_draft_sample -- semi-autoregressive draft ([summary] §3.1; [notes]
+ * "DSpark 핵심 기술 1").  For k = 1..gamma, left to right, for every request r:
+ *   B_k     = W1[x_{k-1}] W2               (x_0 = x0[r]; one [R x r] x [r x V]
+ *                                           contraction per k, fp32 accumulate)
+ *   s_k(v)  = (U_k(v) + B_k(v)) / T         -> scores[r][k-1][v]
+ *   lse_k   = log sum_v exp(s_k(v))         -> lse[r][k-1]
+ *   x_k     = argmax_v s_k(v) + G(seed, r, k, DRAFT, v)   -> x[r][k-1]
+ *   logp_k  = s_k(x_k) - lse_k              -> logp[r][k-1]
+ * so p^d_k(v) = exp(scores - lse) is the locally normalised draft
+ * distribution that verification needs.
+ *
+ * U       [R, gamma, V]  dtype      backbone logits
+ * W1      [V, r]         dtype      Markov head, first factor
+ * W2      [r, V]         dtype      Markov head, second factor
+ * x0      [R]            int32      anchor token per request, in [0, V)
+ * dtype   DSPARK_F32 (fp32 CUDA-core contraction) or DSPARK_BF16 (tensor cores)
+ * x       [R, gamma]     int32      out
+ * logp    [R, gamma]     float      out
+ * lse     [R, gamma]     float      out
+ * scores  [R, gamma, V]  float      out
+ * workspace: >= dspark_draft_workspace_bytes(R, gamma, V, r, dtype) bytes,
+ *   256-byte aligned.  Contents need no initialisation and are scratch.
+ * U, W1, W2 and scores must be 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t dspark_draft_workspace_bytes(int R, int gamma, int V, int r, int dtype);
+int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int32_t* x0,
+                        int dtype, int R, int gamma, int V, int r, float temperature,
+                        uint64_t seed, int32_t* x, float* logp, float* lse, float* scores,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_schedule -- hardware-aware prefix scheduler, Algorithm 1
+ * ([summary] §3.2.2).
+ *   a_{r,j} = prod_{i<=j} c_{r,i}   (sequential fp32 product; c clamped to [0,1])
+ *   Candidates (r, j) are sorted by a descending, ties by smaller j, then
+ *   smaller r.  Start with l = 0, B = R, tau = R, Theta_0 = tau * sps[B].
+ *   Taking candidate i: B += 1, tau += a_i, Theta_i = tau * sps[B]; stop at the
+ *   first i with Theta_i <= Theta_{i-1}.  l_r = number of taken candidates of r.
+ *   tau is kept exactly in 2^-48 fixed point (each a rounded to nearest, ties
+ *   to even); Theta_i = ((double)tau_fixed * 2^-48) * sps[B] in fp64.
+ *
+ * conf    [R, gamma]   float   predicted conditional acceptance c_{r,j}
+ * sps     [sps_len]    double  measured step rate (steps/s) indexed by verify
+ *                              batch size B; sps_len >= R * (1 + gamma) + 1
+ * ell     [R]          int32   out: scheduled verify length l_r in [0, gamma]
+ * diag    [4] double or NULL   out: B*, tau*, Theta*, number of taken candidates
+ * workspace: >= dspark_schedule_workspace_bytes(R, gamma) bytes.
+ * ---------------------------------------------------------------------- */
+size_t dspark_schedule_workspace_bytes(int R, int gamma);
+int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, int gamma,
+                    int32_t* ell, double* diag, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_verify -- standard rejection sampling over the scheduled prefixes
+ * ([summary] opening bullets, §3; [notes] "배경") and the soft label
+ * ([summary] §3.2.1).  With p^t_j = softmax(Z_j / T) and
+ * p^d_j = exp(scores_j - lse_j), for every request r with l = ell[r]:
+ *   c*_j = sum_v min(p^d_j(v), p^t_j(v))  (= 1 - 1/2 |p^d_j - p^t_j|_1), j <= l
+ *   accept x_j (j = 1..l, in order) iff
+ *     ln u_j < (Z_j[x_j]/T - LSE^t_j) - logp_j,  u_j = U01(seed, r, j, ACCEPT, 0)
+ *   n = number of leading accepts.
+ *   n < l : token = argmax_v ln max(0, p^t_{n+1} - p^d_{n+1})(v) + G(seed, r, n+1, RESAMPLE, v)
+ *           (if that residual is zero everywhere: argmax_v Z_{n+1}(v)/T + G)
+ *   n = l : bonus token = argmax_v Z_{l+1}(v)/T + G(seed, r, l+1, RESAMPLE, v)
+ *   Emitted tokens: x_1..x_n, token; n_emit = n + 1.
+ *
+ * x, logp, lse, scores   the draft's outputs (layouts as in dspark_draft_sample)
+ * Z       [R, gamma+1, V]  dtype  target logits at positions 1..gamma+1
+ * ell     [R]              int32  verify lengths (dspark_schedule's output)
+ * n_acc   [R]              int32  out: accepted draft tokens n
+ * tokens  [R, gamma+1]     int32  out: emitted tokens, -1 after the n_emit-th
+ * n_emit  [R]              int32  out: n + 1
+ * cstar   [R, gamma]       float  out: c*_j for j <= l, NaN for j > l
+ * lse_t   [R, gamma+1] float or NULL  out: LSE^t_j for j <= l, NaN otherwise
+ * workspace: >= dspark_verify_workspace_bytes(R, gamma, V) bytes.
+ * Z and scores must be 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t dspark_verify_workspace_bytes(int R, int gamma, int V);
+int dspark_verify(const int32_t* x, const float* logp, const float* lse, const float* scores,
+                  const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
+                  float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
+                  int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* Copies the device status word of `workspace` (as written by the last call
+ * that used it) to *out after synchronising `stream`.  *out is a HOST pointer.
+ * Returns DSPARK_OK, or DSPARK_ERR_CUDA if the copy failed. */
+int dspark_read_device_status(const void* workspace, void* stream, int32_t* out);
+
+/* ------------------------------------------------------------------------
+ * Optional per-kernel timing (for benchmarks; not thread-safe).
+ * dspark_profile_start() makes every later kernel launch of this library be
+ * bracketed by two CUDA events recorded on the launch's own stream (the first
+ * call creates 16384 events; no device memory).  dspark_profile_stop()
+ * synchronises on the last event and returns, per kernel kind, the summed
+ * event-timed milliseconds and the launch count (each may be NULL), plus how
+ * many launches were timed (at most 8192 per start/stop window; the launch
+ * counts keep counting beyond that).
+ * ---------------------------------------------------------------------- */
+enum {
+  DSPARK_KERNEL_GATHER = 0,         /* anchor gather W1[x0] */
+  DSPARK_KERNEL_DRAFT_TILE = 1,     /* draft contraction + fused epilogue (gamma launches) */
+  DSPARK_KERNEL_DRAFT_COMBINE = 2,  /* per-row combine + next gather (gamma launches) */
+  DSPARK_KERNEL_SCHEDULE = 3,
+  DSPARK_KERNEL_VERIFY_ROWS = 4,
+  DSPARK_KERNEL_VERIFY_FINISH = 5,
+  DSPARK_KERNEL_KINDS = 6
+};
+int dspark_profile_start(void);
+int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,33 @@
+"""DSpark per-round speculative-decoding sampling path on GB300 (sm_103a).
+
+The compute lives in ``libdspark.so`` (C-ABI in include/dspark.h); this package
+holds its ctypes binding (``binding``), the in-tree build (``build``) and the
+seeded synthetic workloads (``workload``).
+"""
+from . import workload  # noqa: F401
+from .binding import (  # noqa: F401
+    DSparkError,
+    dspark_draft_sample,
+    dspark_profile_start,
+    dspark_profile_stop,
+    dspark_read_device_status,
+    dspark_schedule,
+    dspark_verify,
+    draft_workspace_bytes,
+    schedule_workspace_bytes,
+    verify_workspace_bytes,
+)
+
+__all__ = [
+    "dspark_draft_sample",
+    "dspark_schedule",
+    "dspark_verify",
+    "dspark_read_device_status",
+    "dspark_profile_start",
+    "dspark_profile_stop",
+    "draft_workspace_bytes",
+    "schedule_workspace_bytes",
+    "verify_workspace_bytes",
+    "DSparkError",
+    "workload",
+]

@@ -1,0 +1,264 @@
+// api.cu -- the C-ABI of libdspark.so (declared in include/dspark.h): argument
+// checks, workspace layout, and the launch sequence of each call.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/dspark.h"
+#include "kernels.h"
+
+namespace dspark {
+
+static thread_local char g_last_error[256] = "";
+
+static int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+  return DSPARK_ERR_CUDA;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype) {
+  (void)gamma;
+  DraftWorkspace w;
+  const size_t esize = dtype == DSPARK_BF16 ? 2 : 4;
+  const size_t tiles = (size_t)((V + kDraftTileN - 1) / kDraftTileN);
+  const size_t rows = ((size_t)R + 127) / 128 * 128;  // A padded to whole 128-row tiles
+  w.status = 0;
+  w.a_rows = align256(w.status + 4);
+  w.stats = align256(w.a_rows + rows * (size_t)r * esize);
+  w.index = align256(w.stats + (size_t)R * tiles * sizeof(float4));
+  w.total = align256(w.index + (size_t)R * tiles * sizeof(int));
+  return w;
+}
+
+static int check_common(int R, int gamma, int V, float T, int dtype) {
+  if (R <= 0 || gamma <= 0 || V <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (!(T > 0.0f) || !isfinite(T)) return DSPARK_ERR_INVALID_ARG;
+  if (dtype != DSPARK_F32 && dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
+  if (gamma > 64 || R > 65535 || V % 8 != 0 || V < 8) return DSPARK_ERR_UNSUPPORTED;
+  return DSPARK_OK;
+}
+
+// Optional event timing: while enabled, every kernel launch of the library is
+// bracketed by two CUDA events recorded on the launch's stream.  Host-side
+// state only (events, no device memory); not thread-safe.
+struct Profiler {
+  static constexpr int kMax = 8192;
+  bool on = false;
+  bool created = false;
+  int n = 0;
+  int launches[kKindCount] = {};
+  int kind[kMax];
+  cudaEvent_t ev[2 * kMax];
+};
+static Profiler g_prof;
+
+static void prof_begin(int kind, cudaStream_t s) {
+  if (!g_prof.on) return;
+  g_prof.launches[kind] += 1;
+  if (g_prof.n < Profiler::kMax) {
+    g_prof.kind[g_prof.n] = kind;
+    cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
+  }
+}
+
+static void prof_end(cudaStream_t s) {
+  if (!g_prof.on || g_prof.n >= Profiler::kMax) return;
+  cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
+  g_prof.n += 1;
+}
+
+}  // namespace dspark
+
+using namespace dspark;
+
+extern "C" {
+
+const char* dspark_status_string(int status) {
+  switch (status) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_ERR_INVALID_ARG: return "invalid argument";
+    case DSPARK_ERR_UNSUPPORTED: return "unsupported size or dtype";
+    case DSPARK_ERR_WORKSPACE: return "workspace missing or too small";
+    case DSPARK_ERR_CUDA: return "CUDA error";
+    case DSPARK_ERR_DEVICE_INPUT: return "device input out of range";
+    case DSPARK_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* dspark_last_error(void) { return g_last_error; }
+
+int dspark_version(void) { return 10000; }
+
+size_t dspark_draft_workspace_bytes(int R, int gamma, int V, int r, int dtype) {
+  if (R <= 0 || gamma <= 0 || V <= 0 || r <= 0) return 0;
+  return draft_workspace_layout(R, gamma, V, r, dtype).total;
+}
+
+int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int32_t* x0,
+                        int dtype, int R, int gamma, int V, int r, float temperature,
+                        uint64_t seed, int32_t* x, float* logp, float* lse, float* scores,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (!U || !W1 || !W2 || !x0 || !x || !logp || !lse || !scores) return DSPARK_ERR_INVALID_ARG;
+  if (r <= 0) return DSPARK_ERR_INVALID_ARG;
+  int st = check_common(R, gamma, V, temperature, dtype);
+  if (st != DSPARK_OK) return st;
+  if (r > 256 || r % 16 != 0 || (dtype == DSPARK_BF16 && r % 64 != 0)) return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(scores))
+    return DSPARK_ERR_INVALID_ARG;
+  const DraftWorkspace L = draft_workspace_layout(R, gamma, V, r, dtype);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  int* status = (int*)(ws + L.status);
+  void* A = ws + L.a_rows;
+  const bool tc = dtype == DSPARK_BF16 && draft_tc_supported(R, V, r);
+  DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index),
+                  tc ? draft_tc_parts(R, V) : (V + kDraftTileN - 1) / kDraftTileN};
+  const float invT = 1.0f / temperature;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "draft status reset");
+  const size_t esize = dtype == DSPARK_BF16 ? 2 : 4;
+  const size_t pad_rows = ((size_t)R + 127) / 128 * 128 - (size_t)R;
+  if (pad_rows) {
+    e = cudaMemsetAsync((char*)A + (size_t)R * r * esize, 0, pad_rows * r * esize, s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft pad reset");
+  }
+  prof_begin(kKindGather, s);
+  e = launch_gather_anchor(W1, x0, R, V, r, dtype, A, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "gather_anchor");
+  for (int k = 1; k <= gamma; ++k) {
+    prof_begin(kKindDraftTile, s);
+    e = tc ? launch_draft_tile_tc(U, A, W2, R, gamma, V, r, k, invT, seed, scores, p, status, s)
+           : launch_draft_tile_simt(U, A, W2, dtype, R, gamma, V, r, k, invT, seed, scores, p, s);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_tile");
+    prof_begin(kKindDraftCombine, s);
+    e = launch_draft_combine(p, R, gamma, V, r, k, W1, dtype, k < gamma ? A : nullptr, x, logp, lse,
+                             status, s);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
+  }
+  return DSPARK_OK;
+}
+
+size_t dspark_schedule_workspace_bytes(int R, int gamma) {
+  (void)R;
+  (void)gamma;
+  return 256;
+}
+
+int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, int gamma,
+                    int32_t* ell, double* diag, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!conf || !sps || !ell) return DSPARK_ERR_INVALID_ARG;
+  if (R <= 0 || gamma <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (gamma > 64 || (long long)R * gamma > 16384) return DSPARK_ERR_UNSUPPORTED;
+  if ((long long)sps_len < (long long)R * (1 + gamma) + 1) return DSPARK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < dspark_schedule_workspace_bytes(R, gamma))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* status = (int*)workspace;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule status reset");
+  prof_begin(kKindSchedule, s);
+  e = launch_schedule(conf, sps, R, gamma, ell, diag, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  return DSPARK_OK;
+}
+
+size_t dspark_verify_workspace_bytes(int R, int gamma, int V) {
+  (void)V;
+  if (R <= 0 || gamma <= 0) return 0;
+  size_t off = 256;
+  off = align256(off + (size_t)R * (gamma + 1) * sizeof(float));  // LSE^t rows
+  off = align256(off + (size_t)R * gamma * sizeof(int));          // accept flags
+  return off;
+}
+
+int dspark_verify(const int32_t* x, const float* logp, const float* lse, const float* scores,
+                  const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
+                  float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
+                  int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (!x || !logp || !lse || !scores || !Z || !ell || !n_acc || !tokens || !n_emit || !cstar)
+    return DSPARK_ERR_INVALID_ARG;
+  int st = check_common(R, gamma, V, temperature, dtype);
+  if (st != DSPARK_OK) return st;
+  if (!aligned16(Z) || !aligned16(scores)) return DSPARK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < dspark_verify_workspace_bytes(R, gamma, V) ||
+      ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  int* status = (int*)ws;
+  float* lse_t_ws = (float*)(ws + 256);
+  int* acc_ws = (int*)(ws + align256(256 + (size_t)R * (gamma + 1) * sizeof(float)));
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify status reset");
+  const float invT = 1.0f / temperature;
+  prof_begin(kKindVerifyRows, s);
+  e = launch_verify_rows(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, cstar,
+                         lse_t_ws, acc_ws, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_rows");
+  prof_begin(kKindVerifyFinish, s);
+  e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
+                           n_acc, tokens, n_emit, cstar, lse_t, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_finish");
+  return DSPARK_OK;
+}
+
+int dspark_read_device_status(const void* workspace, void* stream, int32_t* out) {
+  if (!workspace || !out) return DSPARK_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "read_device_status");
+  return DSPARK_OK;
+}
+
+int dspark_profile_start(void) {
+  if (!g_prof.created) {
+    for (int i = 0; i < 2 * Profiler::kMax; ++i) {
+      cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+      if (e != cudaSuccess) return cuda_fail(e, "profile event create");
+    }
+    g_prof.created = true;
+  }
+  g_prof.n = 0;
+  for (int k = 0; k < kKindCount; ++k) g_prof.launches[k] = 0;
+  g_prof.on = true;
+  return DSPARK_OK;
+}
+
+int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches) {
+  if (!g_prof.on) return DSPARK_ERR_INVALID_ARG;
+  g_prof.on = false;
+  for (int k = 0; k < kKindCount; ++k) {
+    if (ms_by_kind) ms_by_kind[k] = 0.0;
+    if (launches_by_kind) launches_by_kind[k] = g_prof.launches[k];
+  }
+  if (timed_launches) *timed_launches = g_prof.n;
+  if (g_prof.n == 0) return DSPARK_OK;
+  cudaError_t e = cudaEventSynchronize(g_prof.ev[2 * g_prof.n - 1]);
+  if (e != cudaSuccess) return cuda_fail(e, "profile sync");
+  for (int i = 0; i < g_prof.n; ++i) {
+    float ms = 0.0f;
+    e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile elapsed");
+    if (ms_by_kind) ms_by_kind[g_prof.kind[i]] += ms;
+  }
+  return DSPARK_OK;
+}
+
+}  // extern "C"

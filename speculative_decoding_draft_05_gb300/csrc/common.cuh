@@ -1,0 +1,122 @@
+// common.cuh -- device helpers shared by the DSpark kernels.
+//
+// Philox4x32-10 follows Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers:
+// As Easy as 1, 2, 3" (SC'11).  The counter layout, uniform map and Gumbel map
+// are the library's convention, stated in include/dspark.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+// Ten rounds; the key advances by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = kPhiloxM0 * c.x, hi0 = __umulhi(kPhiloxM0, c.x);
+    const uint32_t lo1 = kPhiloxM1 * c.z, hi1 = __umulhi(kPhiloxM1, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint32_t seed_lo(uint64_t s) { return (uint32_t)(s & 0xffffffffu); }
+__device__ __forceinline__ uint32_t seed_hi(uint64_t s) { return (uint32_t)(s >> 32); }
+
+// The four words for vocab ids 4q..4q+3 at (request, position, purpose).
+__device__ __forceinline__ uint4 rng_quad(uint64_t seed, uint32_t request, uint32_t position,
+                                          uint32_t purpose, uint32_t q) {
+  return philox10(make_uint4(q, position, request, purpose), seed_lo(seed), seed_hi(seed));
+}
+
+__device__ __forceinline__ uint32_t rng_word(uint64_t seed, uint32_t request, uint32_t position,
+                                             uint32_t purpose, uint32_t v) {
+  const uint4 w = rng_quad(seed, request, position, purpose, v >> 2);
+  const uint32_t s = v & 3u;
+  return s == 0 ? w.x : s == 1 ? w.y : s == 2 ? w.z : w.w;
+}
+
+// u = (2 (w >> 9) + 1) 2^-24, exact in fp32.
+__device__ __forceinline__ float uniform01(uint32_t w) {
+  return __fmul_rn((float)(((w >> 9) << 1) | 1u), 5.9604644775390625e-8f);
+}
+
+// G = -ln(-ln u) with the accurate logf (never the approximate intrinsic:
+// ln u near 1 needs full relative accuracy).
+__device__ __forceinline__ float gumbel(uint32_t w) { return -logf(-logf(uniform01(w))); }
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// (value, index) order used by every argmax: larger value wins, ties go to the
+// lower index.  NaN keys never win.
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Merge a (max, sum of exp(x - max)) pair into another.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  if (m2 > m) {
+    s = s * __expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s = s + s2 * __expf(m2 - m);
+  }
+}
+
+__device__ __forceinline__ void warp_lse(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+}
+
+// Device status word: OR bits in with an atomic.
+__device__ __forceinline__ void flag_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace dspark

@@ -1,0 +1,221 @@
+// draft.cu -- semi-autoregressive draft step: anchor gather, CUDA-core
+// contraction + fused epilogue (fp32 inputs, and bf16 where the tensor-core
+// path does not apply), and the per-row combine that samples x_k.
+//
+// Method: "DSpark: Confidence-Scheduled Speculative Decoding with
+// Semi-Autoregressive Generation 요약 설명" §3.1 (local normalisation, Markov
+// head B = W1 W2 conditioned on the previous token, left-to-right sampling);
+// "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+// Generation" (notes), "DSpark 핵심 기술 1" (p_k = softmax(U_k + B_k)).
+//
+// One draft step k is two launches:
+//   tile kernel  : B_k tile = A_k[rows] . W2[:, tile]  (A_k = W1[x_{k-1}])
+//                  s = (U_k + B_k) / T -> scores; per (row, tile) partials
+//                  (max, sum exp, best Gumbel-perturbed score, its index and s)
+//   combine      : per row, merge the tiles' partials -> lse_k, x_k, logp_k,
+//                  and gather A_{k+1} = W1[x_k] for the next step.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+namespace {
+
+template <typename T>
+__global__ void gather_anchor_kernel(const T* __restrict__ W1, const int32_t* __restrict__ x0,
+                                     int R, int V, int r, T* __restrict__ A,
+                                     int* __restrict__ status) {
+  const int row = blockIdx.x;
+  if (row >= R) return;
+  int t = x0[row];
+  if (t < 0 || t >= V) {
+    if (threadIdx.x == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
+    t = t < 0 ? 0 : V - 1;
+  }
+  for (int i = threadIdx.x; i < r; i += blockDim.x) A[(size_t)row * r + i] = W1[(size_t)t * r + i];
+}
+
+constexpr int kSimtRows = 16;
+constexpr int kSimtThreads = kDraftTileN;  // one thread per vocab column of the tile
+constexpr int kMaxRank = 256;
+
+// Warp-level argmax carrying the score at the argmax.
+__device__ __forceinline__ void warp_argmax3(float& key, int& idx, float& sval) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ok = __shfl_xor_sync(0xffffffffu, key, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    const float os = __shfl_xor_sync(0xffffffffu, sval, o);
+    if (better(ok, oi, key, idx)) {
+      key = ok;
+      idx = oi;
+      sval = os;
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSimtThreads)
+draft_tile_simt_kernel(const T* __restrict__ U, const T* __restrict__ A, const T* __restrict__ W2,
+                       int R, int gamma, int V, int r, int k, float invT, uint64_t seed,
+                       float* __restrict__ scores, float4* __restrict__ pstats,
+                       int* __restrict__ pindex, int n_tiles) {
+  __shared__ float As[kSimtRows][kMaxRank];
+  __shared__ float red_m[4][kSimtRows], red_s[4][kSimtRows], red_k[4][kSimtRows],
+      red_v[4][kSimtRows];
+  __shared__ int red_i[4][kSimtRows];
+  const int tile = blockIdx.x;
+  const int row0 = blockIdx.y * kSimtRows;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int v = tile * kDraftTileN + tid;
+  const bool valid = v < V;
+
+  for (int i = tid; i < kSimtRows * r; i += kSimtThreads) {
+    const int rr = i / r, c = i - rr * r;
+    As[rr][c] = (row0 + rr < R) ? to_f32(A[(size_t)(row0 + rr) * r + c]) : 0.0f;
+  }
+  __syncthreads();
+
+  float acc[kSimtRows];
+#pragma unroll
+  for (int rr = 0; rr < kSimtRows; ++rr) acc[rr] = 0.0f;
+  if (valid) {
+    for (int i = 0; i < r; ++i) {
+      const float w = to_f32(W2[(size_t)i * V + v]);
+#pragma unroll
+      for (int rr = 0; rr < kSimtRows; ++rr) acc[rr] = fmaf(As[rr][i], w, acc[rr]);
+    }
+  }
+
+#pragma unroll 1
+  for (int rr = 0; rr < kSimtRows; ++rr) {
+    const int row = row0 + rr;
+    if (row >= R) break;  // uniform across the block
+    float s = -INFINITY, key = -INFINITY;
+    if (valid) {
+      const size_t o = ((size_t)row * gamma + (k - 1)) * V + v;
+      s = (to_f32(U[o]) + acc[rr]) * invT;
+      scores[o] = s;
+      key = __fadd_rn(s, gumbel(rng_word(seed, (uint32_t)row, (uint32_t)k, DSPARK_PURPOSE_DRAFT,
+                                         (uint32_t)v)));
+    }
+    float m = valid ? s : -INFINITY, S = valid ? 1.0f : 0.0f;
+    warp_lse(m, S);
+    int idx = valid ? v : 0x7fffffff;
+    float sv = s;
+    warp_argmax3(key, idx, sv);
+    if (lane == 0) {
+      red_m[warp][rr] = m;
+      red_s[warp][rr] = S;
+      red_k[warp][rr] = key;
+      red_i[warp][rr] = idx;
+      red_v[warp][rr] = sv;
+    }
+  }
+  __syncthreads();
+  if (tid < kSimtRows && row0 + tid < R) {
+    const int rr = tid;
+    float m = red_m[0][rr], S = red_s[0][rr], key = red_k[0][rr], sv = red_v[0][rr];
+    int idx = red_i[0][rr];
+    for (int w = 1; w < 4; ++w) {
+      lse_merge(m, S, red_m[w][rr], red_s[w][rr]);
+      if (better(red_k[w][rr], red_i[w][rr], key, idx)) {
+        key = red_k[w][rr];
+        idx = red_i[w][rr];
+        sv = red_v[w][rr];
+      }
+    }
+    const size_t po = (size_t)(row0 + rr) * n_tiles + tile;
+    pstats[po] = make_float4(m, S, key, sv);
+    pindex[po] = idx;
+  }
+}
+
+// One warp per row: merge the row's tile partials, sample x_k, gather W1[x_k].
+template <typename T>
+__global__ void draft_combine_kernel(const float4* __restrict__ pstats,
+                                     const int* __restrict__ pindex, int n_tiles, int R, int gamma,
+                                     int r, int k, const T* __restrict__ W1, T* __restrict__ A_next,
+                                     int32_t* __restrict__ x, float* __restrict__ logp,
+                                     float* __restrict__ lse, int V, int* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= R) return;
+  const float4* ps = pstats + (size_t)row * n_tiles;
+  const int* pi = pindex + (size_t)row * n_tiles;
+  float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
+  int idx = 0x7fffffff;
+  for (int t = lane; t < n_tiles; t += 32) {
+    const float4 q = ps[t];
+    lse_merge(m, S, q.x, q.y);
+    const int qi = pi[t];
+    if (better(q.z, qi, key, idx)) {
+      key = q.z;
+      idx = qi;
+      sv = q.w;
+    }
+  }
+  warp_lse(m, S);
+  warp_argmax3(key, idx, sv);
+  if (idx < 0 || idx >= V) {  // every score of the row was NaN
+    if (lane == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
+    idx = 0;
+  }
+  const float l = m + logf(S);
+  if (lane == 0) {
+    const size_t o = (size_t)row * gamma + (k - 1);
+    x[o] = idx;
+    logp[o] = sv - l;
+    lse[o] = l;
+  }
+  if (A_next) {
+    for (int i = lane; i < r; i += 32) A_next[(size_t)row * r + i] = W1[(size_t)idx * r + i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_anchor(const void* W1, const int32_t* x0, int R, int V, int r, int dtype,
+                                 void* A, int* status, cudaStream_t s) {
+  if (dtype == DSPARK_BF16)
+    gather_anchor_kernel<__nv_bfloat16><<<R, 64, 0, s>>>((const __nv_bfloat16*)W1, x0, R, V, r,
+                                                          (__nv_bfloat16*)A, status);
+  else
+    gather_anchor_kernel<float><<<R, 64, 0, s>>>((const float*)W1, x0, R, V, r, (float*)A, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2, int dtype, int R,
+                                   int gamma, int V, int r, int k, float invT, uint64_t seed,
+                                   float* scores, DraftPartials p, cudaStream_t s) {
+  dim3 grid(p.n_parts, (R + kSimtRows - 1) / kSimtRows);
+  if (dtype == DSPARK_BF16)
+    draft_tile_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, 0, s>>>(
+        (const __nv_bfloat16*)U, (const __nv_bfloat16*)A, (const __nv_bfloat16*)W2, R, gamma, V, r,
+        k, invT, seed, scores, p.stats, p.index, p.n_parts);
+  else
+    draft_tile_simt_kernel<float><<<grid, kSimtThreads, 0, s>>>(
+        (const float*)U, (const float*)A, (const float*)W2, R, gamma, V, r, k, invT, seed, scores,
+        p.stats, p.index, p.n_parts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_combine(DraftPartials p, int R, int gamma, int V, int r, int k,
+                                 const void* W1, int dtype, void* A_next, int32_t* x, float* logp,
+                                 float* lse, int* status, cudaStream_t s) {
+  const int warps = 8;
+  dim3 grid((R + warps - 1) / warps);
+  if (dtype == DSPARK_BF16)
+    draft_combine_kernel<__nv_bfloat16><<<grid, warps * 32, 0, s>>>(
+        p.stats, p.index, p.n_parts, R, gamma, r, k, (const __nv_bfloat16*)W1,
+        (__nv_bfloat16*)A_next, x, logp, lse, V, status);
+  else
+    draft_combine_kernel<float><<<grid, warps * 32, 0, s>>>(p.stats, p.index, p.n_parts, R, gamma,
+                                                            r, k, (const float*)W1, (float*)A_next,
+                                                            x, logp, lse, V, status);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,681 @@
+// draft_tc.cu -- bf16 draft step on the 5th-generation tensor cores (sm_103a).
+//
+// Method: "DSpark: Confidence-Scheduled Speculative Decoding with
+// Semi-Autoregressive Generation 요약 설명" §3.1 -- for draft position k the
+// Markov head adds B_k = W1[x_{k-1}] W2 (rank r) to the backbone logits U_k,
+// the result is normalised locally and x_k is sampled from it, left to right.
+// One launch computes, for all R requests at once,
+//     s = (U_k + A_k W2) / T        A_k = W1[x_{k-1}]  ([R x r], gathered)
+// writes s to `scores`, and leaves per-(row, CTA) partials of the local
+// normaliser and of the Philox-keyed Gumbel-max draw for the combine kernel.
+//
+// Structure (one CTA per SM, persistent):
+//   * The grid is (number of 128-row tiles Mt) x (slots); CTA c owns row tile
+//     c % Mt and the vocab tiles n = c / Mt, c / Mt + slots, ...  Its A tile
+//     (128 x r bf16) is loaded once by TMA and stays in shared memory; the Mt
+//     CTAs that share a vocab tile stream the same W2 tile at about the same
+//     time, so W2 comes from HBM about once per step.
+//   * warp 16 (producer): TMA of W2 chunks [64 x 128] into a 3-stage ring.
+//   * warp 17 (MMA): allocates 256 TMEM columns (two 128 x 128 fp32
+//     accumulators) and issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
+//     M = 128, N = 128, K = 16) from shared-memory descriptors: A K-major,
+//     W2 MN-major, both 128-byte swizzled.
+//   * warps 0..15 (epilogue): warp w reads TMEM lanes 32 (w % 4) .. +31 (its
+//     rows) and columns 32 (w / 4) .. +31 of the tile.  Per tile it TMA-loads
+//     its [32 x 32] block of U_k, computes s, stages it in swizzled shared
+//     memory and TMA-stores it, and updates per-row running statistics in
+//     registers: max / sum-exp (online), and the Gumbel-max best key.
+//   * Gumbel filter: element v can beat the running best key b only if
+//     -ln u_v < exp(s_v - b); since -ln u >= 1 - u, the cheap test
+//     1 - u_v < exp(s_v - b) (with 0.1% slack) lets the two logarithms run only
+//     for candidates.  The decision is the exact fp32 argmax of s + G.
+//   * Every mbarrier wait is bounded (about 2 s of SM clocks); on expiry the
+//     CTA flags DSPARK_DEV_TIMEOUT in the status word, stops issuing work,
+//     drains what it issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kTileN = kDraftTileN;  // 128
+constexpr int kChunkK = 64;          // 128 bytes of bf16: one swizzle atom row
+constexpr int kStages = 3;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = (kEpiWarps + 2) * 32;
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kMaxRank = 256;
+constexpr uint32_t kTmemCols = 256;
+
+constexpr int kAChunkBytes = kTileM * kChunkK * 2;  // 16 KB
+constexpr int kBChunkBytes = kChunkK * kTileN * 2;  // 16 KB (two 64-column boxes)
+constexpr int kUBoxBytes = 32 * 32 * 2;             // 2 KB per epilogue warp
+constexpr int kSBoxBytes = 32 * 32 * 4;             // 4 KB per epilogue warp
+
+// Shared memory layout (offsets from a 1024-aligned base).
+constexpr int kOffA = 0;                                            // 4 x 16 KB
+constexpr int kOffB = kOffA + (kMaxRank / kChunkK) * kAChunkBytes;  // 64 KB
+constexpr int kOffU = kOffB + kStages * kBChunkBytes;               // 112 KB
+constexpr int kOffS = kOffU + kEpiWarps * kUBoxBytes;               // 144 KB
+constexpr int kOffMerge = kOffS + kEpiWarps * kSBoxBytes;           // 208 KB
+constexpr int kMergeBytes = 5 * 4 * kTileM * 4;                     // 10 KB
+constexpr int kOffBar = kOffMerge + kMergeBytes;
+constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + kEpiWarps + 1;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack for 1024 alignment
+
+constexpr long long kWaitBudget = 4000000000ll;  // SM clocks (~2 s)
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete.  Returns false (and
+// raises the CTA's abort flag) if the budget runs out or another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitBudget) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          map),
+      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], one instruction of M=128, N=128, K=16.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets row (lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma: start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // version
+  d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major, B MN-major.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+  return (1u << 4)                        // D format: F32
+         | (1u << 7)                      // A format: BF16
+         | (1u << 10)                     // B format: BF16
+         | (0u << 15)                     // A K-major
+         | (1u << 16)                     // B MN-major
+         | ((uint32_t)(N >> 3) << 17)     // N / 8
+         | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+struct Params {
+  int R, gamma, V, r, k, Mt, slots, n_tiles, n_parts;
+  float invT;
+  uint64_t seed;
+  float4* pstats;
+  int* pindex;
+  int* status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmW2,
+                     const __grid_constant__ CUtensorMap tmU,
+                     const __grid_constant__ CUtensorMap tmS, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + kOffBar);
+  uint64_t* bar_a = bars;                         // A tile loaded
+  uint64_t* bar_full = bars + 1;                  // [kStages] W2 chunk loaded
+  uint64_t* bar_empty = bars + 1 + kStages;       // [kStages] W2 chunk consumed
+  uint64_t* bar_acc_full = bars + 1 + 2 * kStages;   // [2] accumulator ready
+  uint64_t* bar_acc_empty = bar_acc_full + 2;        // [2] accumulator drained
+  uint64_t* bar_u = bar_acc_empty + 2;               // [kEpiWarps] U block loaded
+  uint64_t* bar_drain = bar_u + kEpiWarps;           // MMA drain at exit
+  uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x % p.Mt;
+  const int slot = blockIdx.x / p.Mt;
+  const int n_units = slot < p.n_tiles ? (p.n_tiles - 1 - slot) / p.slots + 1 : 0;
+  const int n_chunks = p.r / kChunkK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_a, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_acc_full[b], 1);
+      mbar_init(&bar_acc_empty[b], kEpiWarps);
+    }
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(&bar_u[w], 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_units > 0) {
+      mbar_expect_tx(bar_a, n_chunks * kAChunkBytes);
+      for (int c = 0; c < n_chunks; ++c)
+        tma_load_2d(smem + kOffA + c * kAChunkBytes, &tmA, c * kChunkK, m_tile * kTileM, bar_a);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = 0; u < n_units && ok; ++u) {
+        const int n = slot + u * p.slots;
+        for (int c = 0; c < n_chunks; ++c) {
+          if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + kOffB + stage * kBChunkBytes;
+          mbar_expect_tx(&bar_full[stage], kBChunkBytes);
+          tma_load_2d(dst, &tmW2, n * kTileN, c * kChunkK, &bar_full[stage]);
+          tma_load_2d(dst + kBChunkBytes / 2, &tmW2, n * kTileN + 64, c * kChunkK, &bar_full[stage]);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) for the loads still in flight before leaving.
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar_a, 0) && clock64() - t0 < kWaitBudget) {
+        }
+        int s = stage, ph = phase;
+        for (int i = 0; i < kStages && i < issued; ++i) {
+          s = (s + kStages - 1) % kStages;
+          if (s == kStages - 1) ph ^= 1;
+          const long long t1 = clock64();
+          while (!mbar_try_wait(&bar_full[s], ph) && clock64() - t1 < kWaitBudget) {
+          }
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_units > 0) {
+      const uint32_t idesc = make_idesc(kTileM, kTileN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = mbar_wait(bar_a, 0, abort_flag);
+      tc_fence_after();
+      for (int u = 0; u < n_units && ok; ++u) {
+        const int buf = u & 1;
+        const uint32_t acc_phase = (u >> 1) & 1;
+        if (!mbar_wait(&bar_acc_empty[buf], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
+        for (int c = 0; c < n_chunks; ++c) {
+          if (!mbar_wait(&bar_full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_addr(smem + kOffA + c * kAChunkBytes);
+          const uint32_t b_base = smem_addr(smem + kOffB + stage * kBChunkBytes);
+#pragma unroll
+          for (int kk = 0; kk < kChunkK / 16; ++kk) {
+            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K advances 32 B.
+            const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            // W2: MN-major, two 64-column boxes 8 KB apart (LBO), 8-row K groups
+            // 1024 B apart (SBO); K advances 16 rows = 2048 B.
+            const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, kBChunkBytes / 2, 1024);
+            tc_mma(d_tmem, ad, bd, idesc, (c | kk) != 0);
+          }
+          tc_commit(&bar_empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bar_acc_full[buf]);
+      }
+      // All MMAs done before TMEM is freed.
+      tc_commit(bar_drain);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitBudget) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int cgrp = warp >> 2;
+    const int row_local = quarter * 32 + lane;
+    const int row = m_tile * kTileM + row_local;
+    const bool row_ok = row < p.R;
+    uint8_t* ubox = smem + kOffU + warp * kUBoxBytes;
+    uint8_t* sbox = smem + kOffS + warp * kSBoxBytes;
+    const int row0 = m_tile * kTileM + quarter * 32;
+    const int kpos = p.k - 1;
+    const float L2E = 1.4426950408889634f;
+
+    float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY, best_s = 0.0f;
+    int best_i = 0x7fffffff;
+    bool ok = true;
+
+    if (lane == 0 && n_units > 0) {
+      mbar_expect_tx(&bar_u[warp], kUBoxBytes);
+      tma_load_3d(ubox, &tmU, slot * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
+    }
+    for (int u = 0; u < n_units; ++u) {
+      const int n = slot + u * p.slots;
+      const int buf = u & 1;
+      const uint32_t acc_phase = (u >> 1) & 1;
+      const int col0 = n * kTileN + cgrp * 32;
+
+      // U block of this warp: row `lane`, 32 bf16 (64-byte rows, 64-byte swizzle).
+      ok = ok && mbar_wait(&bar_u[warp], u & 1, abort_flag);
+      uint32_t upk[16];
+      {
+        const uint32_t* rowp = (const uint32_t*)(ubox + lane * 64);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int pc = c ^ ((lane >> 1) & 3);
+          const uint4 q = *(const uint4*)(rowp + pc * 4);
+          upk[4 * c + 0] = q.x;
+          upk[4 * c + 1] = q.y;
+          upk[4 * c + 2] = q.z;
+          upk[4 * c + 3] = q.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && u + 1 < n_units && ok) {
+        fence_proxy_async();
+        mbar_expect_tx(&bar_u[warp], kUBoxBytes);
+        tma_load_3d(ubox, &tmU, (n + p.slots) * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
+      }
+
+      // Accumulator columns of this warp.
+      ok = ok && mbar_wait(&bar_acc_full[buf], acc_phase, abort_flag);
+      tc_fence_after();
+      uint32_t acc[32];
+      tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kTileN + cgrp * 32),
+                acc);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_acc_empty[buf]);
+
+      float s[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float u0 = __uint_as_float(upk[i] << 16);
+        const float u1 = __uint_as_float(upk[i] & 0xffff0000u);
+        s[2 * i] = (u0 + __uint_as_float(acc[2 * i])) * p.invT;
+        s[2 * i + 1] = (u1 + __uint_as_float(acc[2 * i + 1])) * p.invT;
+      }
+
+      // Stage s (128-byte rows, 128-byte swizzle) and store it with TMA.
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+      {
+        uint8_t* rowp = sbox + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int pc = c ^ (lane & 7);
+          *(float4*)(rowp + pc * 16) = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tmS, sbox, col0, kpos, row0);
+        bulk_commit();
+      }
+
+      // Running statistics of this row over its columns.
+      const int nvalid = row_ok ? min(32, p.V - col0) : 0;
+      if (nvalid > 0) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nvalid) mx = fmaxf(mx, s[i]);
+        const float mxl = mx * L2E;
+        float st = 0.0f;
+        // Gumbel-max over the tile's columns, in increasing vocab id, fused
+        // with the sum of exp(s - mx).
+        float kf = best == -INFINITY ? INFINITY : ex2_approx((mx - best) * L2E) * 1.001f;
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const uint4 w4 = rng_quad(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
+                                    (uint32_t)((col0 >> 2) + q4));
+          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = 4 * q4 + j;
+            if (i >= nvalid) continue;
+            const float e = ex2_approx(fmaf(s[i], L2E, -mxl));
+            st += e;
+            // 1 - u, exactly: (2 m + 1) 2^-24 with m the complemented 23-bit field.
+            const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~wv[j]) >> 9)), 0.99999994f);
+            if (om < e * kf) {
+              const float key = __fadd_rn(s[i], gumbel(wv[j]));
+              if (key > best) {
+                best = key;
+                best_i = col0 + i;
+                best_s = s[i];
+                kf = ex2_approx((mx - best) * L2E) * 1.001f;
+              }
+            }
+          }
+        }
+        lse_merge(run_m, run_s, mx, st);
+      }
+    }
+
+    // Merge the four column groups of each row, then write the row's partial.
+    float* mg = (float*)(smem + kOffMerge);
+    mg[(0 * 4 + cgrp) * kTileM + row_local] = run_m;
+    mg[(1 * 4 + cgrp) * kTileM + row_local] = run_s;
+    mg[(2 * 4 + cgrp) * kTileM + row_local] = best;
+    mg[(3 * 4 + cgrp) * kTileM + row_local] = best_s;
+    ((int*)mg)[(4 * 4 + cgrp) * kTileM + row_local] = best_i;
+    named_barrier(1, kEpiWarps * 32);
+    if (cgrp == 0 && row_ok && n_units > 0) {
+      float m = -INFINITY, S = 0.0f, bk = -INFINITY, bs = 0.0f;
+      int bi = 0x7fffffff;
+      for (int g = 0; g < 4; ++g) {
+        lse_merge(m, S, mg[(0 * 4 + g) * kTileM + row_local], mg[(1 * 4 + g) * kTileM + row_local]);
+        const float k2 = mg[(2 * 4 + g) * kTileM + row_local];
+        const int i2 = ((int*)mg)[(4 * 4 + g) * kTileM + row_local];
+        if (better(k2, i2, bk, bi)) {
+          bk = k2;
+          bi = i2;
+          bs = mg[(3 * 4 + g) * kTileM + row_local];
+        }
+      }
+      const size_t o = (size_t)row * p.n_parts + slot;
+      p.pstats[o] = make_float4(m, S, bk, bs);
+      p.pindex[o] = bi;
+    }
+    if (lane == 0) bulk_wait0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) flag_status(p.status, DSPARK_DEV_TIMEOUT);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+            CUtensorMapSwizzle sw) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides_bytes, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+}  // namespace
+
+bool draft_tc_supported(int R, int V, int r) {
+  (void)R;
+  if (r % kChunkK != 0 || r > kMaxRank || V % 8 != 0) return false;
+  return get_encode() != nullptr;
+}
+
+int draft_tc_parts(int R, int V) {
+  const int Mt = (R + kTileM - 1) / kTileM;
+  const int n_tiles = (V + kTileN - 1) / kTileN;
+  int slots = sm_count() / Mt;
+  if (slots < 1) slots = 1;
+  if (slots > n_tiles) slots = n_tiles;
+  return slots;
+}
+
+cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, int R, int gamma,
+                                 int V, int r, int k, float invT, uint64_t seed, float* scores,
+                                 DraftPartials part, int* status, cudaStream_t s) {
+  const int Mt = (R + kTileM - 1) / kTileM;
+  const int n_tiles = (V + kTileN - 1) / kTileN;
+  const int slots = draft_tc_parts(R, V);
+  CUtensorMap tmA, tmW2, tmU, tmS;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)Mt * kTileM};
+    const cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+    const cuuint32_t box[2] = {kChunkK, kTileM};
+    if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
+    const cuuint64_t strides[1] = {(cuuint64_t)V * 2};
+    const cuuint32_t box[2] = {64, kChunkK};
+    if (!encode(&tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
+    const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
+    const cuuint32_t box[3] = {32, 1, 32};
+    if (!encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, U, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
+    const cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)gamma * V * 4};
+    const cuuint32_t box[3] = {32, 1, 32};
+    if (!encode(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(draft_tile_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  Params p;
+  p.R = R;
+  p.gamma = gamma;
+  p.V = V;
+  p.r = r;
+  p.k = k;
+  p.Mt = Mt;
+  p.slots = slots;
+  p.n_tiles = n_tiles;
+  p.n_parts = slots;
+  p.invT = invT;
+  p.seed = seed;
+  p.pstats = part.stats;
+  p.pindex = part.index;
+  p.status = status;
+  draft_tile_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(tmA, tmW2, tmU, tmS, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,72 @@
+// kernels.h -- host-side launchers of the DSpark kernels (internal to libdspark.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dspark {
+
+// Per-row draft partials over a subset of the vocabulary: max m, sum exp(s - m),
+// best Gumbel-perturbed score, the score at that argmax; plus the argmax index.
+// The CUDA-core path writes one part per 128-column tile, the tensor-core path
+// one part per CTA slot.
+struct DraftPartials {
+  float4* stats;  // [R, n_parts] (m, S, best_key, s_at_best)
+  int* index;     // [R, n_parts]
+  int n_parts;
+};
+
+constexpr int kDraftTileN = 128;  // vocab columns per tile (both contraction paths)
+
+// Workspace layout of dspark_draft_sample (byte offsets, 256-aligned).
+struct DraftWorkspace {
+  size_t status, a_rows, stats, index, total;
+};
+DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype);
+
+cudaError_t launch_gather_anchor(const void* W1, const int32_t* x0, int R, int V, int r, int dtype,
+                                 void* A, int* status, cudaStream_t s);
+
+// fp32 / bf16 CUDA-core contraction + fused epilogue for draft step k (1-based).
+cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2, int dtype, int R,
+                                   int gamma, int V, int r, int k, float invT, uint64_t seed,
+                                   float* scores, DraftPartials p, cudaStream_t s);
+
+// bf16 tcgen05 contraction (TMA-fed, TMEM accumulators) + fused epilogue.
+cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, int R, int gamma,
+                                 int V, int r, int k, float invT, uint64_t seed, float* scores,
+                                 DraftPartials p, int* status, cudaStream_t s);
+bool draft_tc_supported(int R, int V, int r);
+int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path
+
+cudaError_t launch_draft_combine(DraftPartials p, int R, int gamma, int V, int r, int k,
+                                 const void* W1, int dtype, void* A_next, int32_t* x, float* logp,
+                                 float* lse, int* status, cudaStream_t s);
+
+cudaError_t launch_schedule(const float* conf, const double* sps, int R, int gamma, int32_t* ell,
+                            double* diag, int* status, cudaStream_t s);
+
+cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
+                               const float* scores, const void* Z, int dtype, const int32_t* ell,
+                               int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
+                               float* lse_t_ws, int* acc_ws, int* status, cudaStream_t s);
+
+cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
+                                 const void* Z, int dtype, const int32_t* ell, int R, int gamma,
+                                 int V, float invT, uint64_t seed, const float* lse_t_ws,
+                                 const int* acc_ws, int32_t* n_acc, int32_t* tokens,
+                                 int32_t* n_emit, float* cstar, float* lse_t, cudaStream_t s);
+
+// Kernel kinds for the optional event timing (dspark_profile_*).
+enum KernelKind {
+  kKindGather = 0,
+  kKindDraftTile = 1,
+  kKindDraftCombine = 2,
+  kKindSchedule = 3,
+  kKindVerifyRows = 4,
+  kKindVerifyFinish = 5,
+  kKindCount = 6
+};
+
+}  // namespace dspark

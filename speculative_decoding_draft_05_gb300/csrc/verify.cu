@@ -1,0 +1,314 @@
+// verify.cu -- standard rejection sampling over the scheduled prefixes, the
+// soft acceptance label, and the residual / bonus draw.
+//
+// "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
+// Generation 요약 설명": opening bullets (the target verifies the drafted block
+// by rejection sampling, which preserves the target distribution), §3 (the
+// accepted length counts the target's bonus token), §3.2.1 (soft label
+// c*_k = 1 - 1/2 |p^d_k - p^t_k|_1).  "DSpark: ... Semi-Autoregressive
+// Generation" (notes), "배경": accept the longest prefix.
+//
+// Two launches:
+//   verify_rows   one CTA per scheduled row (r, j), j <= l_r: LSE of Z_j / T,
+//                 c*_j = sum_v min(p^d_j, p^t_j), and the accept test of x_j.
+//                 The Z row is streamed twice (the second pass hits L2) and
+//                 the score row once, with 16-byte vector loads.
+//   verify_finish one CTA per request: first rejection n, then the Gumbel-max
+//                 draw from norm(max(0, p^t - p^d)) at row n + 1 or from p^t at
+//                 the bonus row l + 1; writes tokens, n_acc, n_emit and the NaN
+//                 padding of c* / LSE^t beyond l.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kVerifyThreads = 256;
+constexpr int kWarps = kVerifyThreads / 32;
+
+// Eight consecutive elements starting at 8g (row is 16-byte aligned, V % 8 == 0).
+__device__ __forceinline__ void load8(const float* __restrict__ row, int g, float (&o)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(row) + 2 * g);
+  const float4 b = __ldg(reinterpret_cast<const float4*>(row) + 2 * g + 1);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* __restrict__ row, int g, float (&o)[8]) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(row) + g);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Streaming loads for data read exactly once.
+__device__ __forceinline__ void load8_stream(const float* __restrict__ row, int g, float (&o)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(row) + 2 * g);
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(row) + 2 * g + 1);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.0f;
+  if (threadIdx.x < 32) {
+    t = lane < kWarps ? red[lane] : 0.0f;
+    t = warp_sum(t);
+    if (lane == 0) red[0] = t;
+  }
+  __syncthreads();
+  t = red[0];
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ float block_lse(float m, float s, float* rm, float* rs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_lse(m, s);
+  if (lane == 0) {
+    rm[warp] = m;
+    rs[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float mm = lane < kWarps ? rm[lane] : -INFINITY;
+    float ss = lane < kWarps ? rs[lane] : 0.0f;
+    warp_lse(mm, ss);
+    if (lane == 0) {
+      rm[0] = mm;
+      rs[0] = ss;
+    }
+  }
+  __syncthreads();
+  const float out = rm[0] + logf(rs[0]);
+  __syncthreads();
+  return out;
+}
+
+__device__ __forceinline__ void block_argmax(float& key, int& idx, float* rk, int* ri) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_argmax(key, idx);
+  if (lane == 0) {
+    rk[warp] = key;
+    ri[warp] = idx;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float k2 = lane < kWarps ? rk[lane] : -INFINITY;
+    int i2 = lane < kWarps ? ri[lane] : 0x7fffffff;
+    warp_argmax(k2, i2);
+    if (lane == 0) {
+      rk[0] = k2;
+      ri[0] = i2;
+    }
+  }
+  __syncthreads();
+  key = rk[0];
+  idx = ri[0];
+  __syncthreads();
+}
+
+__device__ __forceinline__ int clamp_ell(const int32_t* ell, int r, int gamma, int* status,
+                                         bool report) {
+  int L = ell[r];
+  if (L < 0 || L > gamma) {
+    if (report) flag_status(status, DSPARK_DEV_BAD_INPUT);
+    L = L < 0 ? 0 : gamma;
+  }
+  return L;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kVerifyThreads)
+verify_rows_kernel(const int32_t* __restrict__ x, const float* __restrict__ logp,
+                   const float* __restrict__ lse, const float* __restrict__ scores,
+                   const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
+                   float invT, uint64_t seed, float* __restrict__ cstar,
+                   float* __restrict__ lse_t_ws, int* __restrict__ acc_ws,
+                   int* __restrict__ status) {
+  __shared__ float rm[kWarps], rs[kWarps];
+  const int j = blockIdx.x + 1, r = blockIdx.y;
+  const int L = clamp_ell(ell, r, gamma, status, j == 1 && threadIdx.x == 0);
+  if (j > L) return;
+  const int groups = V >> 3;
+  const T* z = Z + ((size_t)r * (gamma + 1) + (j - 1)) * V;
+  const float* srow = scores + ((size_t)r * gamma + (j - 1)) * V;
+  const float ld = lse[(size_t)r * gamma + (j - 1)];
+
+  // Pass 1: LSE of Z_j / T.
+  float m = -INFINITY, S = 0.0f;
+  for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
+    float e[8];
+    load8(z, g, e);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      e[i] *= invT;
+      mx = fmaxf(mx, e[i]);
+    }
+    if (mx > m) {
+      S = (m == -INFINITY) ? 0.0f : S * __expf(m - mx);
+      m = mx;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S += __expf(e[i] - m);
+  }
+  const float Lt = block_lse(m, S, rm, rs);
+
+  // Pass 2: c*_j = sum_v min(p^d, p^t).
+  float acc = 0.0f;
+  for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
+    float e[8], s[8];
+    load8(z, g, e);
+    load8_stream(srow, g, s);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += fminf(__expf(s[i] - ld), __expf(e[i] * invT - Lt));
+  }
+  const float cs = block_sum(acc, rs);
+
+  if (threadIdx.x == 0) {
+    int xj = x[(size_t)r * gamma + (j - 1)];
+    if (xj < 0 || xj >= V) {
+      flag_status(status, DSPARK_DEV_BAD_INPUT);
+      xj = xj < 0 ? 0 : V - 1;
+    }
+    const float zx = to_f32(z[xj]) * invT;
+    const float rhs = (zx - Lt) - logp[(size_t)r * gamma + (j - 1)];
+    const float u = uniform01(rng_word(seed, (uint32_t)r, (uint32_t)j, DSPARK_PURPOSE_ACCEPT, 0u));
+    acc_ws[(size_t)r * gamma + (j - 1)] = logf(u) < rhs ? 1 : 0;
+    cstar[(size_t)r * gamma + (j - 1)] = cs;
+    lse_t_ws[(size_t)r * (gamma + 1) + (j - 1)] = Lt;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kVerifyThreads)
+verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
+                     const float* __restrict__ scores, const T* __restrict__ Z,
+                     const int32_t* __restrict__ ell, int gamma, int V, float invT, uint64_t seed,
+                     const float* __restrict__ lse_t_ws, const int* __restrict__ acc_ws,
+                     int32_t* __restrict__ n_acc, int32_t* __restrict__ tokens,
+                     int32_t* __restrict__ n_emit, float* __restrict__ cstar,
+                     float* __restrict__ lse_t_out) {
+  __shared__ float rk[kWarps];
+  __shared__ int ri[kWarps];
+  const int r = blockIdx.x;
+  const int L = clamp_ell(ell, r, gamma, nullptr, false);
+  int n = 0;
+  while (n < L && acc_ws[(size_t)r * gamma + n]) ++n;
+  const int groups = V >> 3;
+  const bool residual = n < L;
+  const int row = n + 1;  // 1-based position of the drawn token
+  const T* z = Z + ((size_t)r * (gamma + 1) + (row - 1)) * V;
+
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+  if (residual) {
+    const float* srow = scores + ((size_t)r * gamma + (row - 1)) * V;
+    const float ld = lse[(size_t)r * gamma + (row - 1)];
+    const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+    for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
+      float e[8], s[8];
+      load8(z, g, e);
+      load8(srow, g, s);
+      const uint4 w0 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g);
+      const uint4 w1 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g + 1);
+      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float res = expf(e[i] * invT - Lt) - expf(s[i] - ld);
+        if (res > 0.0f) {
+          const float key = __fadd_rn(logf(res), gumbel(w[i]));
+          if (better(key, 8 * g + i, best, idx)) {
+            best = key;
+            idx = 8 * g + i;
+          }
+        }
+      }
+    }
+    block_argmax(best, idx, rk, ri);
+  }
+  if (!residual || best == -INFINITY) {
+    // bonus row l + 1, or a residual that is zero everywhere: draw from p^t
+    best = -INFINITY;
+    idx = 0x7fffffff;
+    for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
+      float e[8];
+      load8(z, g, e);
+      const uint4 w0 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g);
+      const uint4 w1 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g + 1);
+      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
+        if (better(key, 8 * g + i, best, idx)) {
+          best = key;
+          idx = 8 * g + i;
+        }
+      }
+    }
+    block_argmax(best, idx, rk, ri);
+  }
+
+  int32_t* trow = tokens + (size_t)r * (gamma + 1);
+  for (int t = threadIdx.x; t < gamma + 1; t += kVerifyThreads) {
+    int32_t out = -1;
+    if (t < n) out = x[(size_t)r * gamma + t];
+    else if (t == n) out = idx;
+    trow[t] = out;
+    if (t < gamma && t >= L) cstar[(size_t)r * gamma + t] = __int_as_float(0x7fc00000);
+    if (lse_t_out)
+      lse_t_out[(size_t)r * (gamma + 1) + t] =
+          t < L ? lse_t_ws[(size_t)r * (gamma + 1) + t] : __int_as_float(0x7fc00000);
+  }
+  if (threadIdx.x == 0) {
+    n_acc[r] = n;
+    n_emit[r] = n + 1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
+                               const float* scores, const void* Z, int dtype, const int32_t* ell,
+                               int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
+                               float* lse_t_ws, int* acc_ws, int* status, cudaStream_t s) {
+  dim3 grid(gamma, R);
+  if (dtype == DSPARK_BF16)
+    verify_rows_kernel<__nv_bfloat16><<<grid, kVerifyThreads, 0, s>>>(
+        x, logp, lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, cstar, lse_t_ws,
+        acc_ws, status);
+  else
+    verify_rows_kernel<float><<<grid, kVerifyThreads, 0, s>>>(
+        x, logp, lse, scores, (const float*)Z, ell, gamma, V, invT, seed, cstar, lse_t_ws, acc_ws,
+        status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
+                                 const void* Z, int dtype, const int32_t* ell, int R, int gamma,
+                                 int V, float invT, uint64_t seed, const float* lse_t_ws,
+                                 const int* acc_ws, int32_t* n_acc, int32_t* tokens,
+                                 int32_t* n_emit, float* cstar, float* lse_t, cudaStream_t s) {
+  if (dtype == DSPARK_BF16)
+    verify_finish_kernel<__nv_bfloat16><<<R, kVerifyThreads, 0, s>>>(
+        x, lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, n_acc,
+        tokens, n_emit, cstar, lse_t);
+  else
+    verify_finish_kernel<float><<<R, kVerifyThreads, 0, s>>>(
+        x, lse, scores, (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, n_acc, tokens,
+        n_emit, cstar, lse_t);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark
