@@ -497,11 +497,16 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workload.ORDER)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--R", type=int, default=None, help="override the workload's request count")
+    ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_info()
     w = workload.WORKLOADS[args.workload]
+    over = {k: v for k, v in (("R", args.R), ("gamma", args.gamma)) if v is not None}
+    if over:
+        w = w.resized(**over)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+
 #include "../../include/dspark.h"
 #include "kernels.h"
 
@@ -134,9 +135,14 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   e = launch_gather_anchor(W1, x0, R, V, r, dtype, A, status, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "gather_anchor");
+  DraftTcPlan plan;
+  if (tc) {
+    e = prepare_draft_tc(&plan, U, A, W2, R, gamma, V, r, scores);
+    if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
+  }
   for (int k = 1; k <= gamma; ++k) {
     prof_begin(kKindDraftTile, s);
-    e = tc ? launch_draft_tile_tc(U, A, W2, R, gamma, V, r, k, invT, seed, scores, p, status, s)
+    e = tc ? launch_draft_tile_tc(plan, k, invT, seed, p, status, s)
            : launch_draft_tile_simt(U, A, W2, dtype, R, gamma, V, r, k, invT, seed, scores, p, s);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "draft_tile");

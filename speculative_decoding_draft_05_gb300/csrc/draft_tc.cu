@@ -485,14 +485,28 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       const int nvalid = row_ok ? min(32, p.V - col0) : 0;
       if (nvalid > 0) {
         float mx = -INFINITY;
+        int imx = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (i < nvalid) mx = fmaxf(mx, s[i]);
+          if (i < nvalid && s[i] > mx) {
+            mx = s[i];
+            imx = i;
+          }
+        if (best == -INFINITY) {
+          // Seed the running best with the tile's largest score: every other
+          // element is then filtered against a finite key (which can only rise).
+          const uint32_t w = rng_word(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
+                                      (uint32_t)(col0 + imx));
+          best = __fadd_rn(mx, gumbel(w));
+          best_i = col0 + imx;
+          best_s = mx;
+        }
+        // Pass 1, branch-free: sum of exp(s - mx) and the candidate mask.
+        // Element i can beat the best key b only if 1 - u_i < exp(s_i - b).
         const float mxl = mx * L2E;
+        const float kf = ex2_approx((mx - best) * L2E) * 1.001f;
         float st = 0.0f;
-        // Gumbel-max over the tile's columns, in increasing vocab id, fused
-        // with the sum of exp(s - mx).
-        float kf = best == -INFINITY ? INFINITY : ex2_approx((mx - best) * L2E) * 1.001f;
+        uint32_t cand = 0;
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const uint4 w4 = rng_quad(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
@@ -501,23 +515,30 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int i = 4 * q4 + j;
-            if (i >= nvalid) continue;
             const float e = ex2_approx(fmaf(s[i], L2E, -mxl));
-            st += e;
+            st += i < nvalid ? e : 0.0f;
             // 1 - u, exactly: (2 m + 1) 2^-24 with m the complemented 23-bit field.
             const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~wv[j]) >> 9)), 0.99999994f);
-            if (om < e * kf) {
-              const float key = __fadd_rn(s[i], gumbel(wv[j]));
-              if (key > best) {
-                best = key;
-                best_i = col0 + i;
-                best_s = s[i];
-                kf = ex2_approx((mx - best) * L2E) * 1.001f;
-              }
-            }
+            cand |= (om < e * kf && i < nvalid && i != imx) ? (1u << i) : 0u;
           }
         }
         lse_merge(run_m, run_s, mx, st);
+        // Pass 2: exact keys of the (rare) candidates, in increasing vocab id.
+        while (cand) {
+          const int i = __ffs(cand) - 1;
+          cand &= cand - 1;
+          const uint32_t w = rng_word(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
+                                      (uint32_t)(col0 + i));
+          // s_i from this warp's staged score block (row `lane`, 128-byte swizzle)
+          const float si =
+              *(const float*)(sbox + lane * 128 + (((i >> 2) ^ (lane & 7)) << 4) + ((i & 3) << 2));
+          const float key = __fadd_rn(si, gumbel(w));
+          if (better(key, col0 + i, best, best_i)) {
+            best = key;
+            best_i = col0 + i;
+            best_s = si;
+          }
+        }
       }
     }
 
@@ -613,18 +634,16 @@ int draft_tc_parts(int R, int V) {
   return slots;
 }
 
-cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, int R, int gamma,
-                                 int V, int r, int k, float invT, uint64_t seed, float* scores,
-                                 DraftPartials part, int* status, cudaStream_t s) {
+cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, const void* W2,
+                             int R, int gamma, int V, int r, float* scores) {
+  static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
   const int Mt = (R + kTileM - 1) / kTileM;
-  const int n_tiles = (V + kTileN - 1) / kTileN;
-  const int slots = draft_tc_parts(R, V);
-  CUtensorMap tmA, tmW2, tmU, tmS;
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(plan->maps);
   {
     const cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)Mt * kTileM};
     const cuuint64_t strides[1] = {(cuuint64_t)r * 2};
     const cuuint32_t box[2] = {kChunkK, kTileM};
-    if (!encode(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
+    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -632,7 +651,7 @@ cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, i
     const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
     const cuuint64_t strides[1] = {(cuuint64_t)V * 2};
     const cuuint32_t box[2] = {64, kChunkK};
-    if (!encode(&tmW2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2, dims, strides, box,
+    if (!encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -640,7 +659,7 @@ cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, i
     const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
     const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
     const cuuint32_t box[3] = {32, 1, 32};
-    if (!encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, U, dims, strides, box,
+    if (!encode(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, U, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
@@ -648,7 +667,7 @@ cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, i
     const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
     const cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)gamma * V * 4};
     const cuuint32_t box[3] = {32, 1, 32};
-    if (!encode(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box,
+    if (!encode(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -659,11 +678,24 @@ cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, i
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  plan->R = R;
+  plan->gamma = gamma;
+  plan->V = V;
+  plan->r = r;
+  return cudaSuccess;
+}
+
+cudaError_t launch_draft_tile_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
+                                 DraftPartials part, int* status, cudaStream_t s) {
+  const int Mt = (plan.R + kTileM - 1) / kTileM;
+  const int n_tiles = (plan.V + kTileN - 1) / kTileN;
+  const int slots = draft_tc_parts(plan.R, plan.V);
+  const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(plan.maps);
   Params p;
-  p.R = R;
-  p.gamma = gamma;
-  p.V = V;
-  p.r = r;
+  p.R = plan.R;
+  p.gamma = plan.gamma;
+  p.V = plan.V;
+  p.r = plan.r;
   p.k = k;
   p.Mt = Mt;
   p.slots = slots;
@@ -674,7 +706,7 @@ cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, i
   p.pstats = part.stats;
   p.pindex = part.index;
   p.status = status;
-  draft_tile_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(tmA, tmW2, tmU, tmS, p);
+  draft_tile_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
 }
 

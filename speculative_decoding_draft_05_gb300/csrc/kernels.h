@@ -34,8 +34,14 @@ cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2,
                                    float* scores, DraftPartials p, cudaStream_t s);
 
 // bf16 tcgen05 contraction (TMA-fed, TMEM accumulators) + fused epilogue.
-cudaError_t launch_draft_tile_tc(const void* U, const void* A, const void* W2, int R, int gamma,
-                                 int V, int r, int k, float invT, uint64_t seed, float* scores,
+// Tensor maps of one draft call (A, W2, U, scores), encoded once on the host.
+struct DraftTcPlan {
+  alignas(64) unsigned char maps[4][128];
+  int R, gamma, V, r;
+};
+cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, const void* W2,
+                             int R, int gamma, int V, int r, float* scores);
+cudaError_t launch_draft_tile_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  DraftPartials p, int* status, cudaStream_t s);
 bool draft_tc_supported(int R, int V, int r);
 int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path

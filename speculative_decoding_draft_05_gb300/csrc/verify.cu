@@ -27,6 +27,12 @@ namespace dspark {
 namespace {
 
 constexpr int kVerifyThreads = 256;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 constexpr int kWarps = kVerifyThreads / 32;
 
 // Eight consecutive elements starting at 8g (row is 16-byte aligned, V % 8 == 0).
@@ -211,12 +217,19 @@ verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ ls
   const int row = n + 1;  // 1-based position of the drawn token
   const T* z = Z + ((size_t)r * (gamma + 1) + (row - 1)) * V;
 
+  // Gumbel-max with an exact-preserving filter: element v can beat the running
+  // best key b only if -ln u_v < w_v exp(-b), where w_v is its weight (p^t row
+  // mass for the bonus draw, the residual for the rejection draw); since
+  // -ln u >= 1 - u, elements with 1 - u_v >= w_v exp(-b) (0.1% slack) are
+  // skipped without evaluating the logarithms.
+  const float L2E = 1.4426950408889634f;
   float best = -INFINITY;
   int idx = 0x7fffffff;
   if (residual) {
     const float* srow = scores + ((size_t)r * gamma + (row - 1)) * V;
     const float ld = lse[(size_t)r * gamma + (row - 1)];
     const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+    float kb = INFINITY;  // 1.001 exp(-best)
     for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
       float e[8], s[8];
       load8(z, g, e);
@@ -226,12 +239,17 @@ verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ ls
       const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float res = expf(e[i] * invT - Lt) - expf(s[i] - ld);
-        if (res > 0.0f) {
-          const float key = __fadd_rn(logf(res), gumbel(w[i]));
-          if (better(key, 8 * g + i, best, idx)) {
-            best = key;
-            idx = 8 * g + i;
+        const float ra = __expf(e[i] * invT - Lt) - __expf(s[i] - ld);  // approximate residual
+        const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
+        if (ra > -1e-6f && (best == -INFINITY || om < fmaxf(ra, 1e-6f) * kb)) {
+          const float res = expf(e[i] * invT - Lt) - expf(s[i] - ld);
+          if (res > 0.0f) {
+            const float key = __fadd_rn(logf(res), gumbel(w[i]));
+            if (better(key, 8 * g + i, best, idx)) {
+              best = key;
+              idx = 8 * g + i;
+              kb = ex2_approx(-best * L2E) * 1.001f;
+            }
           }
         }
       }
@@ -250,10 +268,14 @@ verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ ls
       const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
-        if (better(key, 8 * g + i, best, idx)) {
-          best = key;
-          idx = 8 * g + i;
+        const float zt = e[i] * invT;
+        const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
+        if (best == -INFINITY || om < ex2_approx((zt - best) * L2E) * 1.001f) {
+          const float key = __fadd_rn(zt, gumbel(w[i]));
+          if (better(key, 8 * g + i, best, idx)) {
+            best = key;
+            idx = 8 * g + i;
+          }
         }
       }
     }

@@ -1,0 +1,68 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each case copies the oracle and its pin tests into a temporary directory,
+plants one mistake in the copied C source, and runs the pins there: they must
+fail.  The real oracle is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = [
+    ("philox key xor dropped", "uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;",
+     "uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1;"),
+    ("nine Philox rounds", "for (int round = 0; round < 10; ++round)",
+     "for (int round = 0; round < 9; ++round)"),
+    ("uniform off by one step", "return ((double)(w >> 9) * 2.0 + 1.0) * 0x1p-24;",
+     "return ((double)(w >> 9) * 2.0 + 2.0) * 0x1p-24;"),
+    ("anchor ignored", "int32_t prev = J->x0[i];", "int32_t prev = 0;"),
+    ("previous token not advanced", "    prev = xk;", "    prev = prev;"),
+    ("temperature dropped", "s[v] = (Uk[v] + s[v]) / J->T;", "s[v] = (Uk[v] + s[v]);"),
+    ("bias sign", "out[v] += a * w2row[v];", "out[v] -= a * w2row[v];"),
+    ("accept comparison reversed", "if (!((float)lhs < (float)rhs)) break;",
+     "if (!((float)lhs > (float)rhs)) break;"),
+    ("residual sign", "const double res = pt - pd;", "const double res = pd - pt;"),
+    ("emitted token is the rejected draft", "t[n] = tok;",
+     "t[n] = J->x[(size_t)i * g + (n < g ? n : g - 1)];"),
+    ("max instead of min in c*", "cs += pd < pt ? pd : pt;", "cs += pd > pt ? pd : pt;"),
+    ("scheduler never stops", "if (!(theta > theta_prev)) break;",
+     "if (!(theta >= theta_prev)) continue;"),
+    ("survival not a product", "a = (j == 0) ? cj : a * cj;", "a = cj;"),
+    ("bonus row one too early", "const int row = L + 1;", "const int row = L > 0 ? L : 1;"),
+    ("draft stream keyed by the wrong position",
+     "(J->seed, req, (uint32_t)k,\n                                                    ORACLE_PURPOSE_DRAFT",
+     "(J->seed, req, (uint32_t)(k + 1),\n                                                    ORACLE_PURPOSE_DRAFT"),
+]
+
+
+def _prepare(tmp):
+    shutil.copytree(os.path.join(ROOT, "oracle"), os.path.join(tmp, "oracle"),
+                    ignore=shutil.ignore_patterns("*.so", "*.tmp*", "__pycache__"))
+    os.makedirs(os.path.join(tmp, "tests"))
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(tmp, "tests", "golden"))
+    for f in os.listdir(os.path.join(ROOT, "tests")):
+        if f.startswith("test_oracle_") and f.endswith(".py") and f != os.path.basename(__file__):
+            shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(tmp, "tests", f))
+    shutil.copy(os.path.join(ROOT, "tests", "conftest.py"), os.path.join(tmp, "tests", "conftest.py"))
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    tmp = str(tmp_path)
+    _prepare(tmp)
+    src = os.path.join(tmp, "oracle", "dspark_oracle.c")
+    text = open(src).read()
+    assert text.count(old) == 1, f"mutation site not found: {old!r}"
+    open(src, "w").write(text.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=tmp, PYTHONDONTWRITEBYTECODE="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests", "-x", "-q", "-p", "no:cacheprovider",
+                        "-k", "not mutation"], cwd=tmp, env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert "libdspark_oracle" not in r.stderr or r.returncode != 0
+    assert r.returncode != 0, f"pins passed with the mistake '{name}' planted:\n{r.stdout[-500:]}"
+    assert "failed" in r.stdout, r.stdout[-800:] + r.stderr[-800:]
