@@ -492,9 +492,12 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             mx = s[i];
             imx = i;
           }
+        // imx is excluded from the mask only in the tile where it seeds the best.
+        int seeded = -1;
         if (best == -INFINITY) {
           // Seed the running best with the tile's largest score: every other
           // element is then filtered against a finite key (which can only rise).
+          seeded = imx;
           const uint32_t w = rng_word(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
                                       (uint32_t)(col0 + imx));
           best = __fadd_rn(mx, gumbel(w));
@@ -519,7 +522,7 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             st += i < nvalid ? e : 0.0f;
             // 1 - u, exactly: (2 m + 1) 2^-24 with m the complemented 23-bit field.
             const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~wv[j]) >> 9)), 0.99999994f);
-            cand |= (om < e * kf && i < nvalid && i != imx) ? (1u << i) : 0u;
+            cand |= (om < e * kf && i < nvalid && i != seeded) ? (1u << i) : 0u;
           }
         }
         lse_merge(run_m, run_s, mx, st);
