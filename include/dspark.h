@@ -169,6 +169,42 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
                   int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * dspark_verify_noalloc -- dspark_verify for callers that cannot allocate
+ * device memory.  The paper has no counterpart; this is a deployment aid.
+ *
+ * Some callers have no way to obtain a device buffer at the point where they
+ * verify: an engine that carves all of its device memory into fixed pools at
+ * start-up and has none left to hand out, or code running where a cudaMalloc
+ * would synchronise the device in the middle of a serving round.  This entry
+ * point takes the same inputs and outputs as dspark_verify (caller-owned,
+ * same layouts and meaning) but no workspace: its scratch (the status word,
+ * LSE^t of every row and the accept flags) lives in a file-scope device array
+ * of DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES bytes that every GPU which loads the
+ * library holds until the process exits.
+ *
+ * - Size limit: 256 + align256(4 R (gamma+1)) + align256(4 R gamma) bytes
+ *   must fit in the array (with gamma = 16 that is R <= 31,772); larger
+ *   problems return DSPARK_ERR_UNSUPPORTED, with the reason in
+ *   dspark_last_error(), before anything is enqueued.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ * - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - Every call shares the one array, which keeps the previous call's
+ *   contents; the call clears the status word itself.  Calls whose work
+ *   overlaps on the GPU (other streams, or the same array from other host
+ *   threads) race on the array: serialise them.
+ * - Device-side input errors are clamped as in dspark_verify; their status
+ *   word is internal to the array and not reported.
+ * ---------------------------------------------------------------------- */
+#define DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES (4u << 20)
+int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
+                          const float* scores, const void* Z, int dtype, const int32_t* ell, int R,
+                          int gamma, int V, float temperature, uint64_t seed, int32_t* n_acc,
+                          int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
+                          void* stream);
+
 /* Copies the device status word of `workspace` (as written by the last call
  * that used it) to *out after synchronising `stream`.  *out is a HOST pointer.
  * Returns DSPARK_OK, or DSPARK_ERR_CUDA if the copy failed. */

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 
 #include "../../include/dspark.h"
 #include "kernels.h"
@@ -230,6 +231,80 @@ int dspark_read_device_status(const void* workspace, void* stream, int32_t* out)
   cudaError_t e = cudaMemcpyAsync(out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "read_device_status");
+  return DSPARK_OK;
+}
+
+}  // extern "C"
+
+// Scratch of dspark_verify_noalloc: a file-scope device array.  In host code
+// its name is only a stand-in; the kernels get the device address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) unsigned char g_verify_noalloc_scratch[DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES];
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[64] = {};
+
+static int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc current device");
+  if (dev < 0 || dev >= 64) {
+    snprintf(g_last_error, sizeof(g_last_error), "dspark_verify_noalloc: device %d not supported", dev);
+    return DSPARK_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_verify_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc scratch address");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DSPARK_OK;
+}
+
+extern "C" {
+
+int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
+                          const float* scores, const void* Z, int dtype, const int32_t* ell, int R,
+                          int gamma, int V, float temperature, uint64_t seed, int32_t* n_acc,
+                          int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
+                          void* stream) {
+  if (!x || !logp || !lse || !scores || !Z || !ell || !n_acc || !tokens || !n_emit || !cstar)
+    return DSPARK_ERR_INVALID_ARG;
+  int st = check_common(R, gamma, V, temperature, dtype);
+  if (st != DSPARK_OK) return st;
+  if (!aligned16(Z) || !aligned16(scores)) return DSPARK_ERR_INVALID_ARG;
+  const size_t lse_off = 256;
+  const size_t acc_off = align256(lse_off + (size_t)R * (gamma + 1) * sizeof(float));
+  const size_t need = align256(acc_off + (size_t)R * gamma * sizeof(int));
+  if (need > DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "dspark_verify_noalloc: R=%d, gamma=%d needs %zu bytes of scratch, the static array "
+             "holds %u",
+             R, gamma, need, (unsigned)DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES);
+    return DSPARK_ERR_UNSUPPORTED;
+  }
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != DSPARK_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)scratch;
+  int* status = (int*)ws;
+  float* lse_t_ws = (float*)(ws + lse_off);
+  int* acc_ws = (int*)(ws + acc_off);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc status reset");
+  const float invT = 1.0f / temperature;
+  prof_begin(kKindVerifyRows, s);
+  e = launch_verify_rows(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, cstar,
+                         lse_t_ws, acc_ws, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc rows");
+  prof_begin(kKindVerifyFinish, s);
+  e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
+                           n_acc, tokens, n_emit, cstar, lse_t, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc finish");
   return DSPARK_OK;
 }
 
