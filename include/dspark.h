@@ -123,14 +123,18 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
  *   Taking candidate i: B += 1, tau += a_i, Theta_i = tau * sps[B]; stop at the
  *   first i with Theta_i <= Theta_{i-1}.  l_r = number of taken candidates of r.
  *   tau is kept exactly in 2^-48 fixed point (each a rounded to nearest, ties
- *   to even); Theta_i = ((double)tau_fixed * 2^-48) * sps[B] in fp64.
+ *   to even); the test Theta_i > Theta_{i-1} compares the exact products
+ *   tau * sps[B] (no rounding).  diag's Theta* is ((double)tau * 2^-48) * sps[B*].
+ *   Step rates must be positive and finite: others flag DSPARK_DEV_BAD_INPUT
+ *   and count as no improvement.
  *
  * conf    [R, gamma]   float   predicted conditional acceptance c_{r,j}
  * sps     [sps_len]    double  measured step rate (steps/s) indexed by verify
  *                              batch size B; sps_len >= R * (1 + gamma) + 1
  * ell     [R]          int32   out: scheduled verify length l_r in [0, gamma]
  * diag    [4] double or NULL   out: B*, tau*, Theta*, number of taken candidates
- * workspace: >= dspark_schedule_workspace_bytes(R, gamma) bytes.
+ * workspace: >= dspark_schedule_workspace_bytes(R, gamma) bytes, 256-byte aligned
+ *   (holds the R * gamma sorted candidates).
  * ---------------------------------------------------------------------- */
 size_t dspark_schedule_workspace_bytes(int R, int gamma);
 int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, int gamma,
@@ -179,12 +183,15 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
  * would synchronise the device in the middle of a serving round.  This entry
  * point takes the same inputs and outputs as dspark_verify (caller-owned,
  * same layouts and meaning) but no workspace: its scratch (the status word,
- * LSE^t of every row and the accept flags) lives in a file-scope device array
+ * LSE^t of every row, the accept flags and the per-chunk partials of the
+ * drawn token) lives in a file-scope device array
  * of DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES bytes that every GPU which loads the
  * library holds until the process exits.
  *
- * - Size limit: 256 + align256(4 R (gamma+1)) + align256(4 R gamma) bytes
- *   must fit in the array (with gamma = 16 that is R <= 31,772); larger
+ * - Size limit: dspark_verify_workspace_bytes(R, gamma, V) =
+ *   256 + align256(4 R (gamma+1)) + align256(4 R gamma)
+ *   + align256(8 R ceil(V / 16384)) bytes must fit in the array (with
+ *   gamma = 16 and V = 151,936 that is R <= 19,782); larger
  *   problems return DSPARK_ERR_UNSUPPORTED, with the reason in
  *   dspark_last_error(), before anything is enqueued.
  * - The first call on each device looks up the array's device address

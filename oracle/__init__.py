@@ -165,7 +165,7 @@ def schedule(conf, sps):
     a = np.zeros((R, g), dtype=np.float32)
     rc = lib().oracle_schedule(R, g, _ptr(c), _ptr(s), s.size, _ptr(ell), _ptr(diag), _ptr(a))
     if rc != 0:
-        raise ValueError(f"oracle_schedule rejected its arguments (code {rc})")
+        raise ValueError(f"oracle_schedule rejected its arguments (code {rc}; 3 = a step rate that is not positive and finite)")
     return dict(ell=ell, B=int(diag[0]), tau=float(diag[1]), theta=float(diag[2]),
                 n_taken=int(diag[3]), a=a)
 

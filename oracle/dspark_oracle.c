@@ -250,13 +250,41 @@ int oracle_draft(int n_req, const int32_t* req_ids, int gamma, int V, int r, dou
 /*   strictly improve; l_r = number of taken candidates of request r.         */
 /* Precision (the kernel's, since these values decide integers): a is the    */
 /* sequential fp32 product; tau is held exactly in 2^-48 fixed point, each a */
-/* rounded to nearest (ties to even); Theta is fp64:                         */
-/*   Theta = ((double)tau_fixed * 2^-48) * SPS[B].                            */
+/* rounded to nearest (ties to even); the stop test compares the exact       */
+/* products tau_i * SPS[B_i] and tau_{i-1} * SPS[B_{i-1}] (no rounding), the */
+/* plain reading of "Theta does not improve".  The reported Theta* is the    */
+/* fp64 value ((double)tau_fixed * 2^-48) * SPS[B].                          */
 /* ------------------------------------------------------------------------- */
 typedef struct {
   float a;
   int j, r;
 } cand;
+
+/* Exact comparison of t_a * s_a > t_b * s_b for t > 0 (integers) and s > 0
+ * (finite doubles): s = m 2^e with an integer m < 2^53, so each product is a
+ * 117-bit integer times a power of two; compare leading-bit positions, then
+ * the aligned integers. */
+static int bitlen128(unsigned __int128 x) {
+  int n = 0;
+  while (x) {
+    ++n;
+    x >>= 1;
+  }
+  return n;
+}
+
+static int exact_greater(int64_t ta, double sa, int64_t tb, double sb) {
+  int ea, eb;
+  const double fa = frexp(sa, &ea), fb = frexp(sb, &eb); /* s = f 2^e, f in [0.5, 1) */
+  const unsigned __int128 pa = (unsigned __int128)(uint64_t)ta * (uint64_t)ldexp(fa, 53);
+  const unsigned __int128 pb = (unsigned __int128)(uint64_t)tb * (uint64_t)ldexp(fb, 53);
+  const int la = bitlen128(pa) + ea, lb = bitlen128(pb) + eb;
+  if (la != lb) return la > lb;
+  const int da = bitlen128(pa), db = bitlen128(pb);
+  const unsigned __int128 xa = da < db ? pa << (db - da) : pa;
+  const unsigned __int128 xb = db < da ? pb << (da - db) : pb;
+  return xa > xb;
+}
 
 static int cand_cmp(const void* pa, const void* pb) {
   const cand* x = (const cand*)pa;
@@ -292,25 +320,24 @@ int oracle_schedule(int R, int gamma, const float* c, const double* sps, int sps
   }
   qsort(cs, (size_t)n, sizeof(cand), cand_cmp);
   for (int r = 0; r < R; ++r) ell[r] = 0;
+  for (int b = R; b <= R * (1 + gamma); ++b)
+    if (!(sps[b] > 0.0) || !isfinite(sps[b])) return 3; /* step rates must be positive */
   int64_t tau = (int64_t)R << 48;
   int B = R;
-  double theta_prev = ((double)tau * 0x1p-48) * sps[B];
   int taken = 0;
   for (int i = 0; i < n; ++i) {
     const int64_t q = (int64_t)nearbyint((double)cs[i].a * 0x1p48);
     const int64_t tau_i = tau + q;
-    const double theta = ((double)tau_i * 0x1p-48) * sps[B + 1];
-    if (!(theta > theta_prev)) break;
+    if (!exact_greater(tau_i, sps[B + 1], tau, sps[B])) break;
     tau = tau_i;
     B += 1;
-    theta_prev = theta;
     ell[cs[i].r] += 1;
     taken += 1;
   }
   if (diag) {
     diag[0] = (double)B;
     diag[1] = (double)tau * 0x1p-48;
-    diag[2] = theta_prev;
+    diag[2] = ((double)tau * 0x1p-48) * sps[B];
     diag[3] = (double)taken;
   }
   free(cs);

@@ -33,8 +33,24 @@ DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype)
   w.a_rows = align256(w.status + 4);
   w.stats = align256(w.a_rows + rows * (size_t)r * esize);
   w.index = align256(w.stats + (size_t)R * tiles * sizeof(float4));
-  w.total = align256(w.index + (size_t)R * tiles * sizeof(int));
+  w.stats2 = align256(w.index + (size_t)R * tiles * sizeof(int));
+  w.index2 = align256(w.stats2 + (size_t)R * tiles * sizeof(float4));
+  w.total = align256(w.index2 + (size_t)R * tiles * sizeof(int));
   return w;
+}
+
+// Scratch layout of verify (byte offsets, 256-aligned): status word, LSE^t
+// [R, gamma+1], accept flags [R, gamma], draw partials [R, chunks] (float2).
+struct VerifyScratch {
+  size_t lse_t, acc, partials, total;
+};
+static VerifyScratch verify_scratch_layout(int R, int gamma, int V) {
+  VerifyScratch v;
+  v.lse_t = 256;
+  v.acc = align256(v.lse_t + (size_t)R * (gamma + 1) * sizeof(float));
+  v.partials = align256(v.acc + (size_t)R * gamma * sizeof(int));
+  v.total = align256(v.partials + (size_t)R * verify_draw_chunks(V) * sizeof(float2));
+  return v;
 }
 
 static int check_common(int R, int gamma, int V, float T, int dtype) {
@@ -121,8 +137,9 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   int* status = (int*)(ws + L.status);
   void* A = ws + L.a_rows;
   const bool tc = dtype == DSPARK_BF16 && draft_tc_supported(R, V, r);
-  DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index),
-                  tc ? draft_tc_parts(R, V) : (V + kDraftTileN - 1) / kDraftTileN};
+  const int n_parts = tc ? draft_tc_parts(R, V) : (V + kDraftTileN - 1) / kDraftTileN;
+  DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index), n_parts};
+  DraftPartials p2{(float4*)(ws + L.stats2), (int*)(ws + L.index2), n_parts};
   const float invT = 1.0f / temperature;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "draft status reset");
@@ -132,19 +149,34 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
     e = cudaMemsetAsync((char*)A + (size_t)R * r * esize, 0, pad_rows * r * esize, s);
     if (e != cudaSuccess) return cuda_fail(e, "draft pad reset");
   }
+  if (tc) {
+    // Tensor-core path: each step gathers its A tile itself; partials alternate
+    // between two buffers; one combine after the last step.
+    DraftTcPlan plan;
+    e = prepare_draft_tc(&plan, U, W2, R, gamma, V, r, scores);
+    if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
+    const DraftPartials buf[2] = {p, p2};
+    for (int k = 1; k <= gamma; ++k) {
+      prof_begin(kKindDraftTile, s);
+      e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], x, logp, lse,
+                               status, s);
+      prof_end(s);
+      if (e != cudaSuccess) return cuda_fail(e, "draft_step");
+    }
+    prof_begin(kKindDraftCombine, s);
+    e = launch_draft_combine(buf[gamma & 1], R, gamma, V, r, gamma, W1, dtype, nullptr, x, logp, lse,
+                             status, s);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
+    return DSPARK_OK;
+  }
   prof_begin(kKindGather, s);
   e = launch_gather_anchor(W1, x0, R, V, r, dtype, A, status, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "gather_anchor");
-  DraftTcPlan plan;
-  if (tc) {
-    e = prepare_draft_tc(&plan, U, A, W2, R, gamma, V, r, scores);
-    if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
-  }
   for (int k = 1; k <= gamma; ++k) {
     prof_begin(kKindDraftTile, s);
-    e = tc ? launch_draft_tile_tc(plan, k, invT, seed, p, status, s)
-           : launch_draft_tile_simt(U, A, W2, dtype, R, gamma, V, r, k, invT, seed, scores, p, s);
+    e = launch_draft_tile_simt(U, A, W2, dtype, R, gamma, V, r, k, invT, seed, scores, p, s);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "draft_tile");
     prof_begin(kKindDraftCombine, s);
@@ -157,9 +189,8 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
 }
 
 size_t dspark_schedule_workspace_bytes(int R, int gamma) {
-  (void)R;
-  (void)gamma;
-  return 256;
+  if (R <= 0 || gamma <= 0) return 0;
+  return 256 + align256(schedule_sorted_bytes(R, gamma));
 }
 
 int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, int gamma,
@@ -169,26 +200,28 @@ int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, in
   if (R <= 0 || gamma <= 0) return DSPARK_ERR_INVALID_ARG;
   if (gamma > 64 || (long long)R * gamma > 16384) return DSPARK_ERR_UNSUPPORTED;
   if ((long long)sps_len < (long long)R * (1 + gamma) + 1) return DSPARK_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < dspark_schedule_workspace_bytes(R, gamma))
+  if (!workspace || workspace_bytes < dspark_schedule_workspace_bytes(R, gamma) ||
+      ((uintptr_t)workspace & 255u))
     return DSPARK_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   int* status = (int*)workspace;
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule status reset");
+  unsigned long long* sorted = (unsigned long long*)((char*)workspace + 256);
   prof_begin(kKindSchedule, s);
-  e = launch_schedule(conf, sps, R, gamma, ell, diag, status, s);
+  e = launch_schedule_rank(conf, R, gamma, sorted, status, s);
   prof_end(s);
-  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_rank");
+  prof_begin(kKindSchedule, s);
+  e = launch_schedule_scan(sorted, sps, R, gamma, ell, diag, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_scan");
   return DSPARK_OK;
 }
 
 size_t dspark_verify_workspace_bytes(int R, int gamma, int V) {
-  (void)V;
-  if (R <= 0 || gamma <= 0) return 0;
-  size_t off = 256;
-  off = align256(off + (size_t)R * (gamma + 1) * sizeof(float));  // LSE^t rows
-  off = align256(off + (size_t)R * gamma * sizeof(int));          // accept flags
-  return off;
+  if (R <= 0 || gamma <= 0 || V <= 0) return 0;
+  return verify_scratch_layout(R, gamma, V).total;
 }
 
 int dspark_verify(const int32_t* x, const float* logp, const float* lse, const float* scores,
@@ -207,8 +240,10 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)workspace;
   int* status = (int*)ws;
-  float* lse_t_ws = (float*)(ws + 256);
-  int* acc_ws = (int*)(ws + align256(256 + (size_t)R * (gamma + 1) * sizeof(float)));
+  const VerifyScratch lay = verify_scratch_layout(R, gamma, V);
+  float* lse_t_ws = (float*)(ws + lay.lse_t);
+  int* acc_ws = (int*)(ws + lay.acc);
+  float2* partials = (float2*)(ws + lay.partials);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "verify status reset");
   const float invT = 1.0f / temperature;
@@ -219,7 +254,7 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
   if (e != cudaSuccess) return cuda_fail(e, "verify_rows");
   prof_begin(kKindVerifyFinish, s);
   e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                           n_acc, tokens, n_emit, cstar, lse_t, s);
+                           partials, n_acc, tokens, n_emit, cstar, lse_t, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "verify_finish");
   return DSPARK_OK;
@@ -274,9 +309,8 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
   int st = check_common(R, gamma, V, temperature, dtype);
   if (st != DSPARK_OK) return st;
   if (!aligned16(Z) || !aligned16(scores)) return DSPARK_ERR_INVALID_ARG;
-  const size_t lse_off = 256;
-  const size_t acc_off = align256(lse_off + (size_t)R * (gamma + 1) * sizeof(float));
-  const size_t need = align256(acc_off + (size_t)R * gamma * sizeof(int));
+  const VerifyScratch lay = verify_scratch_layout(R, gamma, V);
+  const size_t need = lay.total;
   if (need > DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES) {
     snprintf(g_last_error, sizeof(g_last_error),
              "dspark_verify_noalloc: R=%d, gamma=%d needs %zu bytes of scratch, the static array "
@@ -290,8 +324,9 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)scratch;
   int* status = (int*)ws;
-  float* lse_t_ws = (float*)(ws + lse_off);
-  int* acc_ws = (int*)(ws + acc_off);
+  float* lse_t_ws = (float*)(ws + lay.lse_t);
+  int* acc_ws = (int*)(ws + lay.acc);
+  float2* partials = (float2*)(ws + lay.partials);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
   if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc status reset");
   const float invT = 1.0f / temperature;
@@ -302,7 +337,7 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
   if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc rows");
   prof_begin(kKindVerifyFinish, s);
   e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                           n_acc, tokens, n_emit, cstar, lse_t, s);
+                           partials, n_acc, tokens, n_emit, cstar, lse_t, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc finish");
   return DSPARK_OK;

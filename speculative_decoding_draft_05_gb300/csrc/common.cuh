@@ -32,6 +32,60 @@ __device__ __forceinline__ uint4 philox10(uint4 c, uint32_t k0, uint32_t k1) {
   return c;
 }
 
+// Philox4x32-10 words for one fixed (seed, request, position, purpose) and a
+// varying first counter word q.  The same ten rounds as philox10(); the parts
+// that do not depend on q -- the round keys, round 1's product of the request
+// word, round 2's product of that round's first output -- are computed once.
+struct PhiloxStream {
+  uint32_t rk0[10], rk1[10];
+  uint32_t a0, a1;      // round-1 outputs 0 and 1 (independent of q)
+  uint32_t b_hi, b_lo;  // round-2 product M0 * a0
+  uint32_t pk1;         // purpose ^ round-1 key word 1
+
+  __device__ __forceinline__ PhiloxStream(uint64_t seed, uint32_t request, uint32_t position,
+                                          uint32_t purpose) {
+    uint32_t k0 = (uint32_t)(seed & 0xffffffffu), k1 = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+      rk0[i] = k0;
+      rk1[i] = k1;
+      k0 += kPhiloxW0;
+      k1 += kPhiloxW1;
+    }
+    const unsigned long long p1 = (unsigned long long)kPhiloxM1 * request;
+    a0 = (uint32_t)(p1 >> 32) ^ position ^ rk0[0];
+    a1 = (uint32_t)p1;
+    const unsigned long long pb = (unsigned long long)kPhiloxM0 * a0;
+    b_hi = (uint32_t)(pb >> 32);
+    b_lo = (uint32_t)pb;
+    pk1 = purpose ^ rk1[0];
+  }
+
+  __device__ __forceinline__ uint4 quad(uint32_t q) const {
+    // round 1: (q, position, request, purpose) -> (a0, a1, c2, c3)
+    const unsigned long long p0 = (unsigned long long)kPhiloxM0 * q;
+    const uint32_t c2 = (uint32_t)(p0 >> 32) ^ pk1;
+    const uint32_t c3 = (uint32_t)p0;
+    // round 2: M0 * a0 is fixed
+    const unsigned long long p1 = (unsigned long long)kPhiloxM1 * c2;
+    uint4 c = make_uint4((uint32_t)(p1 >> 32) ^ a1 ^ rk0[1], (uint32_t)p1, b_hi ^ c3 ^ rk1[1], b_lo);
+#pragma unroll
+    for (int i = 2; i < 10; ++i) {
+      const unsigned long long m0 = (unsigned long long)kPhiloxM0 * c.x;
+      const unsigned long long m1 = (unsigned long long)kPhiloxM1 * c.z;
+      c = make_uint4((uint32_t)(m1 >> 32) ^ c.y ^ rk0[i], (uint32_t)m1,
+                     (uint32_t)(m0 >> 32) ^ c.w ^ rk1[i], (uint32_t)m0);
+    }
+    return c;
+  }
+
+  __device__ __forceinline__ uint32_t word(uint32_t v) const {
+    const uint4 w = quad(v >> 2);
+    const uint32_t s = v & 3u;
+    return s == 0 ? w.x : s == 1 ? w.y : s == 2 ? w.z : w.w;
+  }
+};
+
 __device__ __forceinline__ uint32_t seed_lo(uint64_t s) { return (uint32_t)(s & 0xffffffffu); }
 __device__ __forceinline__ uint32_t seed_hi(uint64_t s) { return (uint32_t)(s >> 32); }
 

@@ -12,9 +12,15 @@
 // Structure (one CTA per SM, persistent):
 //   * The grid is (number of 128-row tiles Mt) x (slots); CTA c owns row tile
 //     c % Mt and the vocab tiles n = c / Mt, c / Mt + slots, ...  Its A tile
-//     (128 x r bf16) is loaded once by TMA and stays in shared memory; the Mt
-//     CTAs that share a vocab tile stream the same W2 tile at about the same
-//     time, so W2 comes from HBM about once per step.
+//     (128 x r bf16) stays in shared memory for the whole step; the Mt CTAs
+//     that share a vocab tile stream the same W2 tile at about the same time,
+//     so W2 comes from HBM about once per step.
+//   * The A tile is gathered by the epilogue warps at the start: for step 1
+//     from the anchors, for step k > 1 by first merging step k-1's per-slot
+//     partials of each row (its local normaliser and Gumbel-max argmax), which
+//     also yields step k-1's x, logp and lse (stored by the slot-0 CTAs).  So
+//     consecutive steps need no separate combine launch; one combine follows
+//     the last step.
 //   * warp 16 (producer): TMA of W2 chunks [64 x 128] into a 3-stage ring.
 //   * warp 17 (MMA): allocates 256 TMEM columns (two 128 x 128 fp32
 //     accumulators) and issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
@@ -253,20 +259,60 @@ struct Params {
   int R, gamma, V, r, k, Mt, slots, n_tiles, n_parts;
   float invT;
   uint64_t seed;
-  float4* pstats;
+  const int32_t* x0;             // anchors (step 1)
+  const __nv_bfloat16* W1;       // [V, r]
+  const float4* prev_stats;      // step k-1 partials (k > 1)
+  const int* prev_index;
+  float4* pstats;                // this step's partials
   int* pindex;
+  int32_t* x;                    // step k-1 outputs, written by the slot-0 CTAs
+  float* logp;
+  float* lse;
   int* status;
 };
 
+// Row `row` of step k-1: merge its per-slot partials (lanes split the slots)
+// into x_{k-1}, logp_{k-1}, lse_{k-1}.  All 32 lanes return the same values.
+__device__ __forceinline__ int combine_row(const Params& p, int row, int lane, float& lp, float& l) {
+  const float4* ps = p.prev_stats + (size_t)row * p.n_parts;
+  const int* pi = p.prev_index + (size_t)row * p.n_parts;
+  float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
+  int idx = 0x7fffffff;
+  for (int t = lane; t < p.n_parts; t += 32) {
+    const float4 q = ps[t];
+    lse_merge(m, S, q.x, q.y);
+    const int qi = pi[t];
+    if (better(q.z, qi, key, idx)) {
+      key = q.z;
+      idx = qi;
+      sv = q.w;
+    }
+  }
+  warp_lse(m, S);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ok = __shfl_xor_sync(0xffffffffu, key, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    const float os = __shfl_xor_sync(0xffffffffu, sv, o);
+    if (better(ok, oi, key, idx)) {
+      key = ok;
+      idx = oi;
+      sv = os;
+    }
+  }
+  l = m + logf(S);
+  lp = sv - l;
+  return idx;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmW2,
+draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
                      const __grid_constant__ CUtensorMap tmU,
                      const __grid_constant__ CUtensorMap tmS, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(smem + kOffBar);
-  uint64_t* bar_a = bars;                         // A tile loaded
+  uint64_t* bar_a = bars;                         // A tile gathered (one arrive per epilogue warp)
   uint64_t* bar_full = bars + 1;                  // [kStages] W2 chunk loaded
   uint64_t* bar_empty = bars + 1 + kStages;       // [kStages] W2 chunk consumed
   uint64_t* bar_acc_full = bars + 1 + 2 * kStages;   // [2] accumulator ready
@@ -283,7 +329,7 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   const int n_chunks = p.r / kChunkK;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_a, 1);
+    mbar_init(bar_a, kEpiWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
@@ -306,9 +352,6 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_units > 0) {
-      mbar_expect_tx(bar_a, n_chunks * kAChunkBytes);
-      for (int c = 0; c < n_chunks; ++c)
-        tma_load_2d(smem + kOffA + c * kAChunkBytes, &tmA, c * kChunkK, m_tile * kTileM, bar_a);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -333,9 +376,6 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       if (!ok) {
         // Drain: wait (bounded) for the loads still in flight before leaving.
-        const long long t0 = clock64();
-        while (!mbar_try_wait(bar_a, 0) && clock64() - t0 < kWaitBudget) {
-        }
         int s = stage, ph = phase;
         for (int i = 0; i < kStages && i < issued; ++i) {
           s = (s + kStages - 1) % kStages;
@@ -408,6 +448,7 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int kpos = p.k - 1;
     const float L2E = 1.4426950408889634f;
 
+    const PhiloxStream rng(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT);
     float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY, best_s = 0.0f;
     int best_i = 0x7fffffff;
     bool ok = true;
@@ -416,6 +457,43 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_expect_tx(&bar_u[warp], kUBoxBytes);
       tma_load_3d(ubox, &tmU, slot * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
     }
+    // A tile: rows m_tile*128 + 8 warp .. +7 get W1[x_{k-1}], written straight into
+    // the K-major 128-byte-swizzled layout the MMA reads (zero rows past R).
+    // x_{k-1} is the anchor for k = 1, else the combine of step k-1's partials;
+    // the slot-0 CTA of each row tile also stores step k-1's x, logp, lse.
+    for (int i = 0; i < 8; ++i) {
+      const int rl = warp * 8 + i;
+      const int arow = m_tile * kTileM + rl;
+      int xp = 0;
+      bool valid = arow < p.R;
+      if (valid) {
+        if (p.k == 1) {
+          xp = p.x0[arow];
+        } else {
+          float lp, l;
+          xp = combine_row(p, arow, lane, lp, l);
+          if (slot == 0 && lane == 0) {
+            const size_t o = (size_t)arow * p.gamma + (p.k - 2);
+            p.x[o] = xp;
+            p.logp[o] = lp;
+            p.lse[o] = l;
+          }
+        }
+        if (xp < 0 || xp >= p.V) {
+          if (lane == 0) flag_status(p.status, DSPARK_DEV_BAD_INPUT);
+          xp = xp < 0 ? 0 : p.V - 1;
+        }
+      }
+      if (lane < p.r / 8) {  // 16 bytes = 8 of the row's r bf16 per lane
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) v = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)xp * p.r) + lane);
+        const int c = lane >> 3, piece = lane & 7;
+        *(uint4*)(smem + kOffA + c * kAChunkBytes + rl * 128 + ((piece ^ (rl & 7)) << 4)) = v;
+      }
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_a);
     for (int u = 0; u < n_units; ++u) {
       const int n = slot + u * p.slots;
       const int buf = u & 1;
@@ -484,25 +562,26 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
       // Running statistics of this row over its columns.
       const int nvalid = row_ok ? min(32, p.V - col0) : 0;
       if (nvalid > 0) {
-        float mx = -INFINITY;
-        int imx = 0;
+        if (nvalid < 32) {  // ragged last tile: columns past V take no part
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nvalid && s[i] > mx) {
-            mx = s[i];
-            imx = i;
-          }
-        // imx is excluded from the mask only in the tile where it seeds the best.
-        int seeded = -1;
+          for (int i = 0; i < 32; ++i)
+            if (i >= nvalid) s[i] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
+        uint32_t keep = 0xffffffffu;
         if (best == -INFINITY) {
-          // Seed the running best with the tile's largest score: every other
-          // element is then filtered against a finite key (which can only rise).
-          seeded = imx;
-          const uint32_t w = rng_word(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
-                                      (uint32_t)(col0 + imx));
-          best = __fadd_rn(mx, gumbel(w));
+          // Seed the running best with the tile's largest score (lowest such
+          // column): every other element is then filtered against a finite key.
+          int imx = 0;
+#pragma unroll
+          for (int i = 31; i >= 0; --i)
+            if (s[i] == mx) imx = i;
+          best = __fadd_rn(mx, gumbel(rng.word((uint32_t)(col0 + imx))));
           best_i = col0 + imx;
           best_s = mx;
+          keep = ~(1u << imx);
         }
         // Pass 1, branch-free: sum of exp(s - mx) and the candidate mask.
         // Element i can beat the best key b only if 1 - u_i < exp(s_i - b).
@@ -512,30 +591,28 @@ draft_tile_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t cand = 0;
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const uint4 w4 = rng_quad(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
-                                    (uint32_t)((col0 >> 2) + q4));
+          const uint4 w4 = rng.quad((uint32_t)((col0 >> 2) + q4));
           const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int i = 4 * q4 + j;
             const float e = ex2_approx(fmaf(s[i], L2E, -mxl));
-            st += i < nvalid ? e : 0.0f;
+            st += e;
             // 1 - u, exactly: (2 m + 1) 2^-24 with m the complemented 23-bit field.
             const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~wv[j]) >> 9)), 0.99999994f);
-            cand |= (om < e * kf && i < nvalid && i != seeded) ? (1u << i) : 0u;
+            cand |= (om < e * kf) ? (1u << i) : 0u;
           }
         }
+        cand &= keep;
         lse_merge(run_m, run_s, mx, st);
         // Pass 2: exact keys of the (rare) candidates, in increasing vocab id.
         while (cand) {
           const int i = __ffs(cand) - 1;
           cand &= cand - 1;
-          const uint32_t w = rng_word(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT,
-                                      (uint32_t)(col0 + i));
           // s_i from this warp's staged score block (row `lane`, 128-byte swizzle)
           const float si =
               *(const float*)(sbox + lane * 128 + (((i >> 2) ^ (lane & 7)) << 4) + ((i & 3) << 2));
-          const float key = __fadd_rn(si, gumbel(w));
+          const float key = __fadd_rn(si, gumbel(rng.word((uint32_t)(col0 + i))));
           if (better(key, col0 + i, best, best_i)) {
             best = key;
             best_i = col0 + i;
@@ -637,24 +714,15 @@ int draft_tc_parts(int R, int V) {
   return slots;
 }
 
-cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, const void* W2,
-                             int R, int gamma, int V, int r, float* scores) {
+cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2, int R, int gamma,
+                             int V, int r, float* scores) {
   static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
-  const int Mt = (R + kTileM - 1) / kTileM;
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(plan->maps);
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)Mt * kTileM};
-    const cuuint64_t strides[1] = {(cuuint64_t)r * 2};
-    const cuuint32_t box[2] = {kChunkK, kTileM};
-    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
   {
     const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
     const cuuint64_t strides[1] = {(cuuint64_t)V * 2};
     const cuuint32_t box[2] = {64, kChunkK};
-    if (!encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2, dims, strides, box,
+    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -662,7 +730,7 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, co
     const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
     const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
     const cuuint32_t box[3] = {32, 1, 32};
-    if (!encode(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, U, dims, strides, box,
+    if (!encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, U, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
@@ -670,13 +738,13 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, co
     const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
     const cuuint64_t strides[2] = {(cuuint64_t)V * 4, (cuuint64_t)gamma * V * 4};
     const cuuint32_t box[3] = {32, 1, 32};
-    if (!encode(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box,
+    if (!encode(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_tile_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(draft_step_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -688,8 +756,10 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, co
   return cudaSuccess;
 }
 
-cudaError_t launch_draft_tile_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
-                                 DraftPartials part, int* status, cudaStream_t s) {
+cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
+                                 const int32_t* x0, const void* W1, const DraftPartials& prev,
+                                 const DraftPartials& cur, int32_t* x, float* logp, float* lse,
+                                 int* status, cudaStream_t s) {
   const int Mt = (plan.R + kTileM - 1) / kTileM;
   const int n_tiles = (plan.V + kTileN - 1) / kTileN;
   const int slots = draft_tc_parts(plan.R, plan.V);
@@ -706,10 +776,17 @@ cudaError_t launch_draft_tile_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.n_parts = slots;
   p.invT = invT;
   p.seed = seed;
-  p.pstats = part.stats;
-  p.pindex = part.index;
+  p.x0 = x0;
+  p.W1 = (const __nv_bfloat16*)W1;
+  p.prev_stats = prev.stats;
+  p.prev_index = prev.index;
+  p.pstats = cur.stats;
+  p.pindex = cur.index;
+  p.x = x;
+  p.logp = logp;
+  p.lse = lse;
   p.status = status;
-  draft_tile_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], p);
+  draft_step_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(maps[0], maps[1], maps[2], p);
   return cudaGetLastError();
 }
 

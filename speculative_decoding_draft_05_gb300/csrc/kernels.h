@@ -21,7 +21,7 @@ constexpr int kDraftTileN = 128;  // vocab columns per tile (both contraction pa
 
 // Workspace layout of dspark_draft_sample (byte offsets, 256-aligned).
 struct DraftWorkspace {
-  size_t status, a_rows, stats, index, total;
+  size_t status, a_rows, stats, index, stats2, index2, total;  // two partial buffers
 };
 DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype);
 
@@ -34,15 +34,19 @@ cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2,
                                    float* scores, DraftPartials p, cudaStream_t s);
 
 // bf16 tcgen05 contraction (TMA-fed, TMEM accumulators) + fused epilogue.
-// Tensor maps of one draft call (A, W2, U, scores), encoded once on the host.
+// Tensor maps of one draft call (W2, U, scores), encoded once on the host.
 struct DraftTcPlan {
-  alignas(64) unsigned char maps[4][128];
+  alignas(64) unsigned char maps[3][128];
   int R, gamma, V, r;
 };
-cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* A, const void* W2,
-                             int R, int gamma, int V, int r, float* scores);
-cudaError_t launch_draft_tile_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
-                                 DraftPartials p, int* status, cudaStream_t s);
+cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2, int R, int gamma,
+                             int V, int r, float* scores);
+// Step k (1-based): gathers A from x0 (k = 1) or from the combine of `prev`
+// (step k-1's partials, whose x/logp/lse it stores), writes `cur`.
+cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
+                                 const int32_t* x0, const void* W1, const DraftPartials& prev,
+                                 const DraftPartials& cur, int32_t* x, float* logp, float* lse,
+                                 int* status, cudaStream_t s);
 bool draft_tc_supported(int R, int V, int r);
 int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path
 
@@ -50,26 +54,34 @@ cudaError_t launch_draft_combine(DraftPartials p, int R, int gamma, int V, int r
                                  const void* W1, int dtype, void* A_next, int32_t* x, float* logp,
                                  float* lse, int* status, cudaStream_t s);
 
-cudaError_t launch_schedule(const float* conf, const double* sps, int R, int gamma, int32_t* ell,
-                            double* diag, int* status, cudaStream_t s);
+// Scheduler: rank-and-scatter sort into `sorted` (R * gamma keys), then the scan.
+size_t schedule_sorted_bytes(int R, int gamma);
+cudaError_t launch_schedule_rank(const float* conf, int R, int gamma, unsigned long long* sorted,
+                                 int* status, cudaStream_t s);
+cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double* sps, int R,
+                                 int gamma, int32_t* ell, double* diag, int* status,
+                                 cudaStream_t s);
 
 cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
                                float* lse_t_ws, int* acc_ws, int* status, cudaStream_t s);
 
+// The drawn token: verify_draw over vocab chunks, then verify_emit per request.
+int verify_draw_chunks(int V);
 cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
                                  const void* Z, int dtype, const int32_t* ell, int R, int gamma,
                                  int V, float invT, uint64_t seed, const float* lse_t_ws,
-                                 const int* acc_ws, int32_t* n_acc, int32_t* tokens,
-                                 int32_t* n_emit, float* cstar, float* lse_t, cudaStream_t s);
+                                 const int* acc_ws, float2* partials, int32_t* n_acc,
+                                 int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
+                                 cudaStream_t s);
 
 // Kernel kinds for the optional event timing (dspark_profile_*).
 enum KernelKind {
   kKindGather = 0,
   kKindDraftTile = 1,
   kKindDraftCombine = 2,
-  kKindSchedule = 3,
+  kKindSchedule = 3,  // both scheduler launches
   kKindVerifyRows = 4,
   kKindVerifyFinish = 5,
   kKindCount = 6

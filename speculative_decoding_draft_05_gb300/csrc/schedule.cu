@@ -7,14 +7,21 @@
 // SPS the engine's measured step-rate table.  Algorithm 1 extends prefixes in
 // survival order and stops at the first candidate that does not improve Theta.
 //
-// One CTA does the whole problem (R * gamma <= 16384 candidates): survival
-// products, a bitonic sort of 64-bit keys held 16 per thread in registers
-// (strides below 16 inside a thread, up to 256 by warp shuffles, larger ones
-// through shared memory), an exact int64 prefix sum of the fixed-point
-// survivals, the Theta test of every prefix in parallel and a block-wide
-// minimum to find the first non-improvement.
-// Every step is exact or IEEE-rounded in a fixed order, so the result is
-// bit-reproducible on any device.
+// Two launches, every step exact or IEEE-rounded in a fixed order, so the
+// result is bit-reproducible on any device:
+//   schedule_rank  (up to one CTA per SM) each CTA builds the sort key of every
+//                  candidate in shared memory.  Survival is non-increasing along
+//                  a request, so every request's gamma keys are already sorted;
+//                  a candidate's place in the global order is the sum over
+//                  requests of how many of their keys are smaller (a binary
+//                  search of <= 64 keys each), split across the CTA's warps.
+//                  Keys are unique, so these ranks are a permutation: each
+//                  candidate is written to its slot of the sorted array.
+//   schedule_scan  (one CTA) exact int64 prefix sum of the fixed-point
+//                  survivals in sorted order, the Theta test of every prefix in
+//                  parallel (an exact integer comparison of the products
+//                  tau * SPS, no floating point), a block-wide minimum for the
+//                  first non-improvement, and the per-request counts l_r.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,6 +31,7 @@ namespace {
 
 constexpr int kSchedThreads = 1024;
 constexpr int kMaxCandidates = 16384;
+constexpr int kPerThread = kMaxCandidates / kSchedThreads;  // 16
 
 __device__ __forceinline__ unsigned long long sort_key(float a, int j, int r) {
   // a >= 0: its bit pattern orders like the value.  Complementing it sorts by a
@@ -36,121 +44,143 @@ __device__ __forceinline__ float key_survival(unsigned long long key) {
   return __uint_as_float(~(unsigned)(key >> 32));
 }
 
-constexpr int kPerThread = 16;  // keys held in registers by each sorting thread
-
-__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int d) {
-  const unsigned lo = __shfl_xor_sync(0xffffffffu, (unsigned)v, d);
-  const unsigned hi = __shfl_xor_sync(0xffffffffu, (unsigned)(v >> 32), d);
-  return ((unsigned long long)hi << 32) | lo;
-}
-
+// a * 2^48 rounded to nearest, ties to even, for a in [0, 1], in integer
+// arithmetic: a = m 2^(E - 150) with a 24-bit m (E = 0: m 2^-149).
 __device__ __forceinline__ long long fixed_survival(unsigned long long key) {
-  return __float2ll_rn(__fmul_rn(key_survival(key), 281474976710656.0f));  // a * 2^48
+  const unsigned bits = ~(unsigned)(key >> 32);
+  const int E = (int)((bits >> 23) & 0xFF);
+  const unsigned long long m = E ? ((bits & 0x7FFFFFu) | 0x800000u) : (bits & 0x7FFFFFu);
+  const int sh = 102 - (E ? E : 1);  // a * 2^48 = m 2^-sh
+  if (sh <= 0) return (long long)(m << (-sh));
+  if (sh >= 25) return 0;  // below 1/2
+  const unsigned long long q0 = m >> sh, rem = m & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+  return (long long)(q0 + ((rem > half || (rem == half && (q0 & 1))) ? 1 : 0));
 }
 
-template <int STRIDE>
-__device__ __forceinline__ void reg_stage(unsigned long long (&k)[kPerThread], int base, int size) {
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    if (e & STRIDE) continue;
-    const int e2 = e | STRIDE;
-    const bool up = ((base + e) & size) == 0;
-    if ((k[e] > k[e2]) == up) {
-      const unsigned long long t = k[e];
-      k[e] = k[e2];
-      k[e2] = t;
-    }
+// Exact test of t_a * s_a > t_b * s_b for fixed-point t > 0 and step rates
+// s > 0 (finite doubles), in integer arithmetic only: s = m 2^e with an
+// integer m < 2^53, so each product is a 117-bit integer times 2^e; compare the
+// leading-bit positions, then the aligned 128-bit integers.  A step rate that
+// is not positive and finite flags the status word and counts as no
+// improvement.
+struct U128 {
+  unsigned long long hi, lo;
+};
+
+__device__ __forceinline__ bool split_rate(double s, unsigned long long& m, int& e) {
+  const unsigned long long bits = (unsigned long long)__double_as_longlong(s);
+  const int E = (int)((bits >> 52) & 0x7FF);
+  const unsigned long long F = bits & ((1ull << 52) - 1);
+  if ((bits >> 63) || E == 0x7FF || (E == 0 && F == 0)) return false;
+  m = E ? (F | (1ull << 52)) : F;
+  e = E ? E - 1075 : -1074;
+  return true;
+}
+
+__device__ __forceinline__ int bitlen(const U128& x) {
+  return x.hi ? 128 - __clzll((long long)x.hi) : 64 - __clzll((long long)x.lo);
+}
+
+__device__ __forceinline__ U128 shl(const U128& x, int d) {
+  if (d == 0) return x;
+  if (d >= 64) return U128{x.lo << (d - 64), 0ull};
+  return U128{(x.hi << d) | (x.lo >> (64 - d)), x.lo << d};
+}
+
+__device__ __forceinline__ bool exact_greater(long long ta, double sa, long long tb, double sb,
+                                              int* status) {
+  unsigned long long ma, mb;
+  int ea, eb;
+  if (!split_rate(sa, ma, ea) || !split_rate(sb, mb, eb)) {
+    flag_status(status, DSPARK_DEV_BAD_INPUT);
+    return false;
   }
+  const U128 pa{__umul64hi((unsigned long long)ta, ma), (unsigned long long)ta * ma};
+  const U128 pb{__umul64hi((unsigned long long)tb, mb), (unsigned long long)tb * mb};
+  const int na = bitlen(pa), nb = bitlen(pb);
+  if (na + ea != nb + eb) return na + ea > nb + eb;
+  const U128 xa = na < nb ? shl(pa, nb - na) : pa;
+  const U128 xb = nb < na ? shl(pb, na - nb) : pb;
+  return xa.hi != xb.hi ? xa.hi > xb.hi : xa.lo > xb.lo;
 }
 
-// n_sort = max(512, next power of two >= R * gamma); threads t < n_sort / 16 sort.
 __global__ void __launch_bounds__(kSchedThreads)
-schedule_kernel(const float* __restrict__ conf, const double* __restrict__ sps, int R, int gamma,
-                int n_sort, int32_t* __restrict__ ell, double* __restrict__ diag,
-                int* __restrict__ status) {
-  extern __shared__ unsigned long long keys[];  // [n_sort], staging for cross-warp stages
-  __shared__ long long warp_tot[kSchedThreads / 32];
-  __shared__ int stop_at;
+schedule_rank_kernel(const float* __restrict__ conf, int R, int gamma,
+                     unsigned long long* __restrict__ sorted, int* __restrict__ status) {
+  extern __shared__ unsigned long long keys[];  // [R][gamma], ascending along each request
   const int tid = threadIdx.x;
   const int n = R * gamma;
-  const int sorters = n_sort / kPerThread;
-
   for (int r = tid; r < R; r += kSchedThreads) {
-    ell[r] = 0;
     float a = 1.0f;
     for (int j = 0; j < gamma; ++j) {
       float c = conf[(size_t)r * gamma + j];
       if (!(c >= 0.0f) || c > 1.0f) {
-        flag_status(status, DSPARK_DEV_BAD_INPUT);
+        if (blockIdx.x == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
         c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
       }
       a = (j == 0) ? c : __fmul_rn(a, c);
       const float av = (a == 0.0f) ? 0.0f : a;  // canonical +0
-      keys[j * R + r] = sort_key(av, j, r);
+      keys[r * gamma + j] = sort_key(av, j, r);
     }
   }
-  for (int i = n + tid; i < n_sort; i += kSchedThreads) keys[i] = ~0ull;
-  if (tid == 0) stop_at = n + 1;
   __syncthreads();
-
-  // Bitonic sort, ascending.  Thread t holds elements [16 t, 16 t + 16).
-  unsigned long long k[kPerThread];
-  const bool sorter = tid < sorters;
-  const int base = tid * kPerThread;
-  if (sorter) {
-#pragma unroll
-    for (int e = 0; e < kPerThread; ++e) k[e] = keys[base + e];
-  }
-  for (int size = 2; size <= n_sort; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= 32 * kPerThread) {
-        // partner in another warp: exchange through shared memory
-        __syncthreads();
-        if (sorter) {
-#pragma unroll
-          for (int e = 0; e < kPerThread; ++e) keys[base + e] = k[e];
-        }
-        __syncthreads();
-        if (sorter) {
-#pragma unroll
-          for (int e = 0; e < kPerThread; ++e) {
-            const int i = base + e;
-            const unsigned long long v = keys[i ^ stride];
-            const bool up = (i & size) == 0, lower = (i & stride) == 0;
-            k[e] = (lower == up) ? (k[e] < v ? k[e] : v) : (k[e] > v ? k[e] : v);
-          }
-        }
-      } else if (stride >= kPerThread) {
-        // partner in another lane of the same warp
-        if (sorter) {
-          const int d = stride / kPerThread;
-#pragma unroll
-          for (int e = 0; e < kPerThread; ++e) {
-            const int i = base + e;
-            const unsigned long long v = shfl_xor_u64(k[e], d);
-            const bool up = (i & size) == 0, lower = (i & stride) == 0;
-            k[e] = (lower == up) ? (k[e] < v ? k[e] : v) : (k[e] > v ? k[e] : v);
-          }
-        }
-      } else if (sorter) {
-        // partner in this thread's registers (compile-time register indices)
-        switch (stride) {
-          case 8: reg_stage<8>(k, base, size); break;
-          case 4: reg_stage<4>(k, base, size); break;
-          case 2: reg_stage<2>(k, base, size); break;
-          default: reg_stage<1>(k, base, size); break;
-        }
+  // Blocks of 32 candidates, one per lane; warp w counts, for every lane's
+  // candidate, the keys below it in the lists of requests r = w, w + 32, ...
+  // (all lanes probe the same list at once: no bank conflicts).
+  __shared__ int part[kSchedThreads / 32][33];
+  const int lane = tid & 31, warp = tid >> 5;
+  const int blocks = (n + 31) / 32;
+  for (int blk = blockIdx.x; blk < blocks; blk += gridDim.x) {
+    const int e = blk * 32 + lane;
+    const unsigned long long key = e < n ? keys[e] : ~0ull;
+    int below = 0;
+    for (int r = warp; r < R; r += kSchedThreads / 32) {
+      const unsigned long long* list = keys + r * gamma;
+      int lo = 0, hi = gamma;  // first index with list[idx] >= key
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (list[mid] < key) lo = mid + 1;
+        else hi = mid;
       }
+      below += lo;
     }
+    part[warp][lane] = below;
+    __syncthreads();
+    if (warp == 0) {
+      int rank = 0;
+#pragma unroll 8
+      for (int w = 0; w < kSchedThreads / 32; ++w) rank += part[w][lane];
+      if (e < n) sorted[rank] = key;
+    }
+    __syncthreads();
   }
+}
 
-  // Exclusive prefix of the fixed-point survivals over the threads' chunks.
+__global__ void __launch_bounds__(kSchedThreads)
+schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double* __restrict__ sps,
+                     int R, int gamma, int32_t* __restrict__ ell, double* __restrict__ diag,
+                     int* __restrict__ status) {
+  __shared__ long long warp_tot[kSchedThreads / 32];
+  __shared__ int stop_at;
+  const int tid = threadIdx.x;
+  const int n = R * gamma;
+  const int base = tid * kPerThread;
+  for (int r = tid; r < R; r += kSchedThreads) ell[r] = 0;
+  if (tid == 0) stop_at = n + 1;
+
+  // Coalesced load of the sorted keys into shared memory, then 16 contiguous
+  // keys per thread.
+  extern __shared__ unsigned long long stage[];  // [kMaxCandidates]
+  for (int i = tid; i < kMaxCandidates; i += kSchedThreads) stage[i] = i < n ? sorted[i] : ~0ull;
+  __syncthreads();
+  unsigned long long k[kPerThread];
   long long local = 0;
-  if (sorter) {
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e)
-      if (base + e < n) local += fixed_survival(k[e]);
+  for (int e = 0; e < kPerThread; ++e) {
+    k[e] = stage[base + e];
+    if (base + e < n) local += fixed_survival(k[e]);
   }
+  // Exclusive prefix of the fixed-point survivals over the threads' chunks.
   const int lane = tid & 31, warp = tid >> 5;
   long long incl = local;
 #pragma unroll
@@ -175,31 +205,26 @@ schedule_kernel(const float* __restrict__ conf, const double* __restrict__ sps, 
   // Theta test of every candidate (0-based index i, 1-based number i + 1):
   // before it B = R + i and tau = R + P_i; after it B = R + i + 1.
   const long long tau0 = (long long)R << 48;
-  if (sorter) {
-    long long run = run0;
+  long long run = run0;
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e) {
-      const int i = base + e;
-      if (i < n) {
-        const long long tau_prev = tau0 + run;
-        run += fixed_survival(k[e]);
-        const double th_prev = __dmul_rn(__ll2double_rn(tau_prev) * 0x1p-48, sps[R + i]);
-        const double th_i = __dmul_rn(__ll2double_rn(tau0 + run) * 0x1p-48, sps[R + i + 1]);
-        if (!(th_i > th_prev)) atomicMin(&stop_at, i + 1);
-      }
+  for (int e = 0; e < kPerThread; ++e) {
+    const int i = base + e;
+    if (i < n) {
+      const long long tau_prev = tau0 + run;
+      run += fixed_survival(k[e]);
+      if (!exact_greater(tau0 + run, sps[R + i + 1], tau_prev, sps[R + i], status))
+        atomicMin(&stop_at, i + 1);
     }
   }
   __syncthreads();
   const int taken = stop_at - 1;  // candidates 0..taken-1 were taken
-  if (sorter) {
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e)
-      if (base + e < taken) atomicAdd(&ell[(int)(k[e] & 0xffffu)], 1);
-  }
+  for (int e = 0; e < kPerThread; ++e)
+    if (base + e < taken) atomicAdd(&ell[(int)(k[e] & 0xffffu)], 1);
   if (diag) {
     // tau after the taken candidates: the owner of index taken-1 finishes its chunk's sum.
-    const bool owner = (taken == 0) ? (tid == 0)
-                                    : (sorter && base <= taken - 1 && taken - 1 < base + kPerThread);
+    const bool owner =
+        (taken == 0) ? (tid == 0) : (base <= taken - 1 && taken - 1 < base + kPerThread);
     if (owner) {
       long long tau = tau0 + (taken == 0 ? 0ll : run0);
 #pragma unroll
@@ -213,19 +238,57 @@ schedule_kernel(const float* __restrict__ conf, const double* __restrict__ sps, 
   }
 }
 
+int sm_count_sched() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
 }  // namespace
 
-cudaError_t launch_schedule(const float* conf, const double* sps, int R, int gamma, int32_t* ell,
-                            double* diag, int* status, cudaStream_t s) {
+size_t schedule_sorted_bytes(int R, int gamma) {
+  return (size_t)R * gamma * sizeof(unsigned long long);
+}
+
+cudaError_t launch_schedule_rank(const float* conf, int R, int gamma, unsigned long long* sorted,
+                                 int* status, cudaStream_t s) {
   const int n = R * gamma;
   if (n > kMaxCandidates) return cudaErrorInvalidValue;
-  int n_sort = 32 * kPerThread;
-  while (n_sort < n) n_sort <<= 1;
-  const size_t smem = (size_t)n_sort * sizeof(unsigned long long);
-  cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  schedule_kernel<<<1, kSchedThreads, smem, s>>>(conf, sps, R, gamma, n_sort, ell, diag, status);
+  const size_t smem = (size_t)n * sizeof(unsigned long long);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(schedule_rank_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kMaxCandidates * sizeof(unsigned long long)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int blocks = (n + 31) / 32;  // 32 candidates per CTA pass
+  const int sms = sm_count_sched();
+  if (blocks > sms) blocks = sms;
+  if (blocks < 1) blocks = 1;
+  schedule_rank_kernel<<<blocks, kSchedThreads, smem, s>>>(conf, R, gamma, sorted, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double* sps, int R,
+                                 int gamma, int32_t* ell, double* diag, int* status,
+                                 cudaStream_t s) {
+  if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
+  const size_t smem = kMaxCandidates * sizeof(unsigned long long);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(schedule_scan_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  schedule_scan_kernel<<<1, kSchedThreads, smem, s>>>(sorted, sps, R, gamma, ell, diag, status);
   return cudaGetLastError();
 }
 

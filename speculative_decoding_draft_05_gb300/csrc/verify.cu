@@ -9,14 +9,15 @@
 // Generation" (notes), "배경": accept the longest prefix.
 //
 // Two launches:
-//   verify_rows   one CTA per scheduled row (r, j), j <= l_r: LSE of Z_j / T,
+//   verify_rows   a CTA per scheduled row (r, j), j <= l_r: LSE of Z_j / T,
 //                 c*_j = sum_v min(p^d_j, p^t_j), and the accept test of x_j.
 //                 The Z row is streamed twice (the second pass hits L2) and
 //                 the score row once, with 16-byte vector loads.
-//   verify_finish one CTA per request: first rejection n, then the Gumbel-max
-//                 draw from norm(max(0, p^t - p^d)) at row n + 1 or from p^t at
-//                 the bonus row l + 1; writes tokens, n_acc, n_emit and the NaN
-//                 padding of c* / LSE^t beyond l.
+//   verify_draw   (vocab chunks x requests) CTAs: first rejection n, then the
+//                 Gumbel-max draw from norm(max(0, p^t - p^d)) at row n + 1 or
+//                 from p^t at the bonus row l + 1, one partial per chunk;
+//   verify_emit   one CTA per request: merges the partials, writes tokens,
+//                 n_acc, n_emit and the NaN padding of c* / LSE^t beyond l.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -26,7 +27,7 @@ namespace dspark {
 
 namespace {
 
-constexpr int kVerifyThreads = 256;
+constexpr int kVerifyThreads = 512;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -101,6 +102,8 @@ __device__ __forceinline__ float block_lse(float m, float s, float* rm, float* r
   return out;
 }
 
+// Block-wide argmax over NWARPS warps (rk, ri hold NWARPS entries).
+template <int NWARPS>
 __device__ __forceinline__ void block_argmax(float& key, int& idx, float* rk, int* ri) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   warp_argmax(key, idx);
@@ -110,8 +113,8 @@ __device__ __forceinline__ void block_argmax(float& key, int& idx, float* rk, in
   }
   __syncthreads();
   if (threadIdx.x < 32) {
-    float k2 = lane < kWarps ? rk[lane] : -INFINITY;
-    int i2 = lane < kWarps ? ri[lane] : 0x7fffffff;
+    float k2 = lane < NWARPS ? rk[lane] : -INFINITY;
+    int i2 = lane < NWARPS ? ri[lane] : 0x7fffffff;
     warp_argmax(k2, i2);
     if (lane == 0) {
       rk[0] = k2;
@@ -138,14 +141,16 @@ template <typename T>
 __global__ void __launch_bounds__(kVerifyThreads)
 verify_rows_kernel(const int32_t* __restrict__ x, const float* __restrict__ logp,
                    const float* __restrict__ lse, const float* __restrict__ scores,
-                   const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
-                   float invT, uint64_t seed, float* __restrict__ cstar,
+                   const T* __restrict__ Z, const int32_t* __restrict__ ell, int R, int gamma,
+                   int V, float invT, uint64_t seed, float* __restrict__ cstar,
                    float* __restrict__ lse_t_ws, int* __restrict__ acc_ws,
                    int* __restrict__ status) {
   __shared__ float rm[kWarps], rs[kWarps];
-  const int j = blockIdx.x + 1, r = blockIdx.y;
+  const int items = R * gamma;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  const int r = item / gamma, j = item - r * gamma + 1;
   const int L = clamp_ell(ell, r, gamma, status, j == 1 && threadIdx.x == 0);
-  if (j > L) return;
+  if (j > L) continue;  // uniform across the CTA
   const int groups = V >> 3;
   const T* z = Z + ((size_t)r * (gamma + 1) + (j - 1)) * V;
   const float* srow = scores + ((size_t)r * gamma + (j - 1)) * V;
@@ -195,83 +200,113 @@ verify_rows_kernel(const int32_t* __restrict__ x, const float* __restrict__ logp
     cstar[(size_t)r * gamma + (j - 1)] = cs;
     lse_t_ws[(size_t)r * (gamma + 1) + (j - 1)] = Lt;
   }
+  }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kVerifyThreads)
-verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
-                     const float* __restrict__ scores, const T* __restrict__ Z,
-                     const int32_t* __restrict__ ell, int gamma, int V, float invT, uint64_t seed,
-                     const float* __restrict__ lse_t_ws, const int* __restrict__ acc_ws,
-                     int32_t* __restrict__ n_acc, int32_t* __restrict__ tokens,
-                     int32_t* __restrict__ n_emit, float* __restrict__ cstar,
-                     float* __restrict__ lse_t_out) {
-  __shared__ float rk[kWarps];
-  __shared__ int ri[kWarps];
-  const int r = blockIdx.x;
-  const int L = clamp_ell(ell, r, gamma, nullptr, false);
+// Leading accepts of request r (the first rejection is at row n + 1).
+__device__ __forceinline__ int leading_accepts(const int* __restrict__ acc_ws, int r, int gamma,
+                                               int L) {
   int n = 0;
   while (n < L && acc_ws[(size_t)r * gamma + n]) ++n;
-  const int groups = V >> 3;
+  return n;
+}
+
+constexpr int kDrawThreads = 256;
+constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 ids)
+
+// Gumbel-max over one chunk of the drawn row, with an exact-preserving filter:
+// element v can beat the running best key b only if -ln u_v < w_v exp(-b),
+// where w_v is its weight (the p^t mass for the bonus draw, the residual for
+// the rejection draw).  Since -ln u >= 1 - u, elements with 1 - u_v >= w_v e^-b
+// (0.1% slack) are skipped without the logarithms; the first element a thread
+// meets seeds b.  Writes the chunk's (best key, index) partial.
+template <typename T>
+__global__ void __launch_bounds__(kDrawThreads)
+verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
+                   const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
+                   float invT, uint64_t seed, const float* __restrict__ lse_t_ws,
+                   const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks) {
+  __shared__ float rk[kDrawThreads / 32];
+  __shared__ int ri[kDrawThreads / 32];
+  __shared__ int s_n;
+  const int r = blockIdx.y, chunk = blockIdx.x;
+  const int L = clamp_ell(ell, r, gamma, nullptr, false);
+  if (threadIdx.x == 0) s_n = leading_accepts(acc_ws, r, gamma, L);
+  __syncthreads();
+  const int n = s_n;
   const bool residual = n < L;
   const int row = n + 1;  // 1-based position of the drawn token
   const T* z = Z + ((size_t)r * (gamma + 1) + (row - 1)) * V;
-
-  // Gumbel-max with an exact-preserving filter: element v can beat the running
-  // best key b only if -ln u_v < w_v exp(-b), where w_v is its weight (p^t row
-  // mass for the bonus draw, the residual for the rejection draw); since
-  // -ln u >= 1 - u, elements with 1 - u_v >= w_v exp(-b) (0.1% slack) are
-  // skipped without evaluating the logarithms.
+  const int groups = V >> 3;
+  const int g0 = chunk * kDrawGroups, g1 = min(groups, g0 + kDrawGroups);
   const float L2E = 1.4426950408889634f;
+  const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
   float best = -INFINITY;
   int idx = 0x7fffffff;
   if (residual) {
     const float* srow = scores + ((size_t)r * gamma + (row - 1)) * V;
     const float ld = lse[(size_t)r * gamma + (row - 1)];
     const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
-    float kb = INFINITY;  // 1.001 exp(-best)
-    for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
-      float e[8], s[8];
+    for (int g = g0 + threadIdx.x; g < g1; g += kDrawThreads) {
+      float e[8], sc[8];
       load8(z, g, e);
-      load8(srow, g, s);
-      const uint4 w0 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g);
-      const uint4 w1 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g + 1);
+      load8(srow, g, sc);
+      const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
       const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const float kb = best == -INFINITY ? INFINITY : ex2_approx(-best * L2E) * 1.001f;
+      uint32_t cand = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float ra = __expf(e[i] * invT - Lt) - __expf(s[i] - ld);  // approximate residual
+        const float ra = __expf(e[i] * invT - Lt) - __expf(sc[i] - ld);  // approximate residual
         const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
-        if (ra > -1e-6f && (best == -INFINITY || om < fmaxf(ra, 1e-6f) * kb)) {
-          const float res = expf(e[i] * invT - Lt) - expf(s[i] - ld);
+        cand |= (ra > -1e-6f && om < fmaxf(ra, 1e-6f) * kb) ? (1u << i) : 0u;
+      }
+      if (cand) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (!(cand & (1u << i))) continue;
+          const float res = expf(e[i] * invT - Lt) - expf(sc[i] - ld);
           if (res > 0.0f) {
             const float key = __fadd_rn(logf(res), gumbel(w[i]));
             if (better(key, 8 * g + i, best, idx)) {
               best = key;
               idx = 8 * g + i;
-              kb = ex2_approx(-best * L2E) * 1.001f;
             }
           }
         }
       }
     }
-    block_argmax(best, idx, rk, ri);
-  }
-  if (!residual || best == -INFINITY) {
-    // bonus row l + 1, or a residual that is zero everywhere: draw from p^t
-    best = -INFINITY;
-    idx = 0x7fffffff;
-    for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
+  } else {
+    for (int g = g0 + threadIdx.x; g < g1; g += kDrawThreads) {
       float e[8];
       load8(z, g, e);
-      const uint4 w0 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g);
-      const uint4 w1 = rng_quad(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, 2 * g + 1);
+      const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
       const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      if (best == -INFINITY) {  // seed with the group's largest logit (lowest such id)
+        float em = e[0];
+        uint32_t wm = w[0];
+        int im = 0;
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+          if (e[i] > em) {
+            em = e[i];
+            wm = w[i];
+            im = i;
+          }
+        best = __fadd_rn(em * invT, gumbel(wm));
+        idx = 8 * g + im;
+      }
+      uint32_t cand = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float zt = e[i] * invT;
         const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
-        if (best == -INFINITY || om < ex2_approx((zt - best) * L2E) * 1.001f) {
-          const float key = __fadd_rn(zt, gumbel(w[i]));
+        cand |= (om < ex2_approx((e[i] * invT - best) * L2E) * 1.001f) ? (1u << i) : 0u;
+      }
+      if (cand) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (!(cand & (1u << i))) continue;
+          const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
           if (better(key, 8 * g + i, best, idx)) {
             best = key;
             idx = 8 * g + i;
@@ -279,9 +314,64 @@ verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ ls
         }
       }
     }
-    block_argmax(best, idx, rk, ri);
   }
+  block_argmax<kDrawThreads / 32>(best, idx, rk, ri);
+  if (threadIdx.x == 0)
+    partials[(size_t)r * n_chunks + chunk] = make_float2(best, __int_as_float(idx));
+}
 
+// Per request: merge the chunks' partials into the drawn token (for a residual
+// that is zero everywhere, draw from p^t over the whole row instead), then
+// write tokens, n_acc, n_emit and the NaN padding of c* / LSE^t beyond l.
+template <typename T>
+__global__ void __launch_bounds__(kVerifyThreads)
+verify_emit_kernel(const int32_t* __restrict__ x, const T* __restrict__ Z,
+                   const int32_t* __restrict__ ell, int gamma, int V, float invT, uint64_t seed,
+                   const float* __restrict__ lse_t_ws, const int* __restrict__ acc_ws,
+                   const float2* __restrict__ partials, int n_chunks, int32_t* __restrict__ n_acc,
+                   int32_t* __restrict__ tokens, int32_t* __restrict__ n_emit,
+                   float* __restrict__ cstar, float* __restrict__ lse_t_out) {
+  __shared__ float rk[kWarps];
+  __shared__ int ri[kWarps];
+  __shared__ int s_n;
+  const int r = blockIdx.x;
+  const int L = clamp_ell(ell, r, gamma, nullptr, false);
+  if (threadIdx.x == 0) s_n = leading_accepts(acc_ws, r, gamma, L);
+  __syncthreads();
+  const int n = s_n;
+  const int row = n + 1;
+  float best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int c = threadIdx.x; c < n_chunks; c += kVerifyThreads) {
+    const float2 p = partials[(size_t)r * n_chunks + c];
+    const int pi = __float_as_int(p.y);
+    if (better(p.x, pi, best, idx)) {
+      best = p.x;
+      idx = pi;
+    }
+  }
+  block_argmax<kWarps>(best, idx, rk, ri);
+  if (best == -INFINITY) {
+    // Residual zero everywhere (p^t = p^d numerically): draw from p^t.
+    const T* z = Z + ((size_t)r * (gamma + 1) + (row - 1)) * V;
+    const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
+    idx = 0x7fffffff;
+    for (int g = threadIdx.x; g < (V >> 3); g += kVerifyThreads) {
+      float e[8];
+      load8(z, g, e);
+      const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
+      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
+        if (better(key, 8 * g + i, best, idx)) {
+          best = key;
+          idx = 8 * g + i;
+        }
+      }
+    }
+    block_argmax<kWarps>(best, idx, rk, ri);
+  }
   int32_t* trow = tokens + (size_t)r * (gamma + 1);
   for (int t = threadIdx.x; t < gamma + 1; t += kVerifyThreads) {
     int32_t out = -1;
@@ -301,35 +391,60 @@ verify_finish_kernel(const int32_t* __restrict__ x, const float* __restrict__ ls
 
 }  // namespace
 
+int verify_sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
 cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
                                float* lse_t_ws, int* acc_ws, int* status, cudaStream_t s) {
-  dim3 grid(gamma, R);
+  int grid = R * gamma;
+  const int cap = 4 * verify_sm_count();  // 4 CTAs of 512 threads per SM
+  if (grid > cap) grid = cap;
   if (dtype == DSPARK_BF16)
     verify_rows_kernel<__nv_bfloat16><<<grid, kVerifyThreads, 0, s>>>(
-        x, logp, lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, cstar, lse_t_ws,
-        acc_ws, status);
+        x, logp, lse, scores, (const __nv_bfloat16*)Z, ell, R, gamma, V, invT, seed, cstar,
+        lse_t_ws, acc_ws, status);
   else
     verify_rows_kernel<float><<<grid, kVerifyThreads, 0, s>>>(
-        x, logp, lse, scores, (const float*)Z, ell, gamma, V, invT, seed, cstar, lse_t_ws, acc_ws,
-        status);
+        x, logp, lse, scores, (const float*)Z, ell, R, gamma, V, invT, seed, cstar, lse_t_ws,
+        acc_ws, status);
   return cudaGetLastError();
 }
+
+int verify_draw_chunks(int V) { return ((V >> 3) + kDrawGroups - 1) / kDrawGroups; }
 
 cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
                                  const void* Z, int dtype, const int32_t* ell, int R, int gamma,
                                  int V, float invT, uint64_t seed, const float* lse_t_ws,
-                                 const int* acc_ws, int32_t* n_acc, int32_t* tokens,
-                                 int32_t* n_emit, float* cstar, float* lse_t, cudaStream_t s) {
-  if (dtype == DSPARK_BF16)
-    verify_finish_kernel<__nv_bfloat16><<<R, kVerifyThreads, 0, s>>>(
-        x, lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, n_acc,
-        tokens, n_emit, cstar, lse_t);
-  else
-    verify_finish_kernel<float><<<R, kVerifyThreads, 0, s>>>(
-        x, lse, scores, (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, n_acc, tokens,
-        n_emit, cstar, lse_t);
+                                 const int* acc_ws, float2* partials, int32_t* n_acc,
+                                 int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
+                                 cudaStream_t s) {
+  const int chunks = verify_draw_chunks(V);
+  dim3 grid(chunks, R);
+  if (dtype == DSPARK_BF16) {
+    verify_draw_kernel<__nv_bfloat16><<<grid, kDrawThreads, 0, s>>>(
+        lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials,
+        chunks);
+    verify_emit_kernel<__nv_bfloat16><<<R, kVerifyThreads, 0, s>>>(
+        x, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials, chunks,
+        n_acc, tokens, n_emit, cstar, lse_t);
+  } else {
+    verify_draw_kernel<float><<<grid, kDrawThreads, 0, s>>>(lse, scores, (const float*)Z, ell, gamma,
+                                                            V, invT, seed, lse_t_ws, acc_ws,
+                                                            partials, chunks);
+    verify_emit_kernel<float><<<R, kVerifyThreads, 0, s>>>(x, (const float*)Z, ell, gamma, V, invT,
+                                                           seed, lse_t_ws, acc_ws, partials, chunks,
+                                                           n_acc, tokens, n_emit, cstar, lse_t);
+  }
   return cudaGetLastError();
 }
 

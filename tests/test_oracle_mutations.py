@@ -30,8 +30,12 @@ MUTATIONS = [
     ("emitted token is the rejected draft", "t[n] = tok;",
      "t[n] = J->x[(size_t)i * g + (n < g ? n : g - 1)];"),
     ("max instead of min in c*", "cs += pd < pt ? pd : pt;", "cs += pd > pt ? pd : pt;"),
-    ("scheduler never stops", "if (!(theta > theta_prev)) break;",
-     "if (!(theta >= theta_prev)) continue;"),
+    ("scheduler never stops", "if (!exact_greater(tau_i, sps[B + 1], tau, sps[B])) break;",
+     "if (0) break;"),
+    ("scheduler comparison reversed", "if (!exact_greater(tau_i, sps[B + 1], tau, sps[B])) break;",
+     "if (!exact_greater(tau, sps[B], tau_i, sps[B + 1])) break;"),
+    ("step rate of the wrong batch size", "if (!exact_greater(tau_i, sps[B + 1], tau, sps[B])) break;",
+     "if (!exact_greater(tau_i, sps[B], tau, sps[B])) break;"),
     ("survival not a product", "a = (j == 0) ? cj : a * cj;", "a = cj;"),
     ("bonus row one too early", "const int row = L + 1;", "const int row = L > 0 ? L : 1;"),
     ("draft stream keyed by the wrong position",
