@@ -254,14 +254,16 @@ class Round:
                                         x=self.x, logp=self.logp, lse=self.lse, scores=self.scores,
                                         workspace=self.ws_d)
 
-    def step(self, seed=None):
-        """One round; `seed` keys the round's Philox draws (default: the input seed)."""
-        i = self.inp
+    def step(self, seed=None, inputs=None):
+        """One round; `seed` keys the round's Philox draws (default: the input seed);
+        `inputs` is a list like input_tensors() (default: the resident inputs)."""
+        U, W1, W2, x0, conf, sps, Z = self.input_tensors() if inputs is None else inputs
         d = self.dspark
         seed = self.seed if seed is None else seed
-        self.draft(seed)
-        d.dspark_schedule(i["conf"], i["sps"], ell=self.ell, diag=self.diag, workspace=self.ws_s)
-        d.dspark_verify(self.x, self.logp, self.lse, self.scores, self.Z, self.ell, self.w.T, seed,
+        d.dspark_draft_sample(U, W1, W2, x0, self.w.T, seed, x=self.x, logp=self.logp, lse=self.lse,
+                              scores=self.scores, workspace=self.ws_d)
+        d.dspark_schedule(conf, sps, ell=self.ell, diag=self.diag, workspace=self.ws_s)
+        d.dspark_verify(self.x, self.logp, self.lse, self.scores, Z, self.ell, self.w.T, seed,
                         n_acc=self.n_acc, tokens=self.tokens, n_emit=self.n_emit, cstar=self.cstar,
                         lse_t=self.lse_t, workspace=self.ws_v)
 
@@ -418,26 +420,63 @@ def run_ours(args, w, rank, world, local):
         emitted += int(rnd.n_emit.sum().item())
     accepted = sum_over_ranks(float(emitted), world, device) / (ms_max / 1e3)
 
-    # ---- e2e through the C-ABI with pinned host buffers
+    # ---- e2e through the C-ABI with pinned host buffers: every step copies its
+    # inputs host->device and reads its result back; step i+1's copies (two
+    # copy streams, chunked) overlap step i's compute on double-buffered inputs.
     host_in = [t.cpu().pin_memory() for t in rnd.input_tensors()]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in rnd.result_tensors()]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     e2e_steps = max(3, min(args.steps, 10))
+    sets = [rnd.input_tensors(), [t.clone() for t in rnd.input_tensors()]]
+    copy_streams = [torch.cuda.Stream(device), torch.cuda.Stream(device)]
+    chunk = 256 << 20
+
+    def issue_copies(dst_set):
+        n = 0
+        for dst, src in zip(dst_set, host_in):
+            flat_d, flat_s = dst.view(-1), src.view(-1)
+            step_el = max(1, chunk // dst.element_size())
+            for o in range(0, flat_d.numel(), step_el):
+                with torch.cuda.stream(copy_streams[n % 2]):
+                    flat_d[o:o + step_el].copy_(flat_s[o:o + step_el], non_blocking=True)
+                n += 1
+        evs = []
+        for cs in copy_streams:
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            evs.append(ev)
+        return evs
+
     barrier(world)
     torch.cuda.synchronize(device)
     t0 = time.perf_counter()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for sd in seeds[:e2e_steps]:
-        for dst, src in zip(rnd.input_tensors(), host_in):
-            dst.copy_(src, non_blocking=True)
-        rnd.step(sd)
+    for cs in copy_streams:
+        cs.wait_event(e0)
+    copied = issue_copies(sets[0])
+    done = [None, None]
+    for i, sd in enumerate(seeds[:e2e_steps]):
+        for ev in copied:
+            stream.wait_event(ev)
+        nxt = None
+        if i + 1 < e2e_steps:
+            if done[(i + 1) % 2] is not None:  # that set's previous round must be finished
+                for cs in copy_streams:
+                    cs.wait_event(done[(i + 1) % 2])
+            nxt = issue_copies(sets[(i + 1) % 2])
+        rnd.step(sd, inputs=sets[i % 2])
         for dst, src in zip(host_out, rnd.result_tensors()):
             dst.copy_(src, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        done[i % 2] = ev
+        copied = nxt
     e1.record(stream)
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
+    del sets
     e2e_ms = max(e0.elapsed_time(e1), 1e3 * wall)
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     e2e_value = w.R * w.gamma * e2e_steps * world / (e2e_ms / 1e3)

@@ -228,7 +228,7 @@ int dspark_read_device_status(const void* workspace, void* stream, int32_t* out)
  * counts keep counting beyond that).
  * ---------------------------------------------------------------------- */
 enum {
-  DSPARK_KERNEL_GATHER = 0,         /* anchor gather W1[x0] */
+  DSPARK_KERNEL_PREPARE = 0,        /* draft set-up: W2 transpose (bf16) or anchor gather (fp32) */
   DSPARK_KERNEL_DRAFT_TILE = 1,     /* draft contraction + fused epilogue (gamma launches) */
   DSPARK_KERNEL_DRAFT_COMBINE = 2,  /* per-row combine + next gather (gamma launches) */
   DSPARK_KERNEL_SCHEDULE = 3,

@@ -35,7 +35,8 @@ DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype)
   w.index = align256(w.stats + (size_t)R * tiles * sizeof(float4));
   w.stats2 = align256(w.index + (size_t)R * tiles * sizeof(int));
   w.index2 = align256(w.stats2 + (size_t)R * tiles * sizeof(float4));
-  w.total = align256(w.index2 + (size_t)R * tiles * sizeof(int));
+  w.w2t = align256(w.index2 + (size_t)R * tiles * sizeof(int));  // bf16 W2^T [V, r]
+  w.total = align256(w.w2t + (dtype == DSPARK_BF16 ? (size_t)V * r * 2 : 0));
   return w;
 }
 
@@ -152,8 +153,13 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   if (tc) {
     // Tensor-core path: each step gathers its A tile itself; partials alternate
     // between two buffers; one combine after the last step.
+    void* W2T = ws + L.w2t;
+    prof_begin(kKindPrepare, s);
+    e = launch_transpose_w2(W2, r, V, W2T, s);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
     DraftTcPlan plan;
-    e = prepare_draft_tc(&plan, U, W2, R, gamma, V, r, scores);
+    e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
     if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
     const DraftPartials buf[2] = {p, p2};
     for (int k = 1; k <= gamma; ++k) {
@@ -170,7 +176,7 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
     if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
     return DSPARK_OK;
   }
-  prof_begin(kKindGather, s);
+  prof_begin(kKindPrepare, s);
   e = launch_gather_anchor(W1, x0, R, V, r, dtype, A, status, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "gather_anchor");

@@ -21,11 +21,14 @@
 //     also yields step k-1's x, logp and lse (stored by the slot-0 CTAs).  So
 //     consecutive steps need no separate combine launch; one combine follows
 //     the last step.
-//   * warp 16 (producer): TMA of W2 chunks [64 x 128] into a 3-stage ring.
+//   * warp 16 (producer): TMA of W2^T chunks [128 vocab rows x 64 K] into a
+//     3-stage ring.  W2^T (K-major) is written once per draft call by
+//     transpose_w2_kernel, so each vocab tile's B operand is one contiguous
+//     128 x r block instead of r rows strided V apart.
 //   * warp 17 (MMA): allocates 256 TMEM columns (two 128 x 128 fp32
 //     accumulators) and issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
-//     M = 128, N = 128, K = 16) from shared-memory descriptors: A K-major,
-//     W2 MN-major, both 128-byte swizzled.
+//     M = 128, N = 128, K = 16) from shared-memory descriptors: A and W2^T both
+//     K-major, 128-byte swizzled.
 //   * warps 0..15 (epilogue): warp w reads TMEM lanes 32 (w % 4) .. +31 (its
 //     rows) and columns 32 (w / 4) .. +31 of the tile.  Per tile it TMA-loads
 //     its [32 x 32] block of U_k, computes s, stages it in swizzled shared
@@ -73,7 +76,8 @@ constexpr int kOffU = kOffB + kStages * kBChunkBytes;               // 112 KB
 constexpr int kOffS = kOffU + kEpiWarps * kUBoxBytes;               // 144 KB
 constexpr int kOffMerge = kOffS + kEpiWarps * kSBoxBytes;           // 208 KB
 constexpr int kMergeBytes = 5 * 4 * kTileM * 4;                     // 10 KB
-constexpr int kOffBar = kOffMerge + kMergeBytes;
+constexpr int kOffRowBest = kOffMerge + kMergeBytes;                // [128 rows][4 groups] fp32
+constexpr int kOffBar = kOffRowBest + kTileM * 4 * 4;
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + kEpiWarps + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack for 1024 alignment
 
@@ -234,13 +238,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, A K-major, B MN-major.
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
   return (1u << 4)                        // D format: F32
          | (1u << 7)                      // A format: BF16
          | (1u << 10)                     // B format: BF16
          | (0u << 15)                     // A K-major
-         | (1u << 16)                     // B MN-major
+         | (0u << 16)                     // B K-major
          | ((uint32_t)(N >> 3) << 17)     // N / 8
          | ((uint32_t)(M >> 4) << 24);    // M / 16
 }
@@ -253,6 +257,45 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Pass 1 of the draft epilogue over one warp's 32 columns of a row, branch-free:
+// returns the candidate mask and sets st = sum exp(s - mx).  Element i can beat
+// the running best key b only if 1 - u_i < y_i = exp(s_i - b); with
+// f_i = 1 + (w_i >> 9) 2^-23 = u_i + 1 - 2^-24 that is f_i > 2 - 2^-24 - y_i,
+// tested conservatively as f_i >= fl(2 - 1.001 y_i) (kf = 1.001 exp(mx - b)).
+// The scores are read back from the row's staged block (128-byte swizzle), one
+// 16-byte quad at a time.  MASKED: only the first nvalid columns take part.
+template <bool MASKED>
+__device__ __forceinline__ uint32_t filter_pass(const uint8_t* srow, int lane,
+                                                const PhiloxStream& rng, int col0, float mxl,
+                                                float kf, int nvalid, float& st) {
+  const float L2E = 1.4426950408889634f;
+  float sum = 0.0f;
+  uint32_t cand = 0;
+#pragma unroll 2
+  for (int q4 = 0; q4 < 8; ++q4) {
+    const float4 sv = *(const float4*)(srow + ((q4 ^ (lane & 7)) << 4));
+    const uint4 w4 = rng.quad((uint32_t)((col0 >> 2) + q4));
+    const float sq[4] = {sv.x, sv.y, sv.z, sv.w};
+    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 4 * q4 + j;
+      const float e = ex2_approx(fmaf(sq[j], L2E, -mxl));
+      const float f = __uint_as_float(0x3F800000u | (wv[j] >> 9));
+      const bool c = f >= fmaf(-e, kf, 2.0f);
+      if (MASKED) {
+        sum += i < nvalid ? e : 0.0f;
+        cand |= (c && i < nvalid) ? (1u << i) : 0u;
+      } else {
+        sum += e;
+        cand |= c ? (1u << i) : 0u;
+      }
+    }
+  }
+  st = sum;
+  return cand;
 }
 
 struct Params {
@@ -270,40 +313,6 @@ struct Params {
   float* lse;
   int* status;
 };
-
-// Row `row` of step k-1: merge its per-slot partials (lanes split the slots)
-// into x_{k-1}, logp_{k-1}, lse_{k-1}.  All 32 lanes return the same values.
-__device__ __forceinline__ int combine_row(const Params& p, int row, int lane, float& lp, float& l) {
-  const float4* ps = p.prev_stats + (size_t)row * p.n_parts;
-  const int* pi = p.prev_index + (size_t)row * p.n_parts;
-  float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
-  int idx = 0x7fffffff;
-  for (int t = lane; t < p.n_parts; t += 32) {
-    const float4 q = ps[t];
-    lse_merge(m, S, q.x, q.y);
-    const int qi = pi[t];
-    if (better(q.z, qi, key, idx)) {
-      key = q.z;
-      idx = qi;
-      sv = q.w;
-    }
-  }
-  warp_lse(m, S);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ok = __shfl_xor_sync(0xffffffffu, key, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    const float os = __shfl_xor_sync(0xffffffffu, sv, o);
-    if (better(ok, oi, key, idx)) {
-      key = ok;
-      idx = oi;
-      sv = os;
-    }
-  }
-  l = m + logf(S);
-  lp = sv - l;
-  return idx;
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
@@ -343,6 +352,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     *abort_flag = 0;
     fence_barrier_init();
   }
+  {
+    float* rb = (float*)(smem + kOffRowBest);
+    for (int i = threadIdx.x; i < kTileM * 4; i += blockDim.x) rb[i] = -INFINITY;
+  }
   if (warp == kMmaWarp) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -365,8 +378,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           }
           uint8_t* dst = smem + kOffB + stage * kBChunkBytes;
           mbar_expect_tx(&bar_full[stage], kBChunkBytes);
-          tma_load_2d(dst, &tmW2, n * kTileN, c * kChunkK, &bar_full[stage]);
-          tma_load_2d(dst + kBChunkBytes / 2, &tmW2, n * kTileN + 64, c * kChunkK, &bar_full[stage]);
+          // W2^T rows n*128 .. +127, K columns c*64 .. +63 (one contiguous 64 KB block per tile)
+          tma_load_2d(dst, &tmW2, c * kChunkK, n * kTileN, &bar_full[stage]);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -415,9 +428,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           for (int kk = 0; kk < kChunkK / 16; ++kk) {
             // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K advances 32 B.
             const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-            // W2: MN-major, two 64-column boxes 8 KB apart (LBO), 8-row K groups
-            // 1024 B apart (SBO); K advances 16 rows = 2048 B.
-            const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, kBChunkBytes / 2, 1024);
+            // W2^T: K-major like A (128 vocab rows of 128 bytes).
+            const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
             tc_mma(d_tmem, ad, bd, idesc, (c | kk) != 0);
           }
           tc_commit(&bar_empty[stage]);
@@ -461,34 +473,98 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     // the K-major 128-byte-swizzled layout the MMA reads (zero rows past R).
     // x_{k-1} is the anchor for k = 1, else the combine of step k-1's partials;
     // the slot-0 CTA of each row tile also stores step k-1's x, logp, lse.
-    for (int i = 0; i < 8; ++i) {
-      const int rl = warp * 8 + i;
-      const int arow = m_tile * kTileM + rl;
-      int xp = 0;
-      bool valid = arow < p.R;
-      if (valid) {
-        if (p.k == 1) {
-          xp = p.x0[arow];
-        } else {
-          float lp, l;
-          xp = combine_row(p, arow, lane, lp, l);
-          if (slot == 0 && lane == 0) {
-            const size_t o = (size_t)arow * p.gamma + (p.k - 2);
-            p.x[o] = xp;
-            p.logp[o] = lp;
-            p.lse[o] = l;
-          }
-        }
-        if (xp < 0 || xp >= p.V) {
-          if (lane == 0) flag_status(p.status, DSPARK_DEV_BAD_INPUT);
-          xp = xp < 0 ? 0 : p.V - 1;
+    // All loads of the warp's 8 rows are issued before any is used, so the
+    // prologue costs about two memory round trips.
+    int xps[8];
+    if (p.k == 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int arow = m_tile * kTileM + warp * 8 + i;
+        xps[i] = arow < p.R ? p.x0[arow] : 0;
+      }
+    } else {
+      // lane t holds parts t and t + 32 ... of each row (n_parts <= 64 here)
+      float4 q[8][2];
+      int qi[8][2];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int arow = m_tile * kTileM + warp * 8 + i;
+        const bool ok_row = arow < p.R;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int t = lane + 32 * h;
+          const bool ld = ok_row && t < p.n_parts;
+          q[i][h] = ld ? p.prev_stats[(size_t)arow * p.n_parts + t]
+                       : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+          qi[i][h] = ld ? p.prev_index[(size_t)arow * p.n_parts + t] : 0x7fffffff;
         }
       }
-      if (lane < p.r / 8) {  // 16 bytes = 8 of the row's r bf16 per lane
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) v = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)xp * p.r) + lane);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int arow = m_tile * kTileM + warp * 8 + i;
+        float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
+        int idx = 0x7fffffff;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          lse_merge(m, S, q[i][h].x, q[i][h].y);
+          if (better(q[i][h].z, qi[i][h], key, idx)) {
+            key = q[i][h].z;
+            idx = qi[i][h];
+            sv = q[i][h].w;
+          }
+        }
+        for (int t = lane + 64; t < p.n_parts; t += 32) {  // more than 64 parts
+          if (arow >= p.R) break;
+          const float4 qq = p.prev_stats[(size_t)arow * p.n_parts + t];
+          const int qqi = p.prev_index[(size_t)arow * p.n_parts + t];
+          lse_merge(m, S, qq.x, qq.y);
+          if (better(qq.z, qqi, key, idx)) {
+            key = qq.z;
+            idx = qqi;
+            sv = qq.w;
+          }
+        }
+        warp_lse(m, S);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ok2 = __shfl_xor_sync(0xffffffffu, key, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+          const float os = __shfl_xor_sync(0xffffffffu, sv, o);
+          if (better(ok2, oi, key, idx)) {
+            key = ok2;
+            idx = oi;
+            sv = os;
+          }
+        }
+        xps[i] = idx;
+        if (arow < p.R && slot == 0 && lane == 0) {
+          const float l = m + logf(S);
+          const size_t o = (size_t)arow * p.gamma + (p.k - 2);
+          p.x[o] = idx;
+          p.logp[o] = sv - l;
+          p.lse[o] = l;
+        }
+      }
+    }
+    uint4 gv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int arow = m_tile * kTileM + warp * 8 + i;
+      int xp = xps[i];
+      if (arow < p.R && (xp < 0 || xp >= p.V)) {
+        if (lane == 0) flag_status(p.status, DSPARK_DEV_BAD_INPUT);
+        xp = xp < 0 ? 0 : p.V - 1;
+      }
+      gv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (arow < p.R && lane < p.r / 8)  // 16 bytes = 8 of the row's r bf16 per lane
+        gv[i] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)xp * p.r) + lane);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rl = warp * 8 + i;
+      if (lane < p.r / 8) {
         const int c = lane >> 3, piece = lane & 7;
-        *(uint4*)(smem + kOffA + c * kAChunkBytes + rl * 128 + ((piece ^ (rl & 7)) << 4)) = v;
+        *(uint4*)(smem + kOffA + c * kAChunkBytes + rl * 128 + ((piece ^ (rl & 7)) << 4)) = gv[i];
       }
     }
     fence_proxy_async();
@@ -570,10 +646,18 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         float mx = s[0];
 #pragma unroll
         for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
+        // Threshold: the best key this row has seen so far in any of its four
+        // column groups (published in shared memory; a stale value is still a
+        // lower bound of the row's maximum, so no barrier is needed).
+        volatile float* rowbest = (volatile float*)(smem + kOffRowBest) + row_local * 4;
+        float thr = best;
+#pragma unroll
+        for (int g2 = 0; g2 < 4; ++g2)
+          if (g2 != cgrp) thr = fmaxf(thr, rowbest[g2]);
         uint32_t keep = 0xffffffffu;
-        if (best == -INFINITY) {
-          // Seed the running best with the tile's largest score (lowest such
-          // column): every other element is then filtered against a finite key.
+        if (thr == -INFINITY) {
+          // Seed with the tile's largest score (lowest such column): every
+          // other element is then filtered against a finite key.
           int imx = 0;
 #pragma unroll
           for (int i = 31; i >= 0; --i)
@@ -582,27 +666,15 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           best_i = col0 + imx;
           best_s = mx;
           keep = ~(1u << imx);
+          thr = best;
+          rowbest[cgrp] = best;
         }
-        // Pass 1, branch-free: sum of exp(s - mx) and the candidate mask.
-        // Element i can beat the best key b only if 1 - u_i < exp(s_i - b).
+        // Pass 1 (filter_pass): sum of exp(s - mx) and the candidate mask.
         const float mxl = mx * L2E;
-        const float kf = ex2_approx((mx - best) * L2E) * 1.001f;
-        float st = 0.0f;
-        uint32_t cand = 0;
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const uint4 w4 = rng.quad((uint32_t)((col0 >> 2) + q4));
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int i = 4 * q4 + j;
-            const float e = ex2_approx(fmaf(s[i], L2E, -mxl));
-            st += e;
-            // 1 - u, exactly: (2 m + 1) 2^-24 with m the complemented 23-bit field.
-            const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~wv[j]) >> 9)), 0.99999994f);
-            cand |= (om < e * kf) ? (1u << i) : 0u;
-          }
-        }
+        const float kf = ex2_approx((mx - thr) * L2E) * 1.001f;
+        float st;
+        uint32_t cand = nvalid == 32 ? filter_pass<false>(sbox + lane * 128, lane, rng, col0, mxl, kf, 32, st)
+                                     : filter_pass<true>(sbox + lane * 128, lane, rng, col0, mxl, kf, nvalid, st);
         cand &= keep;
         lse_merge(run_m, run_s, mx, st);
         // Pass 2: exact keys of the (rare) candidates, in increasing vocab id.
@@ -619,6 +691,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
             best_s = si;
           }
         }
+        if (best > thr) rowbest[cgrp] = best;  // publish for the row's other groups
       }
     }
 
@@ -656,6 +729,34 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// W2 [r, V] -> W2^T [V, r] (bf16), 64 x 64 tiles through shared memory, so the
+// MMA's B operand of a vocab tile is one contiguous 128 x r block.
+__global__ void __launch_bounds__(256)
+transpose_w2_kernel(const __nv_bfloat16* __restrict__ W2, int r, int V,
+                    __nv_bfloat16* __restrict__ W2T) {
+  __shared__ __nv_bfloat16 tile[64][66];
+  const int k0 = blockIdx.y * 64, v0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 64; i += 8) {
+    const int k = k0 + i;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int v = v0 + tx + 32 * h;
+      tile[i][tx + 32 * h] = (k < r && v < V) ? W2[(size_t)k * V + v] : __float2bfloat16(0.0f);
+    }
+  }
+  __syncthreads();
+  for (int i = ty; i < 64; i += 8) {
+    const int v = v0 + i;
+    if (v >= V) break;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k = k0 + tx + 32 * h;
+      if (k < r) W2T[(size_t)v * r + k] = tile[tx + 32 * h][i];
+    }
   }
 }
 
@@ -714,15 +815,16 @@ int draft_tc_parts(int R, int V) {
   return slots;
 }
 
-cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2, int R, int gamma,
+cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, int R, int gamma,
                              int V, int r, float* scores) {
   static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
   CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(plan->maps);
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
-    const cuuint64_t strides[1] = {(cuuint64_t)V * 2};
-    const cuuint32_t box[2] = {64, kChunkK};
-    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2, dims, strides, box,
+    // W2^T [V, r], K (r) innermost
+    const cuuint64_t dims[2] = {(cuuint64_t)r, (cuuint64_t)V};
+    const cuuint64_t strides[1] = {(cuuint64_t)r * 2};
+    const cuuint32_t box[2] = {kChunkK, kTileN};
+    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W2T, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -754,6 +856,12 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2, i
   plan->V = V;
   plan->r = r;
   return cudaSuccess;
+}
+
+cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStream_t s) {
+  dim3 grid((V + 63) / 64, (r + 63) / 64);
+  transpose_w2_kernel<<<grid, 256, 0, s>>>((const __nv_bfloat16*)W2, r, V, (__nv_bfloat16*)W2T);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,

@@ -21,7 +21,7 @@ constexpr int kDraftTileN = 128;  // vocab columns per tile (both contraction pa
 
 // Workspace layout of dspark_draft_sample (byte offsets, 256-aligned).
 struct DraftWorkspace {
-  size_t status, a_rows, stats, index, stats2, index2, total;  // two partial buffers
+  size_t status, a_rows, stats, index, stats2, index2, w2t, total;  // two partial buffers
 };
 DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype);
 
@@ -39,8 +39,9 @@ struct DraftTcPlan {
   alignas(64) unsigned char maps[3][128];
   int R, gamma, V, r;
 };
-cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2, int R, int gamma,
+cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, int R, int gamma,
                              int V, int r, float* scores);
+cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStream_t s);
 // Step k (1-based): gathers A from x0 (k = 1) or from the combine of `prev`
 // (step k-1's partials, whose x/logp/lse it stores), writes `cur`.
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
@@ -78,7 +79,7 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
 
 // Kernel kinds for the optional event timing (dspark_profile_*).
 enum KernelKind {
-  kKindGather = 0,
+  kKindPrepare = 0,  // W2 transpose (bf16) or anchor gather (fp32)
   kKindDraftTile = 1,
   kKindDraftCombine = 2,
   kKindSchedule = 3,  // both scheduler launches

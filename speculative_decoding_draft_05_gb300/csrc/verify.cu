@@ -241,33 +241,104 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   const int g0 = chunk * kDrawGroups, g1 = min(groups, g0 + kDrawGroups);
   const float L2E = 1.4426950408889634f;
   const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
-  float best = -INFINITY;
+  // best/idx: this thread's argmax; wbest: a lower bound of the warp's best key,
+  // all-reduced after every group and used as the filter threshold (any lower
+  // bound of the final maximum is a valid threshold).
+  float best = -INFINITY, wbest = -INFINITY;
   int idx = 0x7fffffff;
+  const int lane = threadIdx.x & 31;
+  const int iters = (g1 - g0 + kDrawThreads - 1) / kDrawThreads;  // uniform across the CTA
   if (residual) {
     const float* srow = scores + ((size_t)r * gamma + (row - 1)) * V;
     const float ld = lse[(size_t)r * gamma + (row - 1)];
     const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
-    for (int g = g0 + threadIdx.x; g < g1; g += kDrawThreads) {
-      float e[8], sc[8];
-      load8(z, g, e);
-      load8(srow, g, sc);
-      const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
-      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      const float kb = best == -INFINITY ? INFINITY : ex2_approx(-best * L2E) * 1.001f;
-      uint32_t cand = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float ra = __expf(e[i] * invT - Lt) - __expf(sc[i] - ld);  // approximate residual
-        const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
-        cand |= (ra > -1e-6f && om < fmaxf(ra, 1e-6f) * kb) ? (1u << i) : 0u;
-      }
-      if (cand) {
+    for (int it = 0; it < iters; ++it) {
+      const int g = g0 + it * kDrawThreads + threadIdx.x;
+      if (g < g1) {
+        float e[8], sc[8];
+        load8(z, g, e);
+        load8(srow, g, sc);
+        const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
+        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const float kb = wbest == -INFINITY ? INFINITY : ex2_approx(-wbest * L2E) * 1.001f;
+        uint32_t cand = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          if (!(cand & (1u << i))) continue;
-          const float res = expf(e[i] * invT - Lt) - expf(sc[i] - ld);
-          if (res > 0.0f) {
-            const float key = __fadd_rn(logf(res), gumbel(w[i]));
+          const float ra = __expf(e[i] * invT - Lt) - __expf(sc[i] - ld);  // approximate residual
+          const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
+          cand |= (ra > -1e-6f && om < fmaxf(ra, 1e-6f) * kb) ? (1u << i) : 0u;
+        }
+        if (cand) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (!(cand & (1u << i))) continue;
+            const float res = expf(e[i] * invT - Lt) - expf(sc[i] - ld);
+            if (res > 0.0f) {
+              const float key = __fadd_rn(logf(res), gumbel(w[i]));
+              if (better(key, 8 * g + i, best, idx)) {
+                best = key;
+                idx = 8 * g + i;
+              }
+            }
+          }
+        }
+      }
+      wbest = warp_max(fmaxf(wbest, best));
+    }
+  } else {
+    const float invT_l2e = invT * L2E;
+    for (int it = 0; it < iters; ++it) {
+      const int g = g0 + it * kDrawThreads + threadIdx.x;
+      const bool have = g < g1;
+      float e[8];
+      uint32_t w[8];
+      if (have) {
+        load8(z, g, e);
+        const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
+        w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+        w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
+      }
+      if (wbest == -INFINITY) {
+        // Seed the warp's threshold with one exact key: the lane holding the
+        // warp's largest logit evaluates it.
+        float em = -INFINITY;
+        int im = 0;
+        if (have) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (e[i] > em) {
+              em = e[i];
+              im = i;
+            }
+        }
+        float wm = em;
+        int wl = lane;
+        warp_argmax(wm, wl);
+        if (lane == wl && have) {
+          uint32_t ws = w[0];
+#pragma unroll
+          for (int i = 1; i < 8; ++i)
+            if (i == im) ws = w[i];
+          best = __fadd_rn(em * invT, gumbel(ws));
+          idx = 8 * g + im;
+        }
+        wbest = warp_max(best);
+      }
+      if (have) {
+        // candidate iff f_i >= fl(2 - 1.001 exp(z_i / T - b)), f_i = 1 + (w_i >> 9) 2^-23
+        const float c0 = -wbest * L2E;
+        uint32_t cand = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float y = ex2_approx(fmaf(e[i], invT_l2e, c0));
+          const float f = __uint_as_float(0x3F800000u | (w[i] >> 9));
+          cand |= (f >= fmaf(-1.001f, y, 2.0f)) ? (1u << i) : 0u;
+        }
+        if (cand) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (!(cand & (1u << i))) continue;
+            const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
             if (better(key, 8 * g + i, best, idx)) {
               best = key;
               idx = 8 * g + i;
@@ -275,44 +346,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
           }
         }
       }
-    }
-  } else {
-    for (int g = g0 + threadIdx.x; g < g1; g += kDrawThreads) {
-      float e[8];
-      load8(z, g, e);
-      const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
-      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      if (best == -INFINITY) {  // seed with the group's largest logit (lowest such id)
-        float em = e[0];
-        uint32_t wm = w[0];
-        int im = 0;
-#pragma unroll
-        for (int i = 1; i < 8; ++i)
-          if (e[i] > em) {
-            em = e[i];
-            wm = w[i];
-            im = i;
-          }
-        best = __fadd_rn(em * invT, gumbel(wm));
-        idx = 8 * g + im;
-      }
-      uint32_t cand = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
-        cand |= (om < ex2_approx((e[i] * invT - best) * L2E) * 1.001f) ? (1u << i) : 0u;
-      }
-      if (cand) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (!(cand & (1u << i))) continue;
-          const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
-          if (better(key, 8 * g + i, best, idx)) {
-            best = key;
-            idx = 8 * g + i;
-          }
-        }
-      }
+      wbest = warp_max(fmaxf(wbest, best));
     }
   }
   block_argmax<kDrawThreads / 32>(best, idx, rk, ri);
