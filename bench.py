@@ -110,7 +110,8 @@ def measured_peaks():
 
 def source_digest() -> str:
     h = hashlib.sha256()
-    for rel in DRAFT_TILE_SOURCES + ["speculative_decoding_draft_05_gb300/csrc/common.cuh"]:
+    for rel in DRAFT_TILE_SOURCES + ["speculative_decoding_draft_05_gb300/csrc/common.cuh",
+                                     "speculative_decoding_draft_05_gb300/csrc/ptx.cuh"]:
         p = os.path.join(ROOT, rel)
         if os.path.exists(p):
             h.update(open(p, "rb").read())

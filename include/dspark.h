@@ -184,14 +184,14 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
  * point takes the same inputs and outputs as dspark_verify (caller-owned,
  * same layouts and meaning) but no workspace: its scratch (the status word,
  * LSE^t of every row, the accept flags and the per-chunk partials of the
- * drawn token) lives in a file-scope device array
+ * drawn token, the list of scheduled rows) lives in a file-scope device array
  * of DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES bytes that every GPU which loads the
  * library holds until the process exits.
  *
  * - Size limit: dspark_verify_workspace_bytes(R, gamma, V) =
- *   256 + align256(4 R (gamma+1)) + align256(4 R gamma)
+ *   256 + align256(4 R (gamma+1)) + 2 align256(4 R gamma)
  *   + align256(8 R ceil(V / 16384)) bytes must fit in the array (with
- *   gamma = 16 and V = 151,936 that is R <= 19,782); larger
+ *   gamma = 16 and V = 151,936 that is R <= 15,194); larger
  *   problems return DSPARK_ERR_UNSUPPORTED, with the reason in
  *   dspark_last_error(), before anything is enqueued.
  * - The first call on each device looks up the array's device address

@@ -35,21 +35,26 @@ DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype)
   w.index = align256(w.stats + (size_t)R * tiles * sizeof(float4));
   w.stats2 = align256(w.index + (size_t)R * tiles * sizeof(int));
   w.index2 = align256(w.stats2 + (size_t)R * tiles * sizeof(float4));
-  w.w2t = align256(w.index2 + (size_t)R * tiles * sizeof(int));  // bf16 W2^T [V, r]
+  w.gthr = align256(w.index2 + (size_t)R * tiles * sizeof(int));  // uint32 [2, R]
+  w.w2t = align256(w.gthr + 2 * (size_t)R * sizeof(uint32_t));     // bf16 W2^T [V, r]
   w.total = align256(w.w2t + (dtype == DSPARK_BF16 ? (size_t)V * r * 2 : 0));
   return w;
 }
 
-// Scratch layout of verify (byte offsets, 256-aligned): status word, LSE^t
-// [R, gamma+1], accept flags [R, gamma], draw partials [R, chunks] (float2).
+// Scratch layout of verify (byte offsets, 256-aligned): status word and the
+// scheduled-row count (the first 256 bytes), LSE^t [R, gamma+1], accept flags
+// [R, gamma], the scheduled-row list [R * gamma] (u32), draw partials
+// [R, chunks] (float2).
 struct VerifyScratch {
-  size_t lse_t, acc, partials, total;
+  size_t count, lse_t, acc, list, partials, total;
 };
 static VerifyScratch verify_scratch_layout(int R, int gamma, int V) {
   VerifyScratch v;
+  v.count = 4;
   v.lse_t = 256;
   v.acc = align256(v.lse_t + (size_t)R * (gamma + 1) * sizeof(float));
-  v.partials = align256(v.acc + (size_t)R * gamma * sizeof(int));
+  v.list = align256(v.acc + (size_t)R * gamma * sizeof(int));
+  v.partials = align256(v.list + (size_t)R * gamma * sizeof(uint32_t));
   v.total = align256(v.partials + (size_t)R * verify_draw_chunks(V) * sizeof(float2));
   return v;
 }
@@ -161,11 +166,14 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
     DraftTcPlan plan;
     e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
     if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
+    uint32_t* gthr = (uint32_t*)(ws + L.gthr);
+    e = cudaMemsetAsync(gthr, 0, 2 * (size_t)R * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft key reset");
     const DraftPartials buf[2] = {p, p2};
     for (int k = 1; k <= gamma; ++k) {
       prof_begin(kKindDraftTile, s);
-      e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], x, logp, lse,
-                               status, s);
+      e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], gthr, x,
+                               logp, lse, status, s);
       prof_end(s);
       if (e != cudaSuccess) return cuda_fail(e, "draft_step");
     }
@@ -255,7 +263,8 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
   const float invT = 1.0f / temperature;
   prof_begin(kKindVerifyRows, s);
   e = launch_verify_rows(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, cstar,
-                         lse_t_ws, acc_ws, status, s);
+                         lse_t_ws, acc_ws, (uint32_t*)(ws + lay.list), (int*)(ws + lay.count),
+                         status, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "verify_rows");
   prof_begin(kKindVerifyFinish, s);
@@ -338,7 +347,8 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
   const float invT = 1.0f / temperature;
   prof_begin(kKindVerifyRows, s);
   e = launch_verify_rows(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, cstar,
-                         lse_t_ws, acc_ws, status, s);
+                         lse_t_ws, acc_ws, (uint32_t*)(ws + lay.list), (int*)(ws + lay.count),
+                         status, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc rows");
   prof_begin(kKindVerifyFinish, s);

@@ -169,6 +169,19 @@ __device__ __forceinline__ void warp_lse(float& m, float& s) {
   }
 }
 
+// Order-preserving map of a float key onto uint32: unsigned order equals float
+// order for every non-NaN value, and 0 lies below all of them (it stands for
+// "no key yet", so a zero-filled array starts every row at -inf).
+__device__ __forceinline__ uint32_t key_ord(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float ord_key(uint32_t o) {
+  if (o == 0u) return -INFINITY;
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
 // Device status word: OR bits in with an atomic.
 __device__ __forceinline__ void flag_status(int* status, int bits) {
   if (status) atomicOr(status, bits);

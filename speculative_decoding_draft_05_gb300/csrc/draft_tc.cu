@@ -48,6 +48,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dspark {
 
@@ -81,60 +82,8 @@ constexpr int kOffBar = kOffRowBest + kTileM * 4 * 4;
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + kEpiWarps + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack for 1024 alignment
 
-constexpr long long kWaitBudget = 4000000000ll;  // SM clocks (~2 s)
-
 // ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait for the phase of `parity` to complete.  Returns false (and
-// raises the CTA's abort flag) if the budget runs out or another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudget) {
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
+// (mbarrier and bounded-wait wrappers shared with verify.cu are in ptx.cuh)
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -308,6 +257,8 @@ struct Params {
   const int* prev_index;
   float4* pstats;                // this step's partials
   int* pindex;
+  uint32_t* gthr_cur;            // [R] best key per row reached by any CTA of this step (key_ord)
+  uint32_t* gthr_next;           // [R] zeroed here for step k+1
   int32_t* x;                    // step k-1 outputs, written by the slot-0 CTAs
   float* logp;
   float* lse;
@@ -464,6 +415,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY, best_s = 0.0f;
     int best_i = 0x7fffffff;
     bool ok = true;
+    if (slot == 0 && cgrp == 0 && row_ok) p.gthr_next[row] = 0u;
 
     if (lane == 0 && n_units > 0) {
       mbar_expect_tx(&bar_u[warp], kUBoxBytes);
@@ -473,8 +425,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     // the K-major 128-byte-swizzled layout the MMA reads (zero rows past R).
     // x_{k-1} is the anchor for k = 1, else the combine of step k-1's partials;
     // the slot-0 CTA of each row tile also stores step k-1's x, logp, lse.
-    // All loads of the warp's 8 rows are issued before any is used, so the
-    // prologue costs about two memory round trips.
+    // Lanes 4i .. 4i+3 merge row i of the warp's 8: lane 4i + s holds parts
+    // s, s + 4, s + 8, ..., loaded kMergeBatch at a time so that each batch is
+    // in flight at once (two memory round trips for up to 40 parts, where
+    // holding every part of every row at once would need too many registers).
     int xps[8];
     if (p.k == 1) {
 #pragma unroll
@@ -483,68 +437,56 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         xps[i] = arow < p.R ? p.x0[arow] : 0;
       }
     } else {
-      // lane t holds parts t and t + 32 ... of each row (n_parts <= 64 here)
-      float4 q[8][2];
-      int qi[8][2];
+      constexpr int kMergeBatch = 5;
+      const int sub = lane & 3;
+      const int arow = m_tile * kTileM + warp * 8 + (lane >> 2);
+      const bool ok_row = arow < p.R;
+      float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
+      int idx = 0x7fffffff;
+      for (int t0 = sub; t0 < p.n_parts; t0 += 4 * kMergeBatch) {
+        float4 q[kMergeBatch];
+        int qi[kMergeBatch];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int arow = m_tile * kTileM + warp * 8 + i;
-        const bool ok_row = arow < p.R;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int t = lane + 32 * h;
+        for (int b = 0; b < kMergeBatch; ++b) {
+          const int t = t0 + 4 * b;
           const bool ld = ok_row && t < p.n_parts;
-          q[i][h] = ld ? p.prev_stats[(size_t)arow * p.n_parts + t]
-                       : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-          qi[i][h] = ld ? p.prev_index[(size_t)arow * p.n_parts + t] : 0x7fffffff;
+          q[b] = ld ? p.prev_stats[(size_t)arow * p.n_parts + t]
+                    : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+          qi[b] = ld ? p.prev_index[(size_t)arow * p.n_parts + t] : 0x7fffffff;
+        }
+#pragma unroll
+        for (int b = 0; b < kMergeBatch; ++b) {
+          lse_merge(m, S, q[b].x, q[b].y);
+          if (better(q[b].z, qi[b], key, idx)) {
+            key = q[b].z;
+            idx = qi[b];
+            sv = q[b].w;
+          }
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int arow = m_tile * kTileM + warp * 8 + i;
-        float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
-        int idx = 0x7fffffff;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          lse_merge(m, S, q[i][h].x, q[i][h].y);
-          if (better(q[i][h].z, qi[i][h], key, idx)) {
-            key = q[i][h].z;
-            idx = qi[i][h];
-            sv = q[i][h].w;
-          }
-        }
-        for (int t = lane + 64; t < p.n_parts; t += 32) {  // more than 64 parts
-          if (arow >= p.R) break;
-          const float4 qq = p.prev_stats[(size_t)arow * p.n_parts + t];
-          const int qqi = p.prev_index[(size_t)arow * p.n_parts + t];
-          lse_merge(m, S, qq.x, qq.y);
-          if (better(qq.z, qqi, key, idx)) {
-            key = qq.z;
-            idx = qqi;
-            sv = qq.w;
-          }
-        }
-        warp_lse(m, S);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ok2 = __shfl_xor_sync(0xffffffffu, key, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-          const float os = __shfl_xor_sync(0xffffffffu, sv, o);
-          if (better(ok2, oi, key, idx)) {
-            key = ok2;
-            idx = oi;
-            sv = os;
-          }
-        }
-        xps[i] = idx;
-        if (arow < p.R && slot == 0 && lane == 0) {
-          const float l = m + logf(S);
-          const size_t o = (size_t)arow * p.gamma + (p.k - 2);
-          p.x[o] = idx;
-          p.logp[o] = sv - l;
-          p.lse[o] = l;
+      for (int o = 1; o <= 2; o <<= 1) {  // the row's four lanes
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+        lse_merge(m, S, m2, s2);
+        const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+        const float v2 = __shfl_xor_sync(0xffffffffu, sv, o);
+        if (better(k2, i2, key, idx)) {
+          key = k2;
+          idx = i2;
+          sv = v2;
         }
       }
+      if (ok_row && slot == 0 && sub == 0) {
+        const float l = m + logf(S);
+        const size_t o = (size_t)arow * p.gamma + (p.k - 2);
+        p.x[o] = idx;
+        p.logp[o] = sv - l;
+        p.lse[o] = l;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xps[i] = __shfl_sync(0xffffffffu, idx, 4 * i);
     }
     uint4 gv[8];
 #pragma unroll
@@ -575,6 +517,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       const int buf = u & 1;
       const uint32_t acc_phase = (u >> 1) & 1;
       const int col0 = n * kTileN + cgrp * 32;
+      // The row's best key over all CTAs of this step so far, read early (L2).
+      const uint32_t gkey = row_ok ? __ldcg(p.gthr_cur + row) : 0u;
 
       // U block of this warp: row `lane`, 32 bf16 (64-byte rows, 64-byte swizzle).
       ok = ok && mbar_wait(&bar_u[warp], u & 1, abort_flag);
@@ -646,11 +590,13 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         float mx = s[0];
 #pragma unroll
         for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
-        // Threshold: the best key this row has seen so far in any of its four
-        // column groups (published in shared memory; a stale value is still a
-        // lower bound of the row's maximum, so no barrier is needed).
+        // Threshold: the best key this row has reached so far in any of the
+        // CTA's four column groups (shared memory) or in any CTA of this step
+        // (global, raised with atomicMax).  Every published key is one an
+        // element of the row reached, so a stale value is still a lower bound
+        // of the row's maximum and no barrier is needed.
         volatile float* rowbest = (volatile float*)(smem + kOffRowBest) + row_local * 4;
-        float thr = best;
+        float thr = fmaxf(best, ord_key(gkey));
 #pragma unroll
         for (int g2 = 0; g2 < 4; ++g2)
           if (g2 != cgrp) thr = fmaxf(thr, rowbest[g2]);
@@ -668,6 +614,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           keep = ~(1u << imx);
           thr = best;
           rowbest[cgrp] = best;
+          if (best < INFINITY) atomicMax(p.gthr_cur + row, key_ord(best));
         }
         // Pass 1 (filter_pass): sum of exp(s - mx) and the candidate mask.
         const float mxl = mx * L2E;
@@ -691,7 +638,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
             best_s = si;
           }
         }
-        if (best > thr) rowbest[cgrp] = best;  // publish for the row's other groups
+        if (best > thr) {  // publish for the row's other groups and CTAs
+          rowbest[cgrp] = best;
+          if (best < INFINITY) atomicMax(p.gthr_cur + row, key_ord(best));
+        }
       }
     }
 
@@ -733,29 +683,43 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
 }
 
 // W2 [r, V] -> W2^T [V, r] (bf16), 64 x 64 tiles through shared memory, so the
-// MMA's B operand of a vocab tile is one contiguous 128 x r block.
+// MMA's B operand of a vocab tile is one contiguous 128 x r block.  Both sides
+// move 16-byte chunks (8 bf16): whole 128-byte rows in and out.  Needs
+// V % 8 == 0 and r % 8 == 0 and a 16-byte aligned W2 (the tensor-core path
+// checks all three).
 __global__ void __launch_bounds__(256)
 transpose_w2_kernel(const __nv_bfloat16* __restrict__ W2, int r, int V,
                     __nv_bfloat16* __restrict__ W2T) {
-  __shared__ __nv_bfloat16 tile[64][66];
+  __shared__ unsigned short tile[64][66];  // [k][v]; the padding spreads columns over banks
   const int k0 = blockIdx.y * 64, v0 = blockIdx.x * 64;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  for (int i = ty; i < 64; i += 8) {
-    const int k = k0 + i;
+  const unsigned short* src = reinterpret_cast<const unsigned short*>(W2);
+  unsigned short* dst = reinterpret_cast<unsigned short*>(W2T);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int v = v0 + tx + 32 * h;
-      tile[i][tx + 32 * h] = (k < r && v < V) ? W2[(size_t)k * V + v] : __float2bfloat16(0.0f);
+  for (int h = 0; h < 2; ++h) {
+    const int c = threadIdx.x + 256 * h;  // 512 chunks: 64 k rows x 8 chunks of 8 vocab ids
+    const int i = c >> 3, j = (c & 7) * 8;
+    const int k = k0 + i, v = v0 + j;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (k < r && v < V) q = __ldg(reinterpret_cast<const uint4*>(src + (size_t)k * V + v));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      tile[i][j + 2 * e] = (unsigned short)(w[e] & 0xffffu);
+      tile[i][j + 2 * e + 1] = (unsigned short)(w[e] >> 16);
     }
   }
   __syncthreads();
-  for (int i = ty; i < 64; i += 8) {
-    const int v = v0 + i;
-    if (v >= V) break;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k = k0 + tx + 32 * h;
-      if (k < r) W2T[(size_t)v * r + k] = tile[tx + 32 * h][i];
+  for (int h = 0; h < 2; ++h) {
+    const int c = threadIdx.x + 256 * h;  // 64 vocab rows x 8 chunks of 8 k
+    const int i = c >> 3, j = (c & 7) * 8;
+    const int v = v0 + i, k = k0 + j;
+    if (v < V && k < r) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = (uint32_t)tile[j + 2 * e][i] | ((uint32_t)tile[j + 2 * e + 1][i] << 16);
+      *reinterpret_cast<uint4*>(dst + (size_t)v * r + k) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -866,8 +830,8 @@ cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStr
 
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
-                                 const DraftPartials& cur, int32_t* x, float* logp, float* lse,
-                                 int* status, cudaStream_t s) {
+                                 const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
+                                 float* lse, int* status, cudaStream_t s) {
   const int Mt = (plan.R + kTileM - 1) / kTileM;
   const int n_tiles = (plan.V + kTileN - 1) / kTileN;
   const int slots = draft_tc_parts(plan.R, plan.V);
@@ -890,6 +854,8 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.prev_index = prev.index;
   p.pstats = cur.stats;
   p.pindex = cur.index;
+  p.gthr_cur = gthr + (size_t)(k & 1) * plan.R;
+  p.gthr_next = gthr + (size_t)((k + 1) & 1) * plan.R;
   p.x = x;
   p.logp = logp;
   p.lse = lse;

@@ -21,7 +21,8 @@ constexpr int kDraftTileN = 128;  // vocab columns per tile (both contraction pa
 
 // Workspace layout of dspark_draft_sample (byte offsets, 256-aligned).
 struct DraftWorkspace {
-  size_t status, a_rows, stats, index, stats2, index2, w2t, total;  // two partial buffers
+  // two partial buffers; gthr: [2][R] per-row best keys shared by a step's CTAs
+  size_t status, a_rows, stats, index, stats2, index2, gthr, w2t, total;
 };
 DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype);
 
@@ -43,11 +44,14 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, 
                              int V, int r, float* scores);
 cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStream_t s);
 // Step k (1-based): gathers A from x0 (k = 1) or from the combine of `prev`
-// (step k-1's partials, whose x/logp/lse it stores), writes `cur`.
+// (step k-1's partials, whose x/logp/lse it stores), writes `cur`.  gthr is
+// the [2][R] array of per-row best keys (key_ord form): step k reads and raises
+// row k & 1 and zeroes row (k + 1) & 1 for the next step; row 1 must be zero
+// before step 1.
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
-                                 const DraftPartials& cur, int32_t* x, float* logp, float* lse,
-                                 int* status, cudaStream_t s);
+                                 const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
+                                 float* lse, int* status, cudaStream_t s);
 bool draft_tc_supported(int R, int V, int r);
 int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path
 
@@ -63,10 +67,14 @@ cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double*
                                  int gamma, int32_t* ell, double* diag, int* status,
                                  cudaStream_t s);
 
+// LSE^t, c* and the accept flag of every scheduled row (r, j <= l_r).
+// row_list ([R * gamma] u32) and *row_count are scratch: the list of those rows
+// that verify_index builds first and the row kernel then takes from.
 cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
-                               float* lse_t_ws, int* acc_ws, int* status, cudaStream_t s);
+                               float* lse_t_ws, int* acc_ws, uint32_t* row_list, int* row_count,
+                               int* status, cudaStream_t s);
 
 // The drawn token: verify_draw over vocab chunks, then verify_emit per request.
 int verify_draw_chunks(int V);

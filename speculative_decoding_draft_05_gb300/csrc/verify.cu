@@ -8,11 +8,12 @@
 // c*_k = 1 - 1/2 |p^d_k - p^t_k|_1).  "DSpark: ... Semi-Autoregressive
 // Generation" (notes), "배경": accept the longest prefix.
 //
-// Two launches:
-//   verify_rows   a CTA per scheduled row (r, j), j <= l_r: LSE of Z_j / T,
-//                 c*_j = sum_v min(p^d_j, p^t_j), and the accept test of x_j.
-//                 The Z row is streamed twice (the second pass hits L2) and
-//                 the score row once, with 16-byte vector loads.
+// Launches:
+//   verify_index  one CTA: the scheduled rows (r, j), j <= l_r, as a flat list.
+//   verify_rows   a CTA per listed row at a time: LSE of Z_j / T,
+//                 c*_j = sum_v min(p^d_j, p^t_j), and the accept test of x_j;
+//                 Z_j is streamed twice (the second pass hits L2) and the
+//                 score row once, with several 16-byte loads in flight.
 //   verify_draw   (vocab chunks x requests) CTAs: first rejection n, then the
 //                 Gumbel-max draw from norm(max(0, p^t - p^d)) at row n + 1 or
 //                 from p^t at the bonus row l + 1, one partial per chunk;
@@ -54,14 +55,7 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* __restrict__ row, int
   }
 }
 
-// Streaming loads for data read exactly once.
-__device__ __forceinline__ void load8_stream(const float* __restrict__ row, int g, float (&o)[8]) {
-  const float4 a = __ldcs(reinterpret_cast<const float4*>(row) + 2 * g);
-  const float4 b = __ldcs(reinterpret_cast<const float4*>(row) + 2 * g + 1);
-  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
-  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
-}
-
+template <int NWARPS = kWarps>
 __device__ __forceinline__ float block_sum(float v, float* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   v = warp_sum(v);
@@ -69,7 +63,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   float t = 0.0f;
   if (threadIdx.x < 32) {
-    t = lane < kWarps ? red[lane] : 0.0f;
+    t = lane < NWARPS ? red[lane] : 0.0f;
     t = warp_sum(t);
     if (lane == 0) red[0] = t;
   }
@@ -77,29 +71,6 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   t = red[0];
   __syncthreads();
   return t;
-}
-
-__device__ __forceinline__ float block_lse(float m, float s, float* rm, float* rs) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  warp_lse(m, s);
-  if (lane == 0) {
-    rm[warp] = m;
-    rs[warp] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float mm = lane < kWarps ? rm[lane] : -INFINITY;
-    float ss = lane < kWarps ? rs[lane] : 0.0f;
-    warp_lse(mm, ss);
-    if (lane == 0) {
-      rm[0] = mm;
-      rs[0] = ss;
-    }
-  }
-  __syncthreads();
-  const float out = rm[0] + logf(rs[0]);
-  __syncthreads();
-  return out;
 }
 
 // Block-wide argmax over NWARPS warps (rk, ri hold NWARPS entries).
@@ -137,69 +108,221 @@ __device__ __forceinline__ int clamp_ell(const int32_t* ell, int r, int gamma, i
   return L;
 }
 
+// ---------------------------------------------------------------------------
+// Scheduled rows as a flat list: entry i = r * gamma + (j - 1) for the rows
+// (r, j), 1 <= j <= l_r, in request order; *count = their number.  One CTA,
+// a block-wide exclusive scan of l over tiles of 1024 requests.
+constexpr int kIndexThreads = 1024;
+
+__global__ void __launch_bounds__(kIndexThreads)
+verify_index_kernel(const int32_t* __restrict__ ell, int R, int gamma, uint32_t* __restrict__ list,
+                    int* __restrict__ count, int* __restrict__ status) {
+  __shared__ int warp_tot[kIndexThreads / 32];
+  __shared__ int carry;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < R; base += kIndexThreads) {
+    const int r = base + threadIdx.x;
+    const int L = r < R ? clamp_ell(ell, r, gamma, status, true) : 0;
+    int v = L;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += t;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += t;
+      }
+      warp_tot[lane] = w;  // inclusive totals of warps 0..lane
+    }
+    __syncthreads();
+    const int excl = carry + (warp ? warp_tot[warp - 1] : 0) + v - L;
+    for (int j = 0; j < L; ++j) list[excl + j] = (uint32_t)(r * gamma + j);
+    __syncthreads();
+    if (threadIdx.x == kIndexThreads - 1) carry = excl + L;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *count = carry;
+}
+
+// Block-wide (max, sum exp(x - max)) of the per-thread pairs over NWARPS warps;
+// every thread gets the result.
+template <int NWARPS>
+__device__ __forceinline__ void block_ms(float& m, float& s, float* rm, float* rs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_lse(m, s);
+  if (lane == 0) {
+    rm[warp] = m;
+    rs[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float mm = lane < NWARPS ? rm[lane] : -INFINITY;
+    float ss = lane < NWARPS ? rs[lane] : 0.0f;
+    warp_lse(mm, ss);
+    if (lane == 0) {
+      rm[0] = mm;
+      rs[0] = ss;
+    }
+  }
+  __syncthreads();
+  m = rm[0];
+  s = rs[0];
+  __syncthreads();
+}
+
+// Eight consecutive elements of a row held raw (as loaded) until they are used,
+// so that several 16-byte loads per thread are in flight at once.
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  uint4 a;
+  __device__ __forceinline__ void load(const __nv_bfloat16* row, int g) {
+    a = __ldg(reinterpret_cast<const uint4*>(row) + g);
+  }
+  __device__ __forceinline__ void unpack(float (&o)[8]) const {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* row, int g) {
+    a = __ldg(reinterpret_cast<const float4*>(row) + 2 * g);
+    b = __ldg(reinterpret_cast<const float4*>(row) + 2 * g + 1);
+  }
+  __device__ __forceinline__ void unpack(float (&o)[8]) const {
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+    o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+  }
+};
+
+// LSE^t_j, c*_j and the accept test of x_j for every listed row (r, j), one
+// CTA per row at a time (rows i = CTA, CTA + grid, ...), two CTAs of 512
+// threads per SM.  Pass 1 streams Z_j from HBM (64 bytes of Z in flight per
+// thread) into an online (max, sum exp) of Z_j / T; pass 2 streams
+// Z_j again -- from L2, which holds the rows in flight (2 per SM, 46 MB at
+// V = 151,936) -- with the draft scores (streaming loads, read once) into
+// sum_v min(p^d, p^t).  So HBM sees Z and the scores once.  The row's list
+// entry is loaded a row ahead and its scalars (x_j, the draft LSE, logp_j,
+// then the logit Z_j[x_j]) one pass ahead of their use.
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+template <typename T> constexpr int row_unroll() { return sizeof(T) == 2 ? 4 : 2; }
+
 template <typename T>
-__global__ void __launch_bounds__(kVerifyThreads)
-verify_rows_kernel(const int32_t* __restrict__ x, const float* __restrict__ logp,
-                   const float* __restrict__ lse, const float* __restrict__ scores,
-                   const T* __restrict__ Z, const int32_t* __restrict__ ell, int R, int gamma,
-                   int V, float invT, uint64_t seed, float* __restrict__ cstar,
-                   float* __restrict__ lse_t_ws, int* __restrict__ acc_ws,
-                   int* __restrict__ status) {
-  __shared__ float rm[kWarps], rs[kWarps];
-  const int items = R * gamma;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-  const int r = item / gamma, j = item - r * gamma + 1;
-  const int L = clamp_ell(ell, r, gamma, status, j == 1 && threadIdx.x == 0);
-  if (j > L) continue;  // uniform across the CTA
+__global__ void __launch_bounds__(kRowThreads, 2)
+verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict__ logp,
+                          const float* __restrict__ lse, const float* __restrict__ scores,
+                          const T* __restrict__ Z, const uint32_t* __restrict__ list,
+                          const int* __restrict__ count, int gamma, int V, float invT,
+                          uint64_t seed, float* __restrict__ cstar, float* __restrict__ lse_t_ws,
+                          int* __restrict__ acc_ws, int* __restrict__ status) {
+  __shared__ float rm[kRowWarps], rs[kRowWarps];
+  __shared__ float s_ld;
+  constexpr int kRowUnroll = row_unroll<T>();  // 64 bytes of Z per thread in flight
+  const int n_rows = *count;
   const int groups = V >> 3;
-  const T* z = Z + ((size_t)r * (gamma + 1) + (j - 1)) * V;
-  const float* srow = scores + ((size_t)r * gamma + (j - 1)) * V;
-  const float ld = lse[(size_t)r * gamma + (j - 1)];
-
-  // Pass 1: LSE of Z_j / T.
-  float m = -INFINITY, S = 0.0f;
-  for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
-    float e[8];
-    load8(z, g, e);
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      e[i] *= invT;
-      mx = fmaxf(mx, e[i]);
+  uint32_t item = (int)blockIdx.x < n_rows ? list[blockIdx.x] : 0u;
+  for (int i = blockIdx.x; i < n_rows; i += gridDim.x) {
+    const uint32_t item_next = i + (int)gridDim.x < n_rows ? list[i + gridDim.x] : 0u;
+    const int r = (int)(item / (uint32_t)gamma), j = (int)(item - (uint32_t)r * gamma) + 1;
+    const size_t rj = (size_t)r * gamma + (j - 1);
+    const T* z = Z + ((size_t)r * (gamma + 1) + (j - 1)) * V;
+    const float* srow = scores + rj * V;
+    int xj = 0;
+    float ld0 = 0.0f, lp = 0.0f;
+    if (threadIdx.x == 0) {
+      xj = x[rj];
+      ld0 = lse[rj];
+      lp = logp[rj];
     }
-    if (mx > m) {
-      S = (m == -INFINITY) ? 0.0f : S * __expf(m - mx);
-      m = mx;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) S += __expf(e[i] - m);
-  }
-  const float Lt = block_lse(m, S, rm, rs);
 
-  // Pass 2: c*_j = sum_v min(p^d, p^t).
-  float acc = 0.0f;
-  for (int g = threadIdx.x; g < groups; g += kVerifyThreads) {
-    float e[8], s[8];
-    load8(z, g, e);
-    load8_stream(srow, g, s);
+    // Pass 1: (max, sum exp) of Z_j / T.
+    float m = -INFINITY, S = 0.0f;
+    for (int g0 = threadIdx.x; g0 < groups; g0 += kRowThreads * kRowUnroll) {
+      Raw8<T> raw[kRowUnroll];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc += fminf(__expf(s[i] - ld), __expf(e[i] * invT - Lt));
-  }
-  const float cs = block_sum(acc, rs);
-
-  if (threadIdx.x == 0) {
-    int xj = x[(size_t)r * gamma + (j - 1)];
-    if (xj < 0 || xj >= V) {
-      flag_status(status, DSPARK_DEV_BAD_INPUT);
-      xj = xj < 0 ? 0 : V - 1;
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int g = g0 + u * kRowThreads;
+        if (g < groups) raw[u].load(z, g);
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll; ++u) {
+        if (g0 + u * kRowThreads >= groups) break;
+        float e[8];
+        raw[u].unpack(e);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          e[t] *= invT;
+          mx = fmaxf(mx, e[t]);
+        }
+        if (mx > m) {
+          S = (m == -INFINITY) ? 0.0f : S * __expf(m - mx);
+          m = mx;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) S += __expf(e[t] - m);
+      }
     }
-    const float zx = to_f32(z[xj]) * invT;
-    const float rhs = (zx - Lt) - logp[(size_t)r * gamma + (j - 1)];
-    const float u = uniform01(rng_word(seed, (uint32_t)r, (uint32_t)j, DSPARK_PURPOSE_ACCEPT, 0u));
-    acc_ws[(size_t)r * gamma + (j - 1)] = logf(u) < rhs ? 1 : 0;
-    cstar[(size_t)r * gamma + (j - 1)] = cs;
-    lse_t_ws[(size_t)r * (gamma + 1) + (j - 1)] = Lt;
-  }
+    block_ms<kRowWarps>(m, S, rm, rs);
+    const float Lt = m + logf(S);
+    T zraw = T();
+    if (threadIdx.x == 0) {
+      s_ld = ld0;
+      if (xj < 0 || xj >= V) {
+        flag_status(status, DSPARK_DEV_BAD_INPUT);
+        xj = xj < 0 ? 0 : V - 1;
+      }
+      zraw = z[xj];  // first used after pass 2
+    }
+    __syncthreads();
+    const float ld = s_ld;
+
+    // Pass 2: sum over the row of min(p^d, p^t) = exp(min(s - lse^d, z / T - LSE^t)).
+    float acc = 0.0f;
+    for (int g0 = threadIdx.x; g0 < groups; g0 += kRowThreads * (kRowUnroll / 2)) {
+      Raw8<T> raw[kRowUnroll / 2];
+      float4 sa[kRowUnroll / 2], sb[kRowUnroll / 2];
+#pragma unroll
+      for (int u = 0; u < kRowUnroll / 2; ++u) {
+        const int g = g0 + u * kRowThreads;
+        if (g < groups) {
+          raw[u].load(z, g);
+          sa[u] = __ldcs(reinterpret_cast<const float4*>(srow) + 2 * g);
+          sb[u] = __ldcs(reinterpret_cast<const float4*>(srow) + 2 * g + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowUnroll / 2; ++u) {
+        if (g0 + u * kRowThreads >= groups) break;
+        float e[8];
+        raw[u].unpack(e);
+        const float sv[8] = {sa[u].x, sa[u].y, sa[u].z, sa[u].w, sb[u].x, sb[u].y, sb[u].z, sb[u].w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) acc += __expf(fminf(sv[t] - ld, e[t] * invT - Lt));
+      }
+    }
+    const float csum = block_sum<kRowWarps>(acc, rs);
+    if (threadIdx.x == 0) {
+      const float u = uniform01(rng_word(seed, (uint32_t)r, (uint32_t)j, DSPARK_PURPOSE_ACCEPT, 0u));
+      const float rhs = (to_f32(zraw) * invT - Lt) - lp;
+      acc_ws[rj] = logf(u) < rhs ? 1 : 0;
+      cstar[rj] = csum;
+      lse_t_ws[(size_t)r * (gamma + 1) + (j - 1)] = Lt;
+    }
+    item = item_next;
   }
 }
 
@@ -218,8 +341,10 @@ constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 
 // element v can beat the running best key b only if -ln u_v < w_v exp(-b),
 // where w_v is its weight (the p^t mass for the bonus draw, the residual for
 // the rejection draw).  Since -ln u >= 1 - u, elements with 1 - u_v >= w_v e^-b
-// (0.1% slack) are skipped without the logarithms; the first element a thread
-// meets seeds b.  Writes the chunk's (best key, index) partial.
+// (0.1% slack) are skipped without the logarithms.  b is the best key any
+// warp of the CTA has reached so far (shared memory, raised with atomicMax in
+// key_ord form; a stale value is still a lower bound of the chunk's maximum).
+// Writes the chunk's (best key, index) partial.
 template <typename T>
 __global__ void __launch_bounds__(kDrawThreads)
 verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
@@ -229,10 +354,15 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   __shared__ float rk[kDrawThreads / 32];
   __shared__ int ri[kDrawThreads / 32];
   __shared__ int s_n;
+  __shared__ uint32_t s_best;  // key_ord of the CTA's best key so far (0: none)
   const int r = blockIdx.y, chunk = blockIdx.x;
   const int L = clamp_ell(ell, r, gamma, nullptr, false);
-  if (threadIdx.x == 0) s_n = leading_accepts(acc_ws, r, gamma, L);
+  if (threadIdx.x == 0) {
+    s_n = leading_accepts(acc_ws, r, gamma, L);
+    s_best = 0u;
+  }
   __syncthreads();
+  volatile uint32_t* cta_best = &s_best;
   const int n = s_n;
   const bool residual = n < L;
   const int row = n + 1;  // 1-based position of the drawn token
@@ -241,10 +371,9 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   const int g0 = chunk * kDrawGroups, g1 = min(groups, g0 + kDrawGroups);
   const float L2E = 1.4426950408889634f;
   const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
-  // best/idx: this thread's argmax; wbest: a lower bound of the warp's best key,
-  // all-reduced after every group and used as the filter threshold (any lower
-  // bound of the final maximum is a valid threshold).
-  float best = -INFINITY, wbest = -INFINITY;
+  // best/idx: this thread's argmax; a lane publishes its best key into the
+  // CTA's threshold whenever it beats the threshold it filtered against.
+  float best = -INFINITY;
   int idx = 0x7fffffff;
   const int lane = threadIdx.x & 31;
   const int iters = (g1 - g0 + kDrawThreads - 1) / kDrawThreads;  // uniform across the CTA
@@ -260,7 +389,8 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
         load8(srow, g, sc);
         const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
         const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const float kb = wbest == -INFINITY ? INFINITY : ex2_approx(-wbest * L2E) * 1.001f;
+        const float thr = ord_key(*cta_best);
+        const float kb = thr == -INFINITY ? INFINITY : ex2_approx(-thr * L2E) * 1.001f;
         uint32_t cand = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -281,9 +411,10 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
               }
             }
           }
+          if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
         }
       }
-      wbest = warp_max(fmaxf(wbest, best));
+      __syncwarp();
     }
   } else {
     const float invT_l2e = invT * L2E;
@@ -298,9 +429,10 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
         w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
         w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
       }
-      if (wbest == -INFINITY) {
-        // Seed the warp's threshold with one exact key: the lane holding the
-        // warp's largest logit evaluates it.
+      float thr = __shfl_sync(0xffffffffu, ord_key(*cta_best), 0);  // one value per warp
+      if (thr == -INFINITY) {
+        // Seed the threshold with one exact key: the lane holding the warp's
+        // largest logit evaluates it.
         float em = -INFINITY;
         int im = 0;
         if (have) {
@@ -319,14 +451,18 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
 #pragma unroll
           for (int i = 1; i < 8; ++i)
             if (i == im) ws = w[i];
-          best = __fadd_rn(em * invT, gumbel(ws));
-          idx = 8 * g + im;
+          const float key = __fadd_rn(em * invT, gumbel(ws));
+          if (better(key, 8 * g + im, best, idx)) {
+            best = key;
+            idx = 8 * g + im;
+          }
+          if (best < INFINITY) atomicMax(&s_best, key_ord(best));
         }
-        wbest = warp_max(best);
+        thr = warp_max(best);
       }
       if (have) {
         // candidate iff f_i >= fl(2 - 1.001 exp(z_i / T - b)), f_i = 1 + (w_i >> 9) 2^-23
-        const float c0 = -wbest * L2E;
+        const float c0 = -thr * L2E;
         uint32_t cand = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -344,9 +480,10 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
               idx = 8 * g + i;
             }
           }
+          if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
         }
       }
-      wbest = warp_max(fmaxf(wbest, best));
+      __syncwarp();
     }
   }
   block_argmax<kDrawThreads / 32>(best, idx, rk, ri);
@@ -439,18 +576,22 @@ int verify_sm_count() {
 cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
-                               float* lse_t_ws, int* acc_ws, int* status, cudaStream_t s) {
-  int grid = R * gamma;
-  const int cap = 4 * verify_sm_count();  // 4 CTAs of 512 threads per SM
-  if (grid > cap) grid = cap;
+                               float* lse_t_ws, int* acc_ws, uint32_t* row_list, int* row_count,
+                               int* status, cudaStream_t s) {
+  verify_index_kernel<<<1, kIndexThreads, 0, s>>>(ell, R, gamma, row_list, row_count, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long rows_max = (long long)R * gamma;
+  const int cap = 2 * verify_sm_count();  // two CTAs of 512 threads per SM
+  const int grid = (int)(rows_max < cap ? rows_max : cap);
   if (dtype == DSPARK_BF16)
-    verify_rows_kernel<__nv_bfloat16><<<grid, kVerifyThreads, 0, s>>>(
-        x, logp, lse, scores, (const __nv_bfloat16*)Z, ell, R, gamma, V, invT, seed, cstar,
-        lse_t_ws, acc_ws, status);
+    verify_rows_stream_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, s>>>(
+        x, logp, lse, scores, (const __nv_bfloat16*)Z, row_list, row_count, gamma, V, invT, seed,
+        cstar, lse_t_ws, acc_ws, status);
   else
-    verify_rows_kernel<float><<<grid, kVerifyThreads, 0, s>>>(
-        x, logp, lse, scores, (const float*)Z, ell, R, gamma, V, invT, seed, cstar, lse_t_ws,
-        acc_ws, status);
+    verify_rows_stream_kernel<float><<<grid, kRowThreads, 0, s>>>(
+        x, logp, lse, scores, (const float*)Z, row_list, row_count, gamma, V, invT, seed, cstar,
+        lse_t_ws, acc_ws, status);
   return cudaGetLastError();
 }
 

@@ -80,10 +80,13 @@ def test_round_parity_small(w):
         assert np.isnan(gv["cstar"][i, gs["ell"][i]:]).all()
 
 
-def test_verify_parity_on_oracle_draft():
-    # Verify alone, fed the oracle's draft outputs (rounded to fp32), on a
-    # full-block schedule: every scheduled row is tested and its c* compared.
-    w = QWEN.resized(name="verify_only", R=40, gamma=6, V=3000 - 3000 % 8, r=64)
+@pytest.mark.parametrize("R,gamma,V", [(40, 6, 3000 - 3000 % 8), (6, 3, 262144), (5, 2, 344064)],
+                         ids=["v2992", "v262144", "v344064"])
+def test_verify_parity_on_oracle_draft(R, gamma, V):
+    # Verify alone, fed the oracle's draft outputs (rounded to fp32), with a
+    # random schedule: every scheduled row is tested and its c* compared, at
+    # vocabularies from a few tiles of the row loop to beyond 2^18.
+    w = QWEN.resized(name="verify_only", R=R, gamma=gamma, V=V, r=64)
     seed = 5
     inp = workload.generate(w, seed=seed, device="cpu")
     W1, W2 = f64(inp["W1"]), f64(inp["W2"])
@@ -100,7 +103,9 @@ def test_verify_parity_on_oracle_draft():
     gv = {k: v.cpu().numpy() for k, v in gv.items() if isinstance(v, torch.Tensor) and k != "workspace"}
     ex = compare_verify(gv, ov, ell, w.dtype)
     assert len(ex) <= 1
-    assert ov["n_acc"].sum() > 0 and (ov["n_acc"] < ell).any()  # both outcomes exercised
+    assert ell.sum() > 0
+    if R >= 40:
+        assert ov["n_acc"].sum() > 0 and (ov["n_acc"] < ell).any()  # both outcomes exercised
 
 
 @pytest.mark.parametrize("name", workload.ORDER)

@@ -91,7 +91,7 @@ def test_noalloc_verify_matches_workspace_verify_twice(w):
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
     L = _lib()
-    R, g, V = 40000, 16, 1024  # 4 R (2 g + 1) bytes > 4 MiB
+    R, g, V = 40000, 16, 1024  # more than 4 R (3 g + 1) bytes > 4 MiB of scratch
     p = 256  # never dereferenced: the size check comes before any device work
     st = L.dspark_verify_noalloc(p, p, p, p, p, binding.DSPARK_BF16, p, R, g, V, 1.0, 0, p, p, p, p, None,
                                  None)
