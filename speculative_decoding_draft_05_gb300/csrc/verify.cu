@@ -345,8 +345,9 @@ constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 
 // warp of the CTA has reached so far (shared memory, raised with atomicMax in
 // key_ord form; a stale value is still a lower bound of the chunk's maximum).
 // Writes the chunk's (best key, index) partial.
+// Five CTAs per SM (48 registers): the draw is latency-bound per warp.
 template <typename T>
-__global__ void __launch_bounds__(kDrawThreads)
+__global__ void __launch_bounds__(kDrawThreads, 5)
 verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
                    const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
                    float invT, uint64_t seed, const float* __restrict__ lse_t_ws,
