@@ -11,6 +11,9 @@ Function-level citations are in the C file; the summary:
 * ``draft``     -- DSpark summary §3.1 and DSpark notes "DSpark 핵심 기술 1":
                    s_k = (U_k + W1[x_{k-1}] W2) / T, lse_k, Gumbel-max x_k, logp_k.
 * ``schedule``  -- DSpark summary §3.2.2 (Algorithm 1).
+* ``schedule_capacity`` / ``schedule_topk`` -- DSpark summary §5.2 (zero-overhead
+                   scheduling: capacity from old confidences without the early
+                   stop, then the top K of the current order).
 * ``verify``    -- standard rejection sampling (DSpark summary, opening bullets
                    and §3), soft label c* (DSpark summary §3.2.1).
 
@@ -70,6 +73,10 @@ def lib() -> ctypes.CDLL:
             L.oracle_draft.restype = i32
             L.oracle_schedule.argtypes = [i32, i32, P, P, i32, P, P, P]
             L.oracle_schedule.restype = i32
+            L.oracle_schedule_capacity.argtypes = [i32, i32, P, P, i32, P, P]
+            L.oracle_schedule_capacity.restype = i32
+            L.oracle_schedule_topk.argtypes = [i32, i32, P, i32, P]
+            L.oracle_schedule_topk.restype = i32
             L.oracle_verify.argtypes = [i32, P, i32, i32, dbl, u64, P, P, P, P, P, P, P, P, P, P, P,
                                         P, P, P, i32]
             L.oracle_verify.restype = i32
@@ -168,6 +175,30 @@ def schedule(conf, sps):
         raise ValueError(f"oracle_schedule rejected its arguments (code {rc}; 3 = a step rate that is not positive and finite)")
     return dict(ell=ell, B=int(diag[0]), tau=float(diag[1]), theta=float(diag[2]),
                 n_taken=int(diag[3]), a=a)
+
+
+def schedule_capacity(conf_old, sps):
+    """ZOS capacity K: the first global maximum of Theta along Algorithm 1's order."""
+    c = np.ascontiguousarray(conf_old, dtype=np.float32)
+    R, g = c.shape
+    s = _f64(sps).reshape(-1)
+    K = np.zeros(1, dtype=np.int32)
+    diag = np.zeros(4)
+    rc = lib().oracle_schedule_capacity(R, g, _ptr(c), _ptr(s), s.size, _ptr(K), _ptr(diag))
+    if rc != 0:
+        raise ValueError(f"oracle_schedule_capacity rejected its arguments (code {rc})")
+    return dict(K=int(K[0]), B=int(diag[0]), tau=float(diag[1]), theta=float(diag[2]))
+
+
+def schedule_topk(conf_now, K: int):
+    """ZOS selection: l_r = candidates of r among the top K of the current order."""
+    c = np.ascontiguousarray(conf_now, dtype=np.float32)
+    R, g = c.shape
+    ell = np.zeros(R, dtype=np.int32)
+    rc = lib().oracle_schedule_topk(R, g, _ptr(c), int(K), _ptr(ell))
+    if rc != 0:
+        raise ValueError(f"oracle_schedule_topk rejected its arguments (code {rc})")
+    return ell
 
 
 # --------------------------------------------------------------------------- verify

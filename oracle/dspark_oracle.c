@@ -296,11 +296,9 @@ static int cand_cmp(const void* pa, const void* pb) {
   return 0;
 }
 
-int oracle_schedule(int R, int gamma, const float* c, const double* sps, int sps_len, int32_t* ell,
-                    double* diag /* [4]: B*, tau*, Theta*, n* (may be NULL) */,
-                    float* a_out /* [R, gamma] (may be NULL) */) {
-  if (R < 1 || gamma < 1) return 1;
-  if (sps_len < R * (1 + gamma) + 1) return 1;
+/* The candidates (r, j) with their survivals, sorted (a descending, ties by
+ * smaller j, then smaller r); a_out (may be NULL) receives a. */
+static cand* sorted_candidates(int R, int gamma, const float* c, float* a_out) {
   const int n = R * gamma;
   cand* cs = (cand*)malloc(sizeof(cand) * (size_t)n);
   for (int r = 0; r < R; ++r) {
@@ -319,9 +317,27 @@ int oracle_schedule(int R, int gamma, const float* c, const double* sps, int sps
     }
   }
   qsort(cs, (size_t)n, sizeof(cand), cand_cmp);
-  for (int r = 0; r < R; ++r) ell[r] = 0;
+  return cs;
+}
+
+static int rates_ok(int R, int gamma, const double* sps) {
   for (int b = R; b <= R * (1 + gamma); ++b)
-    if (!(sps[b] > 0.0) || !isfinite(sps[b])) return 3; /* step rates must be positive */
+    if (!(sps[b] > 0.0) || !isfinite(sps[b])) return 0; /* step rates must be positive */
+  return 1;
+}
+
+int oracle_schedule(int R, int gamma, const float* c, const double* sps, int sps_len, int32_t* ell,
+                    double* diag /* [4]: B*, tau*, Theta*, n* (may be NULL) */,
+                    float* a_out /* [R, gamma] (may be NULL) */) {
+  if (R < 1 || gamma < 1) return 1;
+  if (sps_len < R * (1 + gamma) + 1) return 1;
+  const int n = R * gamma;
+  cand* cs = sorted_candidates(R, gamma, c, a_out);
+  for (int r = 0; r < R; ++r) ell[r] = 0;
+  if (!rates_ok(R, gamma, sps)) {
+    free(cs);
+    return 3;
+  }
   int64_t tau = (int64_t)R << 48;
   int B = R;
   int taken = 0;
@@ -340,6 +356,60 @@ int oracle_schedule(int R, int gamma, const float* c, const double* sps, int sps
     diag[2] = ((double)tau * 0x1p-48) * sps[B];
     diag[3] = (double)taken;
   }
+  free(cs);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Zero-overhead scheduling, [P1] §5.2: the serving scheduler sets the next   */
+/* capacity K from confidences two steps old and then takes, among the        */
+/* current candidates, the top K by current survival -- so it never waits    */
+/* for this step's scheduling.  When K is predicted from the past, the early  */
+/* stop of Algorithm 1 is left out (to avoid a local optimum at a throughput  */
+/* cliff of an irregular SPS curve).                                          */
+/* Capacity: the candidates of the given (old) confidences in Algorithm 1's   */
+/* order, Theta_i = tau_i * SPS(R + i) for i = 0..R gamma taken candidates    */
+/* (same exact fixed-point tau and exact product comparison as Algorithm 1);  */
+/* K = the smallest i at which Theta_i is the global maximum.                 */
+/* Selection: l_r = number of candidates of r among the first min(K, R gamma) */
+/* of the current confidences' order.                                         */
+/* ------------------------------------------------------------------------- */
+int oracle_schedule_capacity(int R, int gamma, const float* c_old, const double* sps, int sps_len,
+                             int32_t* K, double* diag /* [4]: B*, tau*, Theta*, K (may be NULL) */) {
+  if (R < 1 || gamma < 1) return 1;
+  if (sps_len < R * (1 + gamma) + 1) return 1;
+  const int n = R * gamma;
+  cand* cs = sorted_candidates(R, gamma, c_old, NULL);
+  if (!rates_ok(R, gamma, sps)) {
+    free(cs);
+    return 3;
+  }
+  int64_t tau = (int64_t)R << 48, best_tau = tau;
+  int best = 0;
+  for (int i = 0; i < n; ++i) {
+    tau += (int64_t)nearbyint((double)cs[i].a * 0x1p48);
+    if (exact_greater(tau, sps[R + i + 1], best_tau, sps[R + best])) { /* strictly: first maximum */
+      best = i + 1;
+      best_tau = tau;
+    }
+  }
+  *K = best;
+  if (diag) {
+    diag[0] = (double)(R + best);
+    diag[1] = (double)best_tau * 0x1p-48;
+    diag[2] = ((double)best_tau * 0x1p-48) * sps[R + best];
+    diag[3] = (double)best;
+  }
+  free(cs);
+  return 0;
+}
+
+int oracle_schedule_topk(int R, int gamma, const float* c_now, int K, int32_t* ell) {
+  if (R < 1 || gamma < 1 || K < 0) return 1;
+  const int n = R * gamma;
+  cand* cs = sorted_candidates(R, gamma, c_now, NULL);
+  for (int r = 0; r < R; ++r) ell[r] = 0;
+  for (int i = 0; i < n && i < K; ++i) ell[cs[i].r] += 1;
   free(cs);
   return 0;
 }

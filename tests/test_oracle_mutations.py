@@ -38,6 +38,14 @@ MUTATIONS = [
      "if (!exact_greater(tau_i, sps[B], tau, sps[B])) break;"),
     ("survival not a product", "a = (j == 0) ? cj : a * cj;", "a = cj;"),
     ("bonus row one too early", "const int row = L + 1;", "const int row = L > 0 ? L : 1;"),
+    ("capacity keeps Algorithm 1's early stop",
+     "if (exact_greater(tau, sps[R + i + 1], best_tau, sps[R + best])) { /* strictly: first maximum */",
+     "if (!exact_greater(tau, sps[R + i + 1], best_tau, sps[R + best])) break;\n    { /* strictly: first maximum */"),
+    ("capacity reads the step rate one batch early",
+     "if (exact_greater(tau, sps[R + i + 1], best_tau, sps[R + best])) { /* strictly: first maximum */",
+     "if (exact_greater(tau, sps[R + i], best_tau, sps[R + best])) { /* strictly: first maximum */"),
+    ("top-k takes one candidate too many", "for (int i = 0; i < n && i < K; ++i) ell[cs[i].r] += 1;",
+     "for (int i = 0; i < n && i <= K; ++i) ell[cs[i].r] += 1;"),
     ("draft stream keyed by the wrong position",
      "(J->seed, req, (uint32_t)k,\n                                                    ORACLE_PURPOSE_DRAFT",
      "(J->seed, req, (uint32_t)(k + 1),\n                                                    ORACLE_PURPOSE_DRAFT"),
