@@ -203,11 +203,14 @@ class ClockSampler:
 class Round:
     """Device buffers of one round and the three C-ABI calls on one stream."""
 
-    def __init__(self, w: workload.Workload, seed: int, device):
+    def __init__(self, w: workload.Workload, seed: int, device, scheduler: str = "alg1",
+                 verify_layout: str = "padded"):
         import speculative_decoding_draft_05_gb300 as dspark
 
         self.dspark = dspark
         self.w, self.seed, self.device = w, seed, device
+        self.scheduler = scheduler
+        self.packed = verify_layout == "packed"
         inp = workload.generate(w, seed=seed, device=device)
         self.inp = inp
         R, g, V = w.R, w.gamma, w.V
@@ -227,6 +230,8 @@ class Round:
         self.ws_d = torch.empty(dspark.draft_workspace_bytes(R, g, V, w.r, w.torch_dtype), dtype=u8,
                                 device=device)
         self.ws_s = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
+        self.ws_s2 = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
+        self.K = torch.empty(1, dtype=i32, device=device)
         self.ws_v = torch.empty(dspark.verify_workspace_bytes(R, g, V), dtype=u8, device=device)
         # Target logits: the workload's target stand-in carries the Markov bias
         # along the draft's own tokens; run the (deterministic) draft once, untimed.
@@ -234,6 +239,19 @@ class Round:
         torch.cuda.synchronize(device)
         self.Z = self._target_logits()
         torch.cuda.synchronize(device)
+        if self.packed:
+            # An engine's packed target output: request r's rows 1..l_r+1 back
+            # to back.  l does not change between rounds here (the workload's
+            # confidences and step rates are fixed), so the rows are packed once.
+            self.schedule()
+            rows = (1 + self.ell.long())
+            self.offsets = torch.cat([torch.zeros(1, dtype=torch.long, device=device),
+                                      torch.cumsum(rows, 0)]).to(torch.int32)
+            req = torch.repeat_interleave(torch.arange(R, device=device), rows)
+            pos = torch.arange(int(rows.sum().item()), device=device) - self.offsets[:-1].long()[req]
+            self.Zp = self.Z[req, pos].contiguous()
+            del self.Z
+            torch.cuda.synchronize(device)
 
     def _target_logits(self):
         w, inp = self.w, self.inp
@@ -256,21 +274,43 @@ class Round:
                                         x=self.x, logp=self.logp, lse=self.lse, scores=self.scores,
                                         workspace=self.ws_d)
 
+    def schedule(self, conf=None, sps=None):
+        d = self.dspark
+        conf = self.inp["conf"] if conf is None else conf
+        sps = self.inp["sps"] if sps is None else sps
+        if self.scheduler == "zos":
+            # Zero-overhead scheduling: capacity from the confidences of two
+            # rounds back -- the same tensor here, the workload's confidences
+            # being fixed -- then the top K of the current ones.
+            d.dspark_schedule_capacity(conf, sps, K=self.K, diag=self.diag, workspace=self.ws_s)
+            d.dspark_schedule_topk(conf, self.K, ell=self.ell, workspace=self.ws_s2)
+        else:
+            d.dspark_schedule(conf, sps, ell=self.ell, diag=self.diag, workspace=self.ws_s)
+
     def step(self, seed=None, inputs=None):
         """One round; `seed` keys the round's Philox draws (default: the input seed);
         `inputs` is a list like input_tensors() (default: the resident inputs)."""
-        U, W1, W2, x0, conf, sps, Z = self.input_tensors() if inputs is None else inputs
+        ins = self.input_tensors() if inputs is None else inputs
+        U, W1, W2, x0, conf, sps, Z = ins[:7]
         d = self.dspark
         seed = self.seed if seed is None else seed
         d.dspark_draft_sample(U, W1, W2, x0, self.w.T, seed, x=self.x, logp=self.logp, lse=self.lse,
                               scores=self.scores, workspace=self.ws_d)
-        d.dspark_schedule(conf, sps, ell=self.ell, diag=self.diag, workspace=self.ws_s)
-        d.dspark_verify(self.x, self.logp, self.lse, self.scores, Z, self.ell, self.w.T, seed,
-                        n_acc=self.n_acc, tokens=self.tokens, n_emit=self.n_emit, cstar=self.cstar,
-                        lse_t=self.lse_t, workspace=self.ws_v)
+        self.schedule(conf, sps)
+        if self.packed:
+            d.dspark_verify_packed(self.x, self.logp, self.lse, self.scores, Z, ins[7], self.ell,
+                                   self.w.T, seed, n_acc=self.n_acc, tokens=self.tokens,
+                                   n_emit=self.n_emit, cstar=self.cstar, lse_t=self.lse_t,
+                                   workspace=self.ws_v)
+        else:
+            d.dspark_verify(self.x, self.logp, self.lse, self.scores, Z, self.ell, self.w.T, seed,
+                            n_acc=self.n_acc, tokens=self.tokens, n_emit=self.n_emit,
+                            cstar=self.cstar, lse_t=self.lse_t, workspace=self.ws_v)
 
     def input_tensors(self):
         i = self.inp
+        if self.packed:
+            return [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"], self.Zp, self.offsets]
         return [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"], self.Z]
 
     def result_tensors(self):
@@ -289,7 +329,7 @@ def draft_tile_flops(w: workload.Workload) -> int:
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample_round(w, inp_cpu, req, seed, nthreads):
+def oracle_sample_round(w, inp_cpu, req, seed, nthreads, scheduler="alg1"):
     """Time one oracle round on the requests `req` (draft + full schedule + verify)."""
     import oracle
 
@@ -308,8 +348,12 @@ def oracle_sample_round(w, inp_cpu, req, seed, nthreads):
     else:
         Z = workload.target_logits(w, inp_cpu["U"][req], seed, requests=req)
     t0 = time.perf_counter()
-    os_ = oracle.schedule(inp_cpu["conf"].numpy(), inp_cpu["sps"].numpy())
-    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), os_["ell"][req], w.T, seed,
+    conf = inp_cpu["conf"].numpy()
+    if scheduler == "zos":
+        ell = oracle.schedule_topk(conf, oracle.schedule_capacity(conf, inp_cpu["sps"].numpy())["K"])
+    else:
+        ell = oracle.schedule(conf, inp_cpu["sps"].numpy())["ell"]
+    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), ell[req], w.T, seed,
                        req_ids=req, nthreads=nthreads)
     t_rest = time.perf_counter() - t0
     return t_draft + t_rest, int(ov["n_emit"].sum())
@@ -357,11 +401,11 @@ def run_reference(args, w, rank, world):
     n = max(1, sample_size(w, nthreads, target_s=120.0 / max(1, args.steps + args.warmup)))
     req = list(range(n))
     for _ in range(args.warmup):
-        oracle_sample_round(w, inp, req, args.seed, nthreads)
+        oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler)
     times = []
     emitted = 0
     for _ in range(args.steps):
-        t, e = oracle_sample_round(w, inp, req, args.seed, nthreads)
+        t, e = oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler)
         times.append(t)
         emitted += e
     tot = sum(times)
@@ -370,7 +414,8 @@ def run_reference(args, w, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(workload.describe(w), seed=args.seed, sample_requests=n),
+            "config": dict(workload.describe(w), seed=args.seed, scheduler=args.scheduler,
+                           sample_requests=n),
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": nthreads,
                              "kind": "oracle",
                              "sample": f"{n} of {w.R} requests per step (all positions, full V) "
@@ -391,7 +436,7 @@ def run_ours(args, w, rank, world, local):
     init_dist(world, "nccl")
     dspark.binding.load()
     stream = torch.cuda.current_stream(device)
-    rnd = Round(w, args.seed, device)
+    rnd = Round(w, args.seed, device, scheduler=args.scheduler, verify_layout=args.verify_layout)
     seeds = [args.seed + i for i in range(args.steps)]  # one Philox key per round
     for i in range(args.warmup):
         rnd.step(args.seed + i)
@@ -520,12 +565,13 @@ def run_ours(args, w, rank, world, local):
                 "ms_per_step_with_kernel_events": ms_prof / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
                 if w.dtype == "bf16" else "f32", "data": "synthetic",
-                "config": dict(workload.describe(w), seed=args.seed,
+                "config": dict(workload.describe(w), seed=args.seed, scheduler=args.scheduler,
+                               verify_layout=args.verify_layout,
                                parallelism="replicas" if world > 1 else "single",
                                l2="inputs larger than L2 (U %.2f GB, scores %.2f GB, Z %.2f GB > 129 MB)" % (
                                    w.R * w.gamma * w.V * (2 if w.dtype == "bf16" else 4) / 1e9,
                                    w.R * w.gamma * w.V * 4 / 1e9,
-                                   w.R * (w.gamma + 1) * w.V * (2 if w.dtype == "bf16" else 4) / 1e9)),
+                                   rnd.input_tensors()[6].numel() * rnd.input_tensors()[6].element_size() / 1e9)),
                 "roofline": roofline, "cpu_baseline": out,
                 "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -549,6 +595,10 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workload.ORDER)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scheduler", choices=["alg1", "zos"], default="alg1",
+                    help="alg1: Algorithm 1 (default); zos: zero-overhead capacity + top-K")
+    ap.add_argument("--verify-layout", choices=["padded", "packed"], default="padded",
+                    help="target logits padded [R, gamma+1, V] (default) or packed rows + offsets")
     ap.add_argument("--R", type=int, default=None, help="override the workload's request count")
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
     args = ap.parse_args(argv)

@@ -142,6 +142,38 @@ int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, in
                     void* stream);
 
 /* ------------------------------------------------------------------------
+ * Zero-overhead scheduling ([summary] §5.2).  The serving scheduler sets the
+ * next capacity K from confidences two steps old and takes, among the current
+ * candidates, the top K by current survival, so it never waits on this step's
+ * scheduling; when K is predicted from the past, Algorithm 1's early stop is
+ * left out, so that a throughput cliff of an irregular SPS curve does not trap
+ * it at a local optimum.  Two calls:
+ *
+ * dspark_schedule_capacity -- K from conf_old: the candidates in Algorithm
+ *   1's order (survival a descending, ties by smaller j, then smaller r),
+ *   Theta_i = tau_i * sps[R + i] for i = 0 .. R gamma taken candidates (tau_i
+ *   exact in 2^-48 fixed point, Theta compared exactly, as in
+ *   dspark_schedule); K = the smallest i at which Theta_i is the maximum.
+ *   K >= dspark_schedule's count, with equality when Theta is unimodal along
+ *   the path.
+ *   conf_old [R, gamma] float; sps as for dspark_schedule;
+ *   K    [1] int32 (device)       out: the capacity
+ *   diag [4] double or NULL       out: R + K, tau*, Theta*, K
+ * dspark_schedule_topk -- l_r = number of candidates of request r among the
+ *   first min(K, R gamma) of conf's order (K read from device memory, so it
+ *   can come straight from dspark_schedule_capacity).  K < 0 flags
+ *   DSPARK_DEV_BAD_INPUT and counts as 0.
+ *   conf [R, gamma] float; K [1] int32 (device); ell [R] int32 out.
+ * Both take a workspace of dspark_schedule_workspace_bytes(R, gamma) bytes
+ * (256-byte aligned) and the limits of dspark_schedule.
+ * ---------------------------------------------------------------------- */
+int dspark_schedule_capacity(const float* conf_old, const double* sps, int sps_len, int R,
+                             int gamma, int32_t* K, double* diag, void* workspace,
+                             size_t workspace_bytes, void* stream);
+int dspark_schedule_topk(const float* conf, const int32_t* K, int R, int gamma, int32_t* ell,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * dspark_verify -- standard rejection sampling over the scheduled prefixes
  * ([summary] opening bullets, §3; [notes] "배경") and the soft label
  * ([summary] §3.2.1).  With p^t_j = softmax(Z_j / T) and
@@ -172,6 +204,31 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
                   float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
                   int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_verify_packed -- dspark_verify over a packed target-logit buffer.
+ * A serving engine that lets each request verify a different length runs its
+ * target on the concatenated rows of all requests ([summary] §5.3: tokens of
+ * the requests are laid out flat, with sequence boundaries passed alongside,
+ * to avoid padding), so its target logits come packed: request r occupies
+ * rows row_offsets[r] .. row_offsets[r] + l_r of Zp (positions 1 .. l_r + 1;
+ * rows beyond l_r + 1 up to row_offsets[r + 1] may exist and are not read).
+ * Same arithmetic, outputs and workspace as dspark_verify; only the target
+ * rows are addressed through the offsets.
+ *
+ * Zp          [n_rows, V] bf16 or fp32, 16-byte aligned
+ * row_offsets [R + 1]     int32 (device), non-decreasing,
+ *                         row_offsets[r + 1] - row_offsets[r] >= 1 + l_r,
+ *                         row_offsets[R] <= n_rows
+ * n_rows      rows of Zp (>= R).  Offsets that break these rules flag
+ *             DSPARK_DEV_BAD_INPUT; every row index is clamped into Zp.
+ * ---------------------------------------------------------------------- */
+int dspark_verify_packed(const int32_t* x, const float* logp, const float* lse,
+                         const float* scores, const void* Zp, int dtype, const int32_t* row_offsets,
+                         int n_rows, const int32_t* ell, int R, int gamma, int V,
+                         float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
+                         int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * dspark_verify_noalloc -- dspark_verify for callers that cannot allocate

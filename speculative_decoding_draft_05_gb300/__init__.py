@@ -12,7 +12,10 @@ from .binding import (  # noqa: F401
     dspark_profile_stop,
     dspark_read_device_status,
     dspark_schedule,
+    dspark_schedule_capacity,
+    dspark_schedule_topk,
     dspark_verify,
+    dspark_verify_packed,
     draft_workspace_bytes,
     schedule_workspace_bytes,
     verify_workspace_bytes,
@@ -21,7 +24,10 @@ from .binding import (  # noqa: F401
 __all__ = [
     "dspark_draft_sample",
     "dspark_schedule",
+    "dspark_schedule_capacity",
+    "dspark_schedule_topk",
     "dspark_verify",
+    "dspark_verify_packed",
     "dspark_read_device_status",
     "dspark_profile_start",
     "dspark_profile_stop",

@@ -57,10 +57,17 @@ def load() -> ctypes.CDLL:
     L.dspark_schedule_workspace_bytes.restype = SZ
     L.dspark_schedule.argtypes = [P, P, I, I, I, P, P, P, SZ, P]
     L.dspark_schedule.restype = I
+    L.dspark_schedule_capacity.argtypes = [P, P, I, I, I, P, P, P, SZ, P]
+    L.dspark_schedule_capacity.restype = I
+    L.dspark_schedule_topk.argtypes = [P, P, I, I, P, P, SZ, P]
+    L.dspark_schedule_topk.restype = I
     L.dspark_verify_workspace_bytes.argtypes = [I, I, I]
     L.dspark_verify_workspace_bytes.restype = SZ
     L.dspark_verify.argtypes = [P, P, P, P, P, I, P, I, I, I, F, U64, P, P, P, P, P, P, SZ, P]
     L.dspark_verify.restype = I
+    L.dspark_verify_packed.argtypes = [P, P, P, P, P, I, P, I, P, I, I, I, F, U64, P, P, P, P, P, P,
+                                       SZ, P]
+    L.dspark_verify_packed.restype = I
     L.dspark_read_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     L.dspark_read_device_status.restype = I
     L.dspark_profile_start.argtypes = []
@@ -161,6 +168,38 @@ def dspark_schedule(conf, sps, *, ell=None, diag=None, workspace=None, stream=No
     return dict(ell=ell, diag=diag, workspace=ws)
 
 
+def dspark_schedule_capacity(conf_old, sps, *, K=None, diag=None, workspace=None,
+                             stream=None) -> dict:
+    """Zero-overhead scheduling, capacity: K from old confidences (no early stop)."""
+    L = load()
+    R, g = conf_old.shape
+    dev = conf_old.device
+    K = torch.empty(1, dtype=torch.int32, device=dev) if K is None else K
+    diag = torch.empty(4, dtype=torch.float64, device=dev) if diag is None else diag
+    ws = _workspace(schedule_workspace_bytes(R, g), dev, workspace)
+    st = L.dspark_schedule_capacity(_dev(conf_old, "conf_old", torch.float32),
+                                    _dev(sps, "sps", torch.float64), sps.numel(), R, g,
+                                    _dev(K, "K", torch.int32, (1,)),
+                                    _dev(diag, "diag", torch.float64, (4,)), ws.data_ptr(),
+                                    ws.numel(), _stream(stream))
+    _check("dspark_schedule_capacity", st)
+    return dict(K=K, diag=diag, workspace=ws)
+
+
+def dspark_schedule_topk(conf, K, *, ell=None, workspace=None, stream=None) -> dict:
+    """Zero-overhead scheduling, selection: the top K (device int32 [1]) of conf's order."""
+    L = load()
+    R, g = conf.shape
+    dev = conf.device
+    ell = torch.empty(R, dtype=torch.int32, device=dev) if ell is None else ell
+    ws = _workspace(schedule_workspace_bytes(R, g), dev, workspace)
+    st = L.dspark_schedule_topk(_dev(conf, "conf", torch.float32), _dev(K, "K", torch.int32, (1,)),
+                                R, g, _dev(ell, "ell", torch.int32, (R,)), ws.data_ptr(),
+                                ws.numel(), _stream(stream))
+    _check("dspark_schedule_topk", st)
+    return dict(ell=ell, workspace=ws)
+
+
 def dspark_verify(x, logp, lse, scores, Z, ell, temperature: float, seed: int, *, n_acc=None,
                   tokens=None, n_emit=None, cstar=None, lse_t=None, want_lse_t=True,
                   workspace=None, stream=None) -> dict:
@@ -186,6 +225,38 @@ def dspark_verify(x, logp, lse, scores, Z, ell, temperature: float, seed: int, *
         None if lse_t is None else _dev(lse_t, "lse_t", torch.float32, (R, g + 1)),
         ws.data_ptr(), ws.numel(), _stream(stream))
     _check("dspark_verify", st)
+    return dict(n_acc=n_acc, tokens=tokens, n_emit=n_emit, cstar=cstar, lse_t=lse_t, workspace=ws)
+
+
+def dspark_verify_packed(x, logp, lse, scores, Zp, row_offsets, ell, temperature: float,
+                         seed: int, *, n_acc=None, tokens=None, n_emit=None, cstar=None,
+                         lse_t=None, want_lse_t=True, workspace=None, stream=None) -> dict:
+    """dspark_verify with packed target logits: Zp [n_rows, V]; request r's rows
+    for positions 1..l_r+1 start at row_offsets[r] (int32 [R + 1], on the device)."""
+    L = load()
+    R, g = x.shape
+    V = scores.shape[2]
+    dev = x.device
+    n_rows = Zp.shape[0]
+    n_acc = torch.empty(R, dtype=torch.int32, device=dev) if n_acc is None else n_acc
+    tokens = torch.empty(R, g + 1, dtype=torch.int32, device=dev) if tokens is None else tokens
+    n_emit = torch.empty(R, dtype=torch.int32, device=dev) if n_emit is None else n_emit
+    cstar = torch.empty(R, g, dtype=torch.float32, device=dev) if cstar is None else cstar
+    if lse_t is None and want_lse_t:
+        lse_t = torch.empty(R, g + 1, dtype=torch.float32, device=dev)
+    ws = _workspace(verify_workspace_bytes(R, g, V), dev, workspace)
+    st = L.dspark_verify_packed(
+        _dev(x, "x", torch.int32, (R, g)), _dev(logp, "logp", torch.float32, (R, g)),
+        _dev(lse, "lse", torch.float32, (R, g)), _dev(scores, "scores", torch.float32, (R, g, V)),
+        _dev(Zp, "Zp", None, (n_rows, V)), _dtype_code(Zp),
+        _dev(row_offsets, "row_offsets", torch.int32, (R + 1,)), n_rows,
+        _dev(ell, "ell", torch.int32, (R,)), R, g, V, float(temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(n_acc, "n_acc", torch.int32, (R,)),
+        _dev(tokens, "tokens", torch.int32, (R, g + 1)), _dev(n_emit, "n_emit", torch.int32, (R,)),
+        _dev(cstar, "cstar", torch.float32, (R, g)),
+        None if lse_t is None else _dev(lse_t, "lse_t", torch.float32, (R, g + 1)),
+        ws.data_ptr(), ws.numel(), _stream(stream))
+    _check("dspark_verify_packed", st)
     return dict(n_acc=n_acc, tokens=tokens, n_emit=n_emit, cstar=cstar, lse_t=lse_t, workspace=ws)
 
 

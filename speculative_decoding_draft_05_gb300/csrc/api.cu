@@ -233,25 +233,75 @@ int dspark_schedule(const float* conf, const double* sps, int sps_len, int R, in
   return DSPARK_OK;
 }
 
+static int schedule_args(const float* conf, int R, int gamma, void* workspace,
+                         size_t workspace_bytes) {
+  if (!conf) return DSPARK_ERR_INVALID_ARG;
+  if (R <= 0 || gamma <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (gamma > 64 || (long long)R * gamma > 16384) return DSPARK_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < dspark_schedule_workspace_bytes(R, gamma) ||
+      ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  return DSPARK_OK;
+}
+
+int dspark_schedule_capacity(const float* conf_old, const double* sps, int sps_len, int R,
+                             int gamma, int32_t* K, double* diag, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!sps || !K) return DSPARK_ERR_INVALID_ARG;
+  if (R > 0 && gamma > 0 && (long long)sps_len < (long long)R * (1 + gamma) + 1)
+    return DSPARK_ERR_INVALID_ARG;
+  int st = schedule_args(conf_old, R, gamma, workspace, workspace_bytes);
+  if (st != DSPARK_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* status = (int*)workspace;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_capacity status reset");
+  unsigned long long* sorted = (unsigned long long*)((char*)workspace + 256);
+  prof_begin(kKindSchedule, s);
+  e = launch_schedule_rank(conf_old, R, gamma, sorted, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_rank");
+  prof_begin(kKindSchedule, s);
+  e = launch_schedule_capacity(sorted, sps, R, gamma, K, diag, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_capacity");
+  return DSPARK_OK;
+}
+
+int dspark_schedule_topk(const float* conf, const int32_t* K, int R, int gamma, int32_t* ell,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!K || !ell) return DSPARK_ERR_INVALID_ARG;
+  int st = schedule_args(conf, R, gamma, workspace, workspace_bytes);
+  if (st != DSPARK_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int* status = (int*)workspace;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_topk status reset");
+  unsigned long long* sorted = (unsigned long long*)((char*)workspace + 256);
+  prof_begin(kKindSchedule, s);
+  e = launch_schedule_rank(conf, R, gamma, sorted, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_rank");
+  prof_begin(kKindSchedule, s);
+  e = launch_schedule_topk(sorted, K, R, gamma, ell, status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_topk");
+  return DSPARK_OK;
+}
+
 size_t dspark_verify_workspace_bytes(int R, int gamma, int V) {
   if (R <= 0 || gamma <= 0 || V <= 0) return 0;
   return verify_scratch_layout(R, gamma, V).total;
 }
 
-int dspark_verify(const int32_t* x, const float* logp, const float* lse, const float* scores,
-                  const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
-                  float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
-                  int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
-                  size_t workspace_bytes, void* stream) {
-  if (!x || !logp || !lse || !scores || !Z || !ell || !n_acc || !tokens || !n_emit || !cstar)
-    return DSPARK_ERR_INVALID_ARG;
-  int st = check_common(R, gamma, V, temperature, dtype);
-  if (st != DSPARK_OK) return st;
-  if (!aligned16(Z) || !aligned16(scores)) return DSPARK_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < dspark_verify_workspace_bytes(R, gamma, V) ||
-      ((uintptr_t)workspace & 255u))
-    return DSPARK_ERR_WORKSPACE;
-  cudaStream_t s = (cudaStream_t)stream;
+}  // extern "C"
+
+// The verify launches on `workspace` (already validated); zr addresses Z.
+static int verify_enqueue(const int32_t* x, const float* logp, const float* lse,
+                          const float* scores, const void* Z, int dtype, const int32_t* ell, int R,
+                          int gamma, int V, float temperature, uint64_t seed, int32_t* n_acc,
+                          int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
+                          void* workspace, ZRows zr, cudaStream_t s, const char* what) {
   char* ws = (char*)workspace;
   int* status = (int*)ws;
   const VerifyScratch lay = verify_scratch_layout(R, gamma, V);
@@ -259,20 +309,68 @@ int dspark_verify(const int32_t* x, const float* logp, const float* lse, const f
   int* acc_ws = (int*)(ws + lay.acc);
   float2* partials = (float2*)(ws + lay.partials);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
-  if (e != cudaSuccess) return cuda_fail(e, "verify status reset");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   const float invT = 1.0f / temperature;
   prof_begin(kKindVerifyRows, s);
   e = launch_verify_rows(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, cstar,
                          lse_t_ws, acc_ws, (uint32_t*)(ws + lay.list), (int*)(ws + lay.count),
-                         status, s);
+                         status, zr, s);
   prof_end(s);
-  if (e != cudaSuccess) return cuda_fail(e, "verify_rows");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   prof_begin(kKindVerifyFinish, s);
   e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                           partials, n_acc, tokens, n_emit, cstar, lse_t, s);
+                           partials, n_acc, tokens, n_emit, cstar, lse_t, zr, s);
   prof_end(s);
-  if (e != cudaSuccess) return cuda_fail(e, "verify_finish");
+  if (e != cudaSuccess) return cuda_fail(e, what);
   return DSPARK_OK;
+}
+
+static int verify_args(const int32_t* x, const float* logp, const float* lse, const float* scores,
+                       const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
+                       float temperature, const int32_t* n_acc, const int32_t* tokens,
+                       const int32_t* n_emit, const float* cstar) {
+  if (!x || !logp || !lse || !scores || !Z || !ell || !n_acc || !tokens || !n_emit || !cstar)
+    return DSPARK_ERR_INVALID_ARG;
+  int st = check_common(R, gamma, V, temperature, dtype);
+  if (st != DSPARK_OK) return st;
+  if (!aligned16(Z) || !aligned16(scores)) return DSPARK_ERR_INVALID_ARG;
+  return DSPARK_OK;
+}
+
+extern "C" {
+
+int dspark_verify(const int32_t* x, const float* logp, const float* lse, const float* scores,
+                  const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
+                  float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
+                  int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  int st = verify_args(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, temperature, n_acc, tokens,
+                       n_emit, cstar);
+  if (st != DSPARK_OK) return st;
+  if (!workspace || workspace_bytes < dspark_verify_workspace_bytes(R, gamma, V) ||
+      ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  return verify_enqueue(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, temperature, seed, n_acc,
+                        tokens, n_emit, cstar, lse_t, workspace, ZRows{nullptr, gamma, 0},
+                        (cudaStream_t)stream, "verify");
+}
+
+int dspark_verify_packed(const int32_t* x, const float* logp, const float* lse,
+                         const float* scores, const void* Zp, int dtype, const int32_t* row_offsets,
+                         int n_rows, const int32_t* ell, int R, int gamma, int V,
+                         float temperature, uint64_t seed, int32_t* n_acc, int32_t* tokens,
+                         int32_t* n_emit, float* cstar, float* lse_t, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  int st = verify_args(x, logp, lse, scores, Zp, dtype, ell, R, gamma, V, temperature, n_acc, tokens,
+                       n_emit, cstar);
+  if (st != DSPARK_OK) return st;
+  if (!row_offsets || n_rows < R) return DSPARK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < dspark_verify_workspace_bytes(R, gamma, V) ||
+      ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  return verify_enqueue(x, logp, lse, scores, Zp, dtype, ell, R, gamma, V, temperature, seed, n_acc,
+                        tokens, n_emit, cstar, lse_t, workspace, ZRows{row_offsets, gamma, n_rows},
+                        (cudaStream_t)stream, "verify_packed");
 }
 
 int dspark_read_device_status(const void* workspace, void* stream, int32_t* out) {
@@ -336,27 +434,9 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != DSPARK_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  char* ws = (char*)scratch;
-  int* status = (int*)ws;
-  float* lse_t_ws = (float*)(ws + lay.lse_t);
-  int* acc_ws = (int*)(ws + lay.acc);
-  float2* partials = (float2*)(ws + lay.partials);
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
-  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc status reset");
-  const float invT = 1.0f / temperature;
-  prof_begin(kKindVerifyRows, s);
-  e = launch_verify_rows(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, cstar,
-                         lse_t_ws, acc_ws, (uint32_t*)(ws + lay.list), (int*)(ws + lay.count),
-                         status, s);
-  prof_end(s);
-  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc rows");
-  prof_begin(kKindVerifyFinish, s);
-  e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                           partials, n_acc, tokens, n_emit, cstar, lse_t, s);
-  prof_end(s);
-  if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc finish");
-  return DSPARK_OK;
+  return verify_enqueue(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, temperature, seed, n_acc,
+                        tokens, n_emit, cstar, lse_t, scratch, ZRows{nullptr, gamma, 0},
+                        (cudaStream_t)stream, "verify_noalloc");
 }
 
 int dspark_profile_start(void) {

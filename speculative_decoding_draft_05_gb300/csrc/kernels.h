@@ -66,6 +66,30 @@ cudaError_t launch_schedule_rank(const float* conf, int R, int gamma, unsigned l
 cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double* sps, int R,
                                  int gamma, int32_t* ell, double* diag, int* status,
                                  cudaStream_t s);
+// Zero-overhead scheduling: capacity K (first global Theta maximum along the
+// sorted order, written to device memory), then the top K of a sorted order.
+cudaError_t launch_schedule_capacity(const unsigned long long* sorted, const double* sps, int R,
+                                     int gamma, int32_t* K, double* diag, int* status,
+                                     cudaStream_t s);
+cudaError_t launch_schedule_topk(const unsigned long long* sorted, const int32_t* K, int R,
+                                 int gamma, int32_t* ell, int* status, cudaStream_t s);
+
+// Where the target row of request r at (1-based) position j starts, in rows
+// of V elements: the padded [R, gamma+1, V] layout (off == nullptr) or a packed
+// [n_rows, V] buffer whose request r occupies rows off[r] .. off[r] + l_r
+// (positions 1 .. l_r + 1), the index clamped into the buffer.
+struct ZRows {
+  const int32_t* off;  // [R + 1] row offsets, or nullptr for the padded layout
+  int gamma, n_rows;
+#ifdef __CUDACC__
+  __device__ __forceinline__ size_t row(int r, int j) const {
+    if (!off) return (size_t)r * (gamma + 1) + (j - 1);
+    long long q = (long long)off[r] + (j - 1);
+    q = q < 0 ? 0 : (q >= n_rows ? n_rows - 1 : q);
+    return (size_t)q;
+  }
+#endif
+};
 
 // LSE^t, c* and the accept flag of every scheduled row (r, j <= l_r).
 // row_list ([R * gamma] u32) and *row_count are scratch: the list of those rows
@@ -74,7 +98,7 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
                                float* lse_t_ws, int* acc_ws, uint32_t* row_list, int* row_count,
-                               int* status, cudaStream_t s);
+                               int* status, ZRows zr, cudaStream_t s);
 
 // The drawn token: verify_draw over vocab chunks, then verify_emit per request.
 int verify_draw_chunks(int V);
@@ -83,7 +107,7 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
                                  int V, float invT, uint64_t seed, const float* lse_t_ws,
                                  const int* acc_ws, float2* partials, int32_t* n_acc,
                                  int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
-                                 cudaStream_t s);
+                                 ZRows zr, cudaStream_t s);
 
 // Kernel kinds for the optional event timing (dspark_profile_*).
 enum KernelKind {

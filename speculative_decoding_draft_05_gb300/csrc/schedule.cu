@@ -22,6 +22,12 @@
 //                  parallel (an exact integer comparison of the products
 //                  tau * SPS, no floating point), a block-wide minimum for the
 //                  first non-improvement, and the per-request counts l_r.
+//
+// Zero-overhead scheduling (same summary, §5.2): the capacity K comes from
+// confidences two steps old without the early stop -- schedule_capacity is
+// schedule_scan's exact Theta of every prefix followed by a block-wide
+// argmax (first maximum) -- and the selection takes the top K of the current
+// order (schedule_topk, one CTA).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -238,6 +244,128 @@ schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double
   }
 }
 
+// Exclusive prefix of the fixed-point survivals of this thread's kPerThread
+// sorted keys (staged in shared memory), as in schedule_scan.
+__device__ __forceinline__ long long stage_and_prefix(const unsigned long long* __restrict__ sorted,
+                                                      int n, unsigned long long* stage,
+                                                      long long* warp_tot,
+                                                      unsigned long long (&k)[kPerThread]) {
+  const int tid = threadIdx.x, base = tid * kPerThread;
+  for (int i = tid; i < kMaxCandidates; i += kSchedThreads) stage[i] = i < n ? sorted[i] : ~0ull;
+  __syncthreads();
+  long long local = 0;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    k[e] = stage[base + e];
+    if (base + e < n) local += fixed_survival(k[e]);
+  }
+  const int lane = tid & 31, warp = tid >> 5;
+  long long incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    long long t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  return (incl - local) + (warp > 0 ? warp_tot[warp - 1] : 0ll);
+}
+
+// The better of two (tau, number taken) points by Theta = tau * sps[R + k],
+// exactly; a tie goes to the smaller k (the first maximum).  k < 0: no point.
+__device__ __forceinline__ void better_theta(long long& t, int& k, long long t2, int k2,
+                                             const double* __restrict__ sps, int R, int* status) {
+  if (k2 < 0) return;
+  if (k < 0 || exact_greater(t2, sps[R + k2], t, sps[R + k], status) ||
+      (k2 < k && !exact_greater(t, sps[R + k], t2, sps[R + k2], status))) {
+    t = t2;
+    k = k2;
+  }
+}
+
+__global__ void __launch_bounds__(kSchedThreads)
+schedule_capacity_kernel(const unsigned long long* __restrict__ sorted,
+                         const double* __restrict__ sps, int R, int gamma,
+                         int32_t* __restrict__ K_out, double* __restrict__ diag,
+                         int* __restrict__ status) {
+  __shared__ long long warp_tot[kSchedThreads / 32];
+  __shared__ long long red_t[kSchedThreads / 32];
+  __shared__ int red_k[kSchedThreads / 32];
+  extern __shared__ unsigned long long stage[];  // [kMaxCandidates]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = R * gamma, base = tid * kPerThread;
+  unsigned long long k[kPerThread];
+  long long run = stage_and_prefix(sorted, n, stage, warp_tot, k);
+  const long long tau0 = (long long)R << 48;
+  // this thread's best prefix; thread 0 also holds the empty one (k = 0)
+  long long bt = tau0;
+  int bk = tid == 0 ? 0 : -1;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    const int i = base + e;
+    if (i < n) {
+      run += fixed_survival(k[e]);
+      better_theta(bt, bk, tau0 + run, i + 1, sps, R, status);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const long long t2 = __shfl_xor_sync(0xffffffffu, bt, o);
+    const int k2 = __shfl_xor_sync(0xffffffffu, bk, o);
+    better_theta(bt, bk, t2, k2, sps, R, status);
+  }
+  if (lane == 0) {
+    red_t[warp] = bt;
+    red_k[warp] = bk;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bt = red_t[lane];
+    bk = red_k[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const long long t2 = __shfl_xor_sync(0xffffffffu, bt, o);
+      const int k2 = __shfl_xor_sync(0xffffffffu, bk, o);
+      better_theta(bt, bk, t2, k2, sps, R, status);
+    }
+    if (lane == 0) {
+      K_out[0] = bk;
+      if (diag) {
+        diag[0] = (double)(R + bk);
+        diag[1] = __ll2double_rn(bt) * 0x1p-48;
+        diag[2] = __dmul_rn(__ll2double_rn(bt) * 0x1p-48, sps[R + bk]);
+        diag[3] = (double)bk;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSchedThreads)
+schedule_topk_kernel(const unsigned long long* __restrict__ sorted, const int32_t* __restrict__ K,
+                     int R, int gamma, int32_t* __restrict__ ell, int* __restrict__ status) {
+  const int n = R * gamma;
+  for (int r = threadIdx.x; r < R; r += kSchedThreads) ell[r] = 0;
+  __syncthreads();
+  int k = *K;
+  if (k < 0) {
+    if (threadIdx.x == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
+    k = 0;
+  }
+  if (k > n) k = n;
+  for (int i = threadIdx.x; i < k; i += kSchedThreads)
+    atomicAdd(&ell[(int)(sorted[i] & 0xffffu)], 1);
+}
+
 int sm_count_sched() {
   static int n = 0;
   if (n == 0) {
@@ -289,6 +417,29 @@ cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double*
     attr_set = true;
   }
   schedule_scan_kernel<<<1, kSchedThreads, smem, s>>>(sorted, sps, R, gamma, ell, diag, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule_capacity(const unsigned long long* sorted, const double* sps, int R,
+                                     int gamma, int32_t* K, double* diag, int* status,
+                                     cudaStream_t s) {
+  if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
+  const size_t smem = kMaxCandidates * sizeof(unsigned long long);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(schedule_capacity_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  schedule_capacity_kernel<<<1, kSchedThreads, smem, s>>>(sorted, sps, R, gamma, K, diag, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule_topk(const unsigned long long* sorted, const int32_t* K, int R,
+                                 int gamma, int32_t* ell, int* status, cudaStream_t s) {
+  if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
+  schedule_topk_kernel<<<1, kSchedThreads, 0, s>>>(sorted, K, R, gamma, ell, status);
   return cudaGetLastError();
 }
 

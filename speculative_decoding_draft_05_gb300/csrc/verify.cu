@@ -116,7 +116,7 @@ constexpr int kIndexThreads = 1024;
 
 __global__ void __launch_bounds__(kIndexThreads)
 verify_index_kernel(const int32_t* __restrict__ ell, int R, int gamma, uint32_t* __restrict__ list,
-                    int* __restrict__ count, int* __restrict__ status) {
+                    int* __restrict__ count, int* __restrict__ status, ZRows zr) {
   __shared__ int warp_tot[kIndexThreads / 32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -125,6 +125,10 @@ verify_index_kernel(const int32_t* __restrict__ ell, int R, int gamma, uint32_t*
   for (int base = 0; base < R; base += kIndexThreads) {
     const int r = base + threadIdx.x;
     const int L = r < R ? clamp_ell(ell, r, gamma, status, true) : 0;
+    if (zr.off && r < R) {  // a packed Z must hold rows 1 .. l_r + 1 of every request
+      const long long a = zr.off[r], b = zr.off[r + 1];
+      if (a < 0 || b - a < 1 + L || b > zr.n_rows) flag_status(status, DSPARK_DEV_BAD_INPUT);
+    }
     int v = L;  // inclusive scan within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -227,7 +231,7 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
                           const T* __restrict__ Z, const uint32_t* __restrict__ list,
                           const int* __restrict__ count, int gamma, int V, float invT,
                           uint64_t seed, float* __restrict__ cstar, float* __restrict__ lse_t_ws,
-                          int* __restrict__ acc_ws, int* __restrict__ status) {
+                          int* __restrict__ acc_ws, int* __restrict__ status, ZRows zr) {
   __shared__ float rm[kRowWarps], rs[kRowWarps];
   __shared__ float s_ld;
   constexpr int kRowUnroll = row_unroll<T>();  // 64 bytes of Z per thread in flight
@@ -238,7 +242,7 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
     const uint32_t item_next = i + (int)gridDim.x < n_rows ? list[i + gridDim.x] : 0u;
     const int r = (int)(item / (uint32_t)gamma), j = (int)(item - (uint32_t)r * gamma) + 1;
     const size_t rj = (size_t)r * gamma + (j - 1);
-    const T* z = Z + ((size_t)r * (gamma + 1) + (j - 1)) * V;
+    const T* z = Z + zr.row(r, j) * V;
     const float* srow = scores + rj * V;
     int xj = 0;
     float ld0 = 0.0f, lp = 0.0f;
@@ -351,7 +355,8 @@ __global__ void __launch_bounds__(kDrawThreads, 5)
 verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
                    const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
                    float invT, uint64_t seed, const float* __restrict__ lse_t_ws,
-                   const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks) {
+                   const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks,
+                   ZRows zr) {
   __shared__ float rk[kDrawThreads / 32];
   __shared__ int ri[kDrawThreads / 32];
   __shared__ int s_n;
@@ -367,7 +372,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   const int n = s_n;
   const bool residual = n < L;
   const int row = n + 1;  // 1-based position of the drawn token
-  const T* z = Z + ((size_t)r * (gamma + 1) + (row - 1)) * V;
+  const T* z = Z + zr.row(r, row) * V;
   const int groups = V >> 3;
   const int g0 = chunk * kDrawGroups, g1 = min(groups, g0 + kDrawGroups);
   const float L2E = 1.4426950408889634f;
@@ -502,7 +507,7 @@ verify_emit_kernel(const int32_t* __restrict__ x, const T* __restrict__ Z,
                    const float* __restrict__ lse_t_ws, const int* __restrict__ acc_ws,
                    const float2* __restrict__ partials, int n_chunks, int32_t* __restrict__ n_acc,
                    int32_t* __restrict__ tokens, int32_t* __restrict__ n_emit,
-                   float* __restrict__ cstar, float* __restrict__ lse_t_out) {
+                   float* __restrict__ cstar, float* __restrict__ lse_t_out, ZRows zr) {
   __shared__ float rk[kWarps];
   __shared__ int ri[kWarps];
   __shared__ int s_n;
@@ -525,7 +530,7 @@ verify_emit_kernel(const int32_t* __restrict__ x, const T* __restrict__ Z,
   block_argmax<kWarps>(best, idx, rk, ri);
   if (best == -INFINITY) {
     // Residual zero everywhere (p^t = p^d numerically): draw from p^t.
-    const T* z = Z + ((size_t)r * (gamma + 1) + (row - 1)) * V;
+    const T* z = Z + zr.row(r, row) * V;
     const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
     idx = 0x7fffffff;
     for (int g = threadIdx.x; g < (V >> 3); g += kVerifyThreads) {
@@ -578,8 +583,8 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
                                float* lse_t_ws, int* acc_ws, uint32_t* row_list, int* row_count,
-                               int* status, cudaStream_t s) {
-  verify_index_kernel<<<1, kIndexThreads, 0, s>>>(ell, R, gamma, row_list, row_count, status);
+                               int* status, ZRows zr, cudaStream_t s) {
+  verify_index_kernel<<<1, kIndexThreads, 0, s>>>(ell, R, gamma, row_list, row_count, status, zr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows_max = (long long)R * gamma;
@@ -588,11 +593,11 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
   if (dtype == DSPARK_BF16)
     verify_rows_stream_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, s>>>(
         x, logp, lse, scores, (const __nv_bfloat16*)Z, row_list, row_count, gamma, V, invT, seed,
-        cstar, lse_t_ws, acc_ws, status);
+        cstar, lse_t_ws, acc_ws, status, zr);
   else
     verify_rows_stream_kernel<float><<<grid, kRowThreads, 0, s>>>(
         x, logp, lse, scores, (const float*)Z, row_list, row_count, gamma, V, invT, seed, cstar,
-        lse_t_ws, acc_ws, status);
+        lse_t_ws, acc_ws, status, zr);
   return cudaGetLastError();
 }
 
@@ -603,23 +608,23 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
                                  int V, float invT, uint64_t seed, const float* lse_t_ws,
                                  const int* acc_ws, float2* partials, int32_t* n_acc,
                                  int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
-                                 cudaStream_t s) {
+                                 ZRows zr, cudaStream_t s) {
   const int chunks = verify_draw_chunks(V);
   dim3 grid(chunks, R);
   if (dtype == DSPARK_BF16) {
     verify_draw_kernel<__nv_bfloat16><<<grid, kDrawThreads, 0, s>>>(
         lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials,
-        chunks);
+        chunks, zr);
     verify_emit_kernel<__nv_bfloat16><<<R, kVerifyThreads, 0, s>>>(
         x, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials, chunks,
-        n_acc, tokens, n_emit, cstar, lse_t);
+        n_acc, tokens, n_emit, cstar, lse_t, zr);
   } else {
     verify_draw_kernel<float><<<grid, kDrawThreads, 0, s>>>(lse, scores, (const float*)Z, ell, gamma,
                                                             V, invT, seed, lse_t_ws, acc_ws,
-                                                            partials, chunks);
+                                                            partials, chunks, zr);
     verify_emit_kernel<float><<<R, kVerifyThreads, 0, s>>>(x, (const float*)Z, ell, gamma, V, invT,
                                                            seed, lse_t_ws, acc_ws, partials, chunks,
-                                                           n_acc, tokens, n_emit, cstar, lse_t);
+                                                           n_acc, tokens, n_emit, cstar, lse_t, zr);
   }
   return cudaGetLastError();
 }

@@ -94,3 +94,17 @@ def test_schedule_and_verify_reject_bad_arguments_on_the_host(lib):
     bad = list(base)
     bad[18] = 8
     assert lib.dspark_verify(*bad[:10], 1.0, *bad[11:]) == 3
+
+
+def test_zero_overhead_schedule_calls_reject_bad_arguments_on_the_host(lib):
+    # capacity(conf_old, sps, sps_len, R, gamma, K, diag, ws, wsb, stream)
+    assert lib.dspark_schedule_capacity(None, 16, 100, 4, 4, 16, None, 256, 256, None) == 1
+    assert lib.dspark_schedule_capacity(16, 16, 10, 4, 4, 16, None, 256, 256, None) == 1
+    assert lib.dspark_schedule_capacity(16, 16, 100, 4, 4, None, None, 256, 256, None) == 1
+    assert lib.dspark_schedule_capacity(16, 16, 10**6, 2048, 16, 16, None, 256, 256, None) == 2
+    assert lib.dspark_schedule_capacity(16, 16, 100, 4, 4, 16, None, None, 256, None) == 3
+    # topk(conf, K, R, gamma, ell, ws, wsb, stream)
+    assert lib.dspark_schedule_topk(16, None, 4, 4, 16, 256, 256, None) == 1
+    assert lib.dspark_schedule_topk(16, 16, 0, 4, 16, 256, 256, None) == 1
+    assert lib.dspark_schedule_topk(16, 16, 4, 65, 16, 256, 1 << 20, None) == 2
+    assert lib.dspark_schedule_topk(16, 16, 4, 4, 16, 256, 8, None) == 3
