@@ -11,6 +11,9 @@ Function-level citations are in the C file; the summary:
 * ``draft``     -- DSpark summary §3.1 and DSpark notes "DSpark 핵심 기술 1":
                    s_k = (U_k + W1[x_{k-1}] W2) / T, lse_k, Gumbel-max x_k, logp_k.
 * ``schedule``  -- DSpark summary §3.2.2 (Algorithm 1).
+* ``sts_calibrate`` / ``sts_ece`` / ``schedule_threshold`` -- DSpark summary
+                   §3.2.1 (sequential temperature scaling) and §4.3.3 (static
+                   threshold).
 * ``schedule_capacity`` / ``schedule_topk`` -- DSpark summary §5.2 (zero-overhead
                    scheduling: capacity from old confidences without the early
                    stop, then the top K of the current order).
@@ -77,6 +80,14 @@ def lib() -> ctypes.CDLL:
             L.oracle_schedule_capacity.restype = i32
             L.oracle_schedule_topk.argtypes = [i32, i32, P, i32, P]
             L.oracle_schedule_topk.restype = i32
+            L.oracle_temper.argtypes = [dbl, dbl]
+            L.oracle_temper.restype = dbl
+            L.oracle_sts_calibrate.argtypes = [i32, i32, P, P, P, i32, i32, P, P]
+            L.oracle_sts_calibrate.restype = i32
+            L.oracle_sts_ece.argtypes = [i32, i32, P, P, P, i32, P]
+            L.oracle_sts_ece.restype = i32
+            L.oracle_schedule_threshold.argtypes = [i32, i32, P, P, dbl, P]
+            L.oracle_schedule_threshold.restype = i32
             L.oracle_verify.argtypes = [i32, P, i32, i32, dbl, u64, P, P, P, P, P, P, P, P, P, P, P,
                                         P, P, P, i32]
             L.oracle_verify.restype = i32
@@ -198,6 +209,55 @@ def schedule_topk(conf_now, K: int):
     rc = lib().oracle_schedule_topk(R, g, _ptr(c), int(K), _ptr(ell))
     if rc != 0:
         raise ValueError(f"oracle_schedule_topk rejected its arguments (code {rc})")
+    return ell
+
+
+def sts_grid(n=121):
+    """A temperature grid: n log-spaced values from 0.1 to 10, T = 1 exactly in the middle."""
+    h = (n - 1) / 2
+    return 10.0 ** ((np.arange(n) - h) / h)
+
+
+def temper(c: float, T: float) -> float:
+    return float(lib().oracle_temper(float(c), float(T)))
+
+
+def sts_calibrate(conf, accept, grid=None, bins=15):
+    """Left-to-right grid search of per-position temperatures (minimum ECE each)."""
+    c = np.ascontiguousarray(conf, dtype=np.float32)
+    y = np.ascontiguousarray(accept, dtype=np.uint8)
+    N, g = c.shape
+    gr = _f64(sts_grid() if grid is None else grid).reshape(-1)
+    temps = np.zeros(g)
+    ece = np.zeros(g)
+    rc = lib().oracle_sts_calibrate(N, g, _ptr(c), _ptr(y), _ptr(gr), gr.size, int(bins), _ptr(temps),
+                                    _ptr(ece))
+    if rc != 0:
+        raise ValueError(f"oracle_sts_calibrate rejected its arguments (code {rc})")
+    return dict(temps=temps, ece=ece)
+
+
+def sts_ece(conf, accept, temps, bins=15):
+    c = np.ascontiguousarray(conf, dtype=np.float32)
+    y = np.ascontiguousarray(accept, dtype=np.uint8)
+    N, g = c.shape
+    t = _f64(temps).reshape(-1)
+    out = np.zeros(g)
+    rc = lib().oracle_sts_ece(N, g, _ptr(c), _ptr(y), _ptr(t), int(bins), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_sts_ece rejected its arguments (code {rc})")
+    return out
+
+
+def schedule_threshold(conf, theta: float, temps=None):
+    """Static threshold: l_r = leading positions with calibrated survival >= theta."""
+    c = np.ascontiguousarray(conf, dtype=np.float32)
+    R, g = c.shape
+    t = None if temps is None else _f64(temps).reshape(-1)
+    ell = np.zeros(R, dtype=np.int32)
+    rc = lib().oracle_schedule_threshold(R, g, _ptr(c), _ptr(t), float(theta), _ptr(ell))
+    if rc != 0:
+        raise ValueError(f"oracle_schedule_threshold rejected its arguments (code {rc})")
     return ell
 
 

@@ -555,3 +555,123 @@ int oracle_verify(int n_req, const int32_t* req_ids, int gamma, int V, double T,
   run_parallel(&J, n_req, nthreads, (size_t)V, verify_fn);
   return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Sequential Temperature Scaling, [P1] §3.2.1: on held-out data, the          */
+/* cumulative prefix survival is calibrated by a left-to-right 1-D grid search */
+/* that minimises each position's Expected Calibration Error with the earlier  */
+/* positions' calibration held fixed.                                          */
+/*   Sample s, position k: raw confidence c_{s,k}, outcome y_{s,k} in {0,1}    */
+/*   (position k accepted given the prefix accepted); the survival label is    */
+/*   Y_{s,k} = prod_{i<=k} y_{s,i}.                                            */
+/*   Temperature scaling: chat(c; T) = sigmoid(logit(c) / T) (0 and 1 stay,     */
+/*   T = 1 returns c itself).                                                  */
+/*   Calibrated survival: ahat_{s,k} = prod_{i<=k} chat(c_{s,i}; T_i).         */
+/*   ECE_k = (1/N) sum_b | sum_{s in bin b} (ahat_{s,k} - Y_{s,k}) |, with     */
+/*   M equal-width bins on [0, 1], b = min(floor(ahat M), M - 1).              */
+/*   T_k = the grid temperature with the smallest ECE_k (ties: the earlier     */
+/*   grid entry), given T_1 .. T_{k-1}.                                        */
+/* Static-threshold pruning, [P1] §4.3.3: l_r = the number of leading          */
+/* positions whose calibrated survival is at least theta (the survival does    */
+/* not increase along a request, so this is a prefix).                         */
+/* ------------------------------------------------------------------------- */
+double oracle_temper(double c, double T) {
+  if (!(c > 0.0)) return 0.0;
+  if (!(c < 1.0)) return 1.0;
+  if (T == 1.0) return c; /* sigmoid(logit(c)) = c */
+  const double z = (log(c) - log1p(-c)) / T;
+  return 1.0 / (1.0 + exp(-z));
+}
+
+int oracle_sts_calibrate(int N, int gamma, const float* c, const uint8_t* y, const double* grid,
+                         int G, int M, double* temps, double* ece_out /* [gamma] or NULL */) {
+  if (N < 1 || gamma < 1 || G < 1 || M < 1) return 1;
+  for (int g = 0; g < G; ++g)
+    if (!(grid[g] > 0.0) || !isfinite(grid[g])) return 1;
+  double* ahat = (double*)malloc(sizeof(double) * (size_t)N);
+  uint8_t* Y = (uint8_t*)malloc((size_t)N);
+  double* bins = (double*)malloc(sizeof(double) * (size_t)M);
+  for (int s = 0; s < N; ++s) {
+    ahat[s] = 1.0;
+    Y[s] = 1;
+  }
+  for (int k = 0; k < gamma; ++k) {
+    int best = 0;
+    double best_ece = INFINITY;
+    for (int g = 0; g < G; ++g) {
+      for (int b = 0; b < M; ++b) bins[b] = 0.0;
+      for (int s = 0; s < N; ++s) {
+        const double a = ahat[s] * oracle_temper((double)c[(size_t)s * gamma + k], grid[g]);
+        const int yk = Y[s] && y[(size_t)s * gamma + k];
+        int b = (int)floor(a * M);
+        if (b > M - 1) b = M - 1;
+        if (b < 0) b = 0;
+        bins[b] += a - (double)yk;
+      }
+      double e = 0.0;
+      for (int b = 0; b < M; ++b) e += fabs(bins[b]);
+      e /= (double)N;
+      if (e < best_ece) {
+        best_ece = e;
+        best = g;
+      }
+    }
+    temps[k] = grid[best];
+    if (ece_out) ece_out[k] = best_ece;
+    for (int s = 0; s < N; ++s) {
+      ahat[s] *= oracle_temper((double)c[(size_t)s * gamma + k], grid[best]);
+      Y[s] = Y[s] && y[(size_t)s * gamma + k];
+    }
+  }
+  free(ahat);
+  free(Y);
+  free(bins);
+  return 0;
+}
+
+/* ECE of given temperatures at every position (the objective above). */
+int oracle_sts_ece(int N, int gamma, const float* c, const uint8_t* y, const double* temps, int M,
+                   double* ece_out) {
+  if (N < 1 || gamma < 1 || M < 1) return 1;
+  double* bins = (double*)malloc(sizeof(double) * (size_t)M);
+  double* ahat = (double*)malloc(sizeof(double) * (size_t)N);
+  uint8_t* Y = (uint8_t*)malloc((size_t)N);
+  for (int s = 0; s < N; ++s) {
+    ahat[s] = 1.0;
+    Y[s] = 1;
+  }
+  for (int k = 0; k < gamma; ++k) {
+    for (int b = 0; b < M; ++b) bins[b] = 0.0;
+    for (int s = 0; s < N; ++s) {
+      ahat[s] *= oracle_temper((double)c[(size_t)s * gamma + k], temps[k]);
+      Y[s] = Y[s] && y[(size_t)s * gamma + k];
+      int b = (int)floor(ahat[s] * M);
+      if (b > M - 1) b = M - 1;
+      if (b < 0) b = 0;
+      bins[b] += ahat[s] - (double)Y[s];
+    }
+    double e = 0.0;
+    for (int b = 0; b < M; ++b) e += fabs(bins[b]);
+    ece_out[k] = e / (double)N;
+  }
+  free(bins);
+  free(ahat);
+  free(Y);
+  return 0;
+}
+
+int oracle_schedule_threshold(int R, int gamma, const float* c, const double* temps /* or NULL */,
+                              double theta, int32_t* ell) {
+  if (R < 1 || gamma < 1) return 1;
+  for (int r = 0; r < R; ++r) {
+    double a = 1.0;
+    int l = 0;
+    for (int j = 0; j < gamma; ++j) {
+      a *= oracle_temper((double)c[(size_t)r * gamma + j], temps ? temps[j] : 1.0); /* T = 1: c */
+      if (!(a >= theta)) break;
+      l = j + 1;
+    }
+    ell[r] = l;
+  }
+  return 0;
+}

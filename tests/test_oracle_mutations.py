@@ -46,6 +46,16 @@ MUTATIONS = [
      "if (exact_greater(tau, sps[R + i], best_tau, sps[R + best])) { /* strictly: first maximum */"),
     ("top-k takes one candidate too many", "for (int i = 0; i < n && i < K; ++i) ell[cs[i].r] += 1;",
      "for (int i = 0; i < n && i <= K; ++i) ell[cs[i].r] += 1;"),
+    ("temperature multiplies the logit", "const double z = (log(c) - log1p(-c)) / T;",
+     "const double z = (log(c) - log1p(-c)) * T;"),
+    ("ECE without the absolute value",
+     "      double e = 0.0;\n      for (int b = 0; b < M; ++b) e += fabs(bins[b]);\n      e /= (double)N;",
+     "      double e = 0.0;\n      for (int b = 0; b < M; ++b) e += bins[b];\n      e /= (double)N;"),
+    ("ECE bins one short", "        int b = (int)floor(a * M);", "        int b = (int)floor(a * (M - 1));"),
+    ("earlier positions' calibration not kept",
+     "      ahat[s] *= oracle_temper((double)c[(size_t)s * gamma + k], grid[best]);",
+     "      ahat[s] *= 1.0;"),
+    ("threshold test strict", "if (!(a >= theta)) break;", "if (!(a > theta)) break;"),
     ("draft stream keyed by the wrong position",
      "(J->seed, req, (uint32_t)k,\n                                                    ORACLE_PURPOSE_DRAFT",
      "(J->seed, req, (uint32_t)(k + 1),\n                                                    ORACLE_PURPOSE_DRAFT"),
