@@ -174,6 +174,40 @@ int dspark_schedule_topk(const float* conf, const int32_t* K, int R, int gamma, 
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Sequential Temperature Scaling ([summary] §3.2.1) and the static-threshold
+ * scheduler ([summary] §4.3.3).
+ *
+ * temper(c; T) = sigmoid(logit(c) / T) (0 and 1 stay, T = 1 returns c), in
+ * fp32; calibrated survival ahat_{s,k} = prod_{i<=k} temper(c_{s,i}; T_i)
+ * (fp64 product).
+ *
+ * dspark_sts_calibrate -- on held-out samples s = 0..N-1 with raw confidences
+ *   conf [N, gamma] float and outcomes accept [N, gamma] uint8 (1 = position k
+ *   accepted given its prefix accepted; the survival label is
+ *   Y_{s,k} = prod_{i<=k} accept_{s,i}), a left-to-right 1-D grid search:
+ *   for k = 1..gamma, with T_1..T_{k-1} fixed, T_k = the first entry of grid
+ *   [G] (device, fp64, positive) with the smallest
+ *     ECE_k = (1/N) sum_b | sum_{s in bin b} (ahat_{s,k} - Y_{s,k}) |,
+ *   M equal-width bins on [0, 1], b = min(floor(ahat M), M - 1).  The bin
+ *   sums are exact in 2^-40 fixed point, so each ECE is independent of the
+ *   summation order.
+ *   temps [gamma] double (device) out; ece [gamma] double (device) or NULL out.
+ *   workspace: >= dspark_sts_workspace_bytes(N, G, M) bytes, 256-byte aligned.
+ *   Limits: N <= 2^22, M <= 1024, gamma <= 64 (else DSPARK_ERR_UNSUPPORTED).
+ * dspark_schedule_threshold -- l_r = the number of leading positions of
+ *   request r whose survival prod_{i<=j} temper(c_{r,i}; T_i) is at least
+ *   theta (temps [gamma] device, or NULL for the raw product of c).  The
+ *   survival does not increase along a request, so the result is a prefix.
+ *   conf [R, gamma] float; ell [R] int32 out.
+ * ---------------------------------------------------------------------- */
+size_t dspark_sts_workspace_bytes(int N, int G, int M);
+int dspark_sts_calibrate(const float* conf, const uint8_t* accept, int N, int gamma,
+                         const double* grid, int G, int M, double* temps, double* ece,
+                         void* workspace, size_t workspace_bytes, void* stream);
+int dspark_schedule_threshold(const float* conf, const double* temps, double theta, int R,
+                              int gamma, int32_t* ell, void* stream);
+
+/* ------------------------------------------------------------------------
  * dspark_verify -- standard rejection sampling over the scheduled prefixes
  * ([summary] opening bullets, §3; [notes] "배경") and the soft label
  * ([summary] §3.2.1).  With p^t_j = softmax(Z_j / T) and

@@ -14,10 +14,13 @@ from .binding import (  # noqa: F401
     dspark_schedule,
     dspark_schedule_capacity,
     dspark_schedule_topk,
+    dspark_schedule_threshold,
+    dspark_sts_calibrate,
     dspark_verify,
     dspark_verify_packed,
     draft_workspace_bytes,
     schedule_workspace_bytes,
+    sts_workspace_bytes,
     verify_workspace_bytes,
 )
 
@@ -26,6 +29,9 @@ __all__ = [
     "dspark_schedule",
     "dspark_schedule_capacity",
     "dspark_schedule_topk",
+    "dspark_schedule_threshold",
+    "dspark_sts_calibrate",
+    "sts_workspace_bytes",
     "dspark_verify",
     "dspark_verify_packed",
     "dspark_read_device_status",

@@ -55,6 +55,12 @@ def load() -> ctypes.CDLL:
     L.dspark_draft_sample.restype = I
     L.dspark_schedule_workspace_bytes.argtypes = [I, I]
     L.dspark_schedule_workspace_bytes.restype = SZ
+    L.dspark_sts_workspace_bytes.argtypes = [I, I, I]
+    L.dspark_sts_workspace_bytes.restype = SZ
+    L.dspark_sts_calibrate.argtypes = [P, P, I, I, P, I, I, P, P, P, SZ, P]
+    L.dspark_sts_calibrate.restype = I
+    L.dspark_schedule_threshold.argtypes = [P, P, D, I, I, P, P]
+    L.dspark_schedule_threshold.restype = I
     L.dspark_schedule.argtypes = [P, P, I, I, I, P, P, P, SZ, P]
     L.dspark_schedule.restype = I
     L.dspark_schedule_capacity.argtypes = [P, P, I, I, I, P, P, P, SZ, P]
@@ -123,6 +129,44 @@ def draft_workspace_bytes(R: int, gamma: int, V: int, r: int, dtype: torch.dtype
 
 def schedule_workspace_bytes(R: int, gamma: int) -> int:
     return int(load().dspark_schedule_workspace_bytes(R, gamma))
+
+
+def sts_workspace_bytes(N: int, G: int, M: int) -> int:
+    return int(load().dspark_sts_workspace_bytes(N, G, M))
+
+
+def dspark_sts_calibrate(conf, accept, grid, bins: int = 15, *, temps=None, ece=None,
+                         workspace=None, stream=None) -> dict:
+    """Sequential temperature scaling: conf [N, gamma] float32, accept [N, gamma] uint8,
+    grid [G] float64 (all on the device).  Returns temps, ece [gamma] float64."""
+    L = load()
+    N, g = conf.shape
+    G = grid.numel()
+    dev = conf.device
+    temps = torch.empty(g, dtype=torch.float64, device=dev) if temps is None else temps
+    ece = torch.empty(g, dtype=torch.float64, device=dev) if ece is None else ece
+    ws = _workspace(sts_workspace_bytes(N, G, bins), dev, workspace)
+    st = L.dspark_sts_calibrate(_dev(conf, "conf", torch.float32), _dev(accept, "accept", torch.uint8, (N, g)),
+                                N, g, _dev(grid, "grid", torch.float64, (G,)), G, int(bins),
+                                _dev(temps, "temps", torch.float64, (g,)),
+                                _dev(ece, "ece", torch.float64, (g,)), ws.data_ptr(), ws.numel(),
+                                _stream(stream))
+    _check("dspark_sts_calibrate", st)
+    return dict(temps=temps, ece=ece, workspace=ws)
+
+
+def dspark_schedule_threshold(conf, theta: float, temps=None, *, ell=None, stream=None) -> dict:
+    """Static threshold: l_r = leading positions whose (calibrated) survival >= theta."""
+    L = load()
+    R, g = conf.shape
+    dev = conf.device
+    ell = torch.empty(R, dtype=torch.int32, device=dev) if ell is None else ell
+    st = L.dspark_schedule_threshold(_dev(conf, "conf", torch.float32),
+                                     None if temps is None else _dev(temps, "temps", torch.float64, (g,)),
+                                     float(theta), R, g, _dev(ell, "ell", torch.int32, (R,)),
+                                     _stream(stream))
+    _check("dspark_schedule_threshold", st)
+    return dict(ell=ell)
 
 
 def verify_workspace_bytes(R: int, gamma: int, V: int) -> int:

@@ -289,6 +289,38 @@ int dspark_schedule_topk(const float* conf, const int32_t* K, int R, int gamma, 
   return DSPARK_OK;
 }
 
+size_t dspark_sts_workspace_bytes(int N, int G, int M) {
+  if (N <= 0 || G <= 0 || M <= 0) return 0;
+  return sts_workspace_layout(N, G, M).total;
+}
+
+int dspark_sts_calibrate(const float* conf, const uint8_t* accept, int N, int gamma,
+                         const double* grid, int G, int M, double* temps, double* ece,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!conf || !accept || !grid || !temps) return DSPARK_ERR_INVALID_ARG;
+  if (N <= 0 || gamma <= 0 || G <= 0 || M <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (N > (1 << 22) || M > 1024 || gamma > 64) return DSPARK_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < dspark_sts_workspace_bytes(N, G, M) ||
+      ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_sts_calibrate(conf, accept, N, gamma, grid, G, M, temps, ece, workspace, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sts_calibrate");
+  return DSPARK_OK;
+}
+
+int dspark_schedule_threshold(const float* conf, const double* temps, double theta, int R,
+                              int gamma, int32_t* ell, void* stream) {
+  if (!conf || !ell) return DSPARK_ERR_INVALID_ARG;
+  if (R <= 0 || gamma <= 0 || !(theta == theta)) return DSPARK_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  prof_begin(kKindSchedule, s);
+  cudaError_t e = launch_schedule_threshold(conf, temps, theta, R, gamma, ell, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule_threshold");
+  return DSPARK_OK;
+}
+
 size_t dspark_verify_workspace_bytes(int R, int gamma, int V) {
   if (R <= 0 || gamma <= 0 || V <= 0) return 0;
   return verify_scratch_layout(R, gamma, V).total;

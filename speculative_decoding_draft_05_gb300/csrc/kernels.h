@@ -109,6 +109,19 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
                                  int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
                                  ZRows zr, cudaStream_t s);
 
+// Sequential temperature scaling: workspace (byte offsets, 256-aligned) of the
+// chosen grid index, the [G, M] fixed-point bins, the running survival [N]
+// (fp64) and the running outcome [N] (u8).
+struct StsWorkspace {
+  size_t choice, bins, ahat, Y, total;
+};
+StsWorkspace sts_workspace_layout(int N, int G, int M);
+cudaError_t launch_sts_calibrate(const float* conf, const uint8_t* accept, int N, int gamma,
+                                 const double* grid, int G, int M, double* temps, double* ece,
+                                 void* workspace, cudaStream_t s);
+cudaError_t launch_schedule_threshold(const float* conf, const double* temps, double theta, int R,
+                                      int gamma, int32_t* ell, cudaStream_t s);
+
 // Kernel kinds for the optional event timing (dspark_profile_*).
 enum KernelKind {
   kKindPrepare = 0,  // W2 transpose (bf16) or anchor gather (fp32)
