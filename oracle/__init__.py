@@ -10,6 +10,9 @@ Function-level citations are in the C file; the summary:
 
 * ``draft``     -- DSpark summary §3.1 and DSpark notes "DSpark 핵심 기술 1":
                    s_k = (U_k + W1[x_{k-1}] W2) / T, lse_k, Gumbel-max x_k, logp_k.
+* ``draft_rnn`` -- DSpark summary §3.1 (the RNN head: a state across the block
+                   and the backbone hidden state; an Elman recurrence in the
+                   Markov head's rank-r space).
 * ``schedule``  -- DSpark summary §3.2.2 (Algorithm 1).
 * ``sts_calibrate`` / ``sts_ece`` / ``schedule_threshold`` -- DSpark summary
                    §3.2.1 (sequential temperature scaling) and §4.3.3 (static
@@ -74,6 +77,11 @@ def lib() -> ctypes.CDLL:
             L.oracle_markov_bias_rows.restype = None
             L.oracle_draft.argtypes = [i32, P, i32, i32, i32, dbl, u64, P, P, P, P, P, P, P, P, P, i32]
             L.oracle_draft.restype = i32
+            L.oracle_draft_rnn.argtypes = [i32, P, i32, i32, i32, dbl, u64, P, P, P, P, P, P, P, P, P,
+                                           P, P, i32]
+            L.oracle_draft_rnn.restype = i32
+            L.oracle_round_bf16.argtypes = [dbl]
+            L.oracle_round_bf16.restype = dbl
             L.oracle_schedule.argtypes = [i32, i32, P, P, i32, P, P, P]
             L.oracle_schedule.restype = i32
             L.oracle_schedule_capacity.argtypes = [i32, i32, P, P, i32, P, P]
@@ -169,6 +177,37 @@ def draft(U, W1, W2, x0, T: float, seed: int, req_ids=None, want_scores=True, nt
                             nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_draft rejected its arguments (code {rc})")
+    return dict(x=x, logp=logp, lse=lse, scores=scores, margin=margin)
+
+
+def round_bf16(v: float) -> float:
+    return float(lib().oracle_round_bf16(float(v)))
+
+
+def draft_rnn(U, W1, W2, Wh, Q, x0, T: float, seed: int, req_ids=None, want_scores=True, nthreads=None):
+    """Draft with the RNN head: h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k), B_k = bf16(h_k) W2.
+
+    U [n, gamma, V]; W1 [V, r]; W2 [r, V]; Wh [r, r]; Q [n, gamma, r]; x0 [n]."""
+    U = _f64(U)
+    W1 = _f64(W1)
+    W2 = _f64(W2)
+    Wh = _f64(Wh)
+    Q = _f64(Q)
+    x0 = _i32(x0).reshape(-1)
+    n, g, V = U.shape
+    r = W1.shape[1]
+    assert Wh.shape == (r, r) and Q.shape == (n, g, r)
+    req = _i32(np.arange(n) if req_ids is None else req_ids).reshape(-1)
+    x = np.zeros((n, g), dtype=np.int32)
+    logp = np.zeros((n, g))
+    lse = np.zeros((n, g))
+    margin = np.zeros((n, g))
+    scores = np.zeros((n, g, V)) if want_scores else None
+    rc = lib().oracle_draft_rnn(n, _ptr(req), g, V, r, float(T), int(seed), _ptr(U), _ptr(W1), _ptr(W2),
+                                _ptr(Wh), _ptr(Q), _ptr(x0), _ptr(x), _ptr(logp), _ptr(lse),
+                                _ptr(scores), _ptr(margin), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_draft_rnn rejected its arguments (code {rc})")
     return dict(x=x, logp=logp, lse=lse, scores=scores, margin=margin)
 
 

@@ -188,6 +188,74 @@ static void draft_one(const draft_job* J, int i, double* s, double* key) {
   }
 }
 
+/* ------------------------------------------------------------------------- */
+/* RNN head, [P1] §3.1: the alternative sequential head keeps a state across */
+/* the block and also takes the backbone's hidden state.  Reading: an Elman  */
+/* recurrence in the Markov head's rank-r space,                              */
+/*   h_0 = 0,  h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k),  B_k = h_k W2,     */
+/* with Q_k [r] the backbone hidden state of position k projected into the   */
+/* head (an input) and Wh [r, r].  The state is exact (fp64 here); the       */
+/* contraction takes it rounded to bf16 (nearest, ties to even), like every  */
+/* operand of the bf16 contraction.  Everything else is the Markov draft.    */
+/* ------------------------------------------------------------------------- */
+double oracle_round_bf16(double v) {
+  if (!isfinite(v) || v == 0.0) return v;
+  int e;
+  const double f = frexp(v, &e);            /* v = f 2^e, |f| in [0.5, 1) */
+  const double q = nearbyint(ldexp(f, 8));  /* 8 significant bits: |q| in [128, 256] */
+  return ldexp(q, e - 8);
+}
+
+static void draft_rnn_one(const draft_job* J, const double* Wh, const double* Q, int i, double* s,
+                          double* key) {
+  const int g = J->gamma, V = J->V, r = J->r;
+  const uint32_t req = (uint32_t)J->req_ids[i];
+  int32_t prev = J->x0[i];
+  double* h = (double*)calloc((size_t)r, sizeof(double));
+  double* hn = (double*)malloc(sizeof(double) * (size_t)r);
+  double* A = (double*)malloc(sizeof(double) * (size_t)r);
+  for (int k = 1; k <= g; ++k) {
+    const double* Qk = Q + ((size_t)i * g + (k - 1)) * r;
+    for (int j = 0; j < r; ++j) {
+      double z = J->W1[(size_t)prev * r + j] + Qk[j];
+      for (int a = 0; a < r; ++a) z += h[a] * Wh[(size_t)a * r + j];
+      hn[j] = tanh(z);
+    }
+    for (int j = 0; j < r; ++j) {
+      h[j] = hn[j];
+      A[j] = oracle_round_bf16(hn[j]);
+    }
+    for (int v = 0; v < V; ++v) s[v] = 0.0;
+    for (int a = 0; a < r; ++a) {
+      const double* w2row = J->W2 + (size_t)a * V;
+      for (int v = 0; v < V; ++v) s[v] += A[a] * w2row[v];
+    }
+    const double* Uk = J->U + ((size_t)i * g + (k - 1)) * V;
+    for (int v = 0; v < V; ++v) s[v] = (Uk[v] + s[v]) / J->T;
+    const double lse = logsumexp(s, V);
+    for (int v = 0; v < V; ++v)
+      key[v] = s[v] + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)k,
+                                                    ORACLE_PURPOSE_DRAFT, (uint32_t)v));
+    double margin = 0.0;
+    const int xk = argmax_fp32(key, V, &margin);
+    const size_t o = (size_t)i * g + (k - 1);
+    J->x[o] = xk;
+    J->logp[o] = s[xk] - lse;
+    J->lse[o] = lse;
+    if (J->margin) J->margin[o] = margin;
+    if (J->scores) memcpy(J->scores + o * V, s, sizeof(double) * (size_t)V);
+    prev = xk;
+  }
+  free(h);
+  free(hn);
+  free(A);
+}
+
+typedef struct {
+  draft_job base;
+  const double *Wh, *Q;
+} draft_rnn_job;
+
 typedef struct {
   const void* job;
   int n, nthreads, tid;
@@ -227,6 +295,25 @@ static void run_parallel(const void* job, int n, int nthreads, size_t scratch,
 
 static void draft_fn(const void* job, int i, double* a, double* b) {
   draft_one((const draft_job*)job, i, a, b);
+}
+
+static void draft_rnn_fn(const void* job, int i, double* a, double* b) {
+  const draft_rnn_job* J = (const draft_rnn_job*)job;
+  draft_rnn_one(&J->base, J->Wh, J->Q, i, a, b);
+}
+
+int oracle_draft_rnn(int n_req, const int32_t* req_ids, int gamma, int V, int r, double T,
+                     uint64_t seed, const double* U, const double* W1, const double* W2,
+                     const double* Wh, const double* Q, const int32_t* x0, int32_t* x, double* logp,
+                     double* lse, double* scores, double* margin, int nthreads) {
+  if (n_req < 0 || gamma < 1 || V < 1 || r < 1 || !(T > 0.0)) return 1;
+  for (int i = 0; i < n_req; ++i)
+    if (x0[i] < 0 || x0[i] >= V) return 2;
+  draft_rnn_job J = {{n_req, gamma, V, r, T, seed, req_ids, U, W1, W2, x0, x, logp, lse, scores,
+                      margin},
+                     Wh, Q};
+  run_parallel(&J, n_req, nthreads, (size_t)V, draft_rnn_fn);
+  return 0;
 }
 
 int oracle_draft(int n_req, const int32_t* req_ids, int gamma, int V, int r, double T,

@@ -56,6 +56,11 @@ MUTATIONS = [
      "      ahat[s] *= oracle_temper((double)c[(size_t)s * gamma + k], grid[best]);",
      "      ahat[s] *= 1.0;"),
     ("threshold test strict", "if (!(a >= theta)) break;", "if (!(a > theta)) break;"),
+    ("RNN head without the tanh", "      hn[j] = tanh(z);", "      hn[j] = z;"),
+    ("RNN state not carried", "      h[j] = hn[j];", "      h[j] = 0.0;"),
+    ("RNN recurrent matrix transposed", "for (int a = 0; a < r; ++a) z += h[a] * Wh[(size_t)a * r + j];",
+     "for (int a = 0; a < r; ++a) z += h[a] * Wh[(size_t)j * r + a];"),
+    ("RNN operand not rounded to bf16", "      A[j] = oracle_round_bf16(hn[j]);", "      A[j] = hn[j];"),
     ("draft stream keyed by the wrong position",
      "(J->seed, req, (uint32_t)k,\n                                                    ORACLE_PURPOSE_DRAFT",
      "(J->seed, req, (uint32_t)(k + 1),\n                                                    ORACLE_PURPOSE_DRAFT"),
