@@ -78,7 +78,7 @@ def lib() -> ctypes.CDLL:
             L.oracle_draft.argtypes = [i32, P, i32, i32, i32, dbl, u64, P, P, P, P, P, P, P, P, P, i32]
             L.oracle_draft.restype = i32
             L.oracle_draft_rnn.argtypes = [i32, P, i32, i32, i32, dbl, u64, P, P, P, P, P, P, P, P, P,
-                                           P, P, i32]
+                                           P, P, P, i32]
             L.oracle_draft_rnn.restype = i32
             L.oracle_round_bf16.argtypes = [dbl]
             L.oracle_round_bf16.restype = dbl
@@ -184,10 +184,12 @@ def round_bf16(v: float) -> float:
     return float(lib().oracle_round_bf16(float(v)))
 
 
-def draft_rnn(U, W1, W2, Wh, Q, x0, T: float, seed: int, req_ids=None, want_scores=True, nthreads=None):
+def draft_rnn(U, W1, W2, Wh, Q, x0, T: float, seed: int, req_ids=None, want_scores=True, want_state=False,
+              nthreads=None):
     """Draft with the RNN head: h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k), B_k = bf16(h_k) W2.
 
-    U [n, gamma, V]; W1 [V, r]; W2 [r, V]; Wh [r, r]; Q [n, gamma, r]; x0 [n]."""
+    U [n, gamma, V]; W1 [V, r]; W2 [r, V]; Wh [r, r]; Q [n, gamma, r]; x0 [n].
+    want_state adds "h" [n, gamma, r], the fp64 state h_k of every step."""
     U = _f64(U)
     W1 = _f64(W1)
     W2 = _f64(W2)
@@ -203,12 +205,16 @@ def draft_rnn(U, W1, W2, Wh, Q, x0, T: float, seed: int, req_ids=None, want_scor
     lse = np.zeros((n, g))
     margin = np.zeros((n, g))
     scores = np.zeros((n, g, V)) if want_scores else None
+    h = np.zeros((n, g, r)) if want_state else None
     rc = lib().oracle_draft_rnn(n, _ptr(req), g, V, r, float(T), int(seed), _ptr(U), _ptr(W1), _ptr(W2),
                                 _ptr(Wh), _ptr(Q), _ptr(x0), _ptr(x), _ptr(logp), _ptr(lse),
-                                _ptr(scores), _ptr(margin), nthreads or default_threads())
+                                _ptr(scores), _ptr(margin), _ptr(h), nthreads or default_threads())
     if rc != 0:
         raise ValueError(f"oracle_draft_rnn rejected its arguments (code {rc})")
-    return dict(x=x, logp=logp, lse=lse, scores=scores, margin=margin)
+    out = dict(x=x, logp=logp, lse=lse, scores=scores, margin=margin)
+    if want_state:
+        out["h"] = h
+    return out
 
 
 # --------------------------------------------------------------------------- schedule

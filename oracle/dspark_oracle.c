@@ -164,27 +164,34 @@ typedef struct {
   double *logp, *lse, *scores, *margin;
 } draft_job;
 
-static void draft_one(const draft_job* J, int i, double* s, double* key) {
+/* One draft position k of request i, shared by both heads: s holds the bias */
+/* B_k on entry and the scores s_k = (U_k + B_k) / T on return; the token is  */
+/* the Gumbel argmax of s_k, its log-probability s_k[x] - lse(s_k).           */
+static int32_t draft_sample(const draft_job* J, int i, int k, double* s, double* key) {
   const int g = J->gamma, V = J->V;
   const uint32_t req = (uint32_t)J->req_ids[i];
+  const double* Uk = J->U + ((size_t)i * g + (k - 1)) * V;
+  for (int v = 0; v < V; ++v) s[v] = (Uk[v] + s[v]) / J->T;
+  const double lse = logsumexp(s, V);
+  for (int v = 0; v < V; ++v)
+    key[v] = s[v] + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)k,
+                                                  ORACLE_PURPOSE_DRAFT, (uint32_t)v));
+  double margin = 0.0;
+  const int xk = argmax_fp32(key, V, &margin);
+  const size_t o = (size_t)i * g + (k - 1);
+  J->x[o] = xk;
+  J->logp[o] = s[xk] - lse;
+  J->lse[o] = lse;
+  if (J->margin) J->margin[o] = margin;
+  if (J->scores) memcpy(J->scores + o * V, s, sizeof(double) * (size_t)V);
+  return xk;
+}
+
+static void draft_one(const draft_job* J, int i, double* s, double* key) {
   int32_t prev = J->x0[i];
-  for (int k = 1; k <= g; ++k) {
-    const double* Uk = J->U + ((size_t)i * g + (k - 1)) * V;
-    oracle_markov_bias(J->W1, J->W2, V, J->r, prev, s);
-    for (int v = 0; v < V; ++v) s[v] = (Uk[v] + s[v]) / J->T;
-    const double lse = logsumexp(s, V);
-    for (int v = 0; v < V; ++v)
-      key[v] = s[v] + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)k,
-                                                    ORACLE_PURPOSE_DRAFT, (uint32_t)v));
-    double margin = 0.0;
-    const int xk = argmax_fp32(key, V, &margin);
-    const size_t o = (size_t)i * g + (k - 1);
-    J->x[o] = xk;
-    J->logp[o] = s[xk] - lse;
-    J->lse[o] = lse;
-    if (J->margin) J->margin[o] = margin;
-    if (J->scores) memcpy(J->scores + o * V, s, sizeof(double) * (size_t)V);
-    prev = xk;
+  for (int k = 1; k <= J->gamma; ++k) {
+    oracle_markov_bias(J->W1, J->W2, J->V, J->r, prev, s);
+    prev = draft_sample(J, i, k, s, key);
   }
 }
 
@@ -206,10 +213,9 @@ double oracle_round_bf16(double v) {
   return ldexp(q, e - 8);
 }
 
-static void draft_rnn_one(const draft_job* J, const double* Wh, const double* Q, int i, double* s,
-                          double* key) {
+static void draft_rnn_one(const draft_job* J, const double* Wh, const double* Q, double* hstate,
+                          int i, double* s, double* key) {
   const int g = J->gamma, V = J->V, r = J->r;
-  const uint32_t req = (uint32_t)J->req_ids[i];
   int32_t prev = J->x0[i];
   double* h = (double*)calloc((size_t)r, sizeof(double));
   double* hn = (double*)malloc(sizeof(double) * (size_t)r);
@@ -225,26 +231,13 @@ static void draft_rnn_one(const draft_job* J, const double* Wh, const double* Q,
       h[j] = hn[j];
       A[j] = oracle_round_bf16(hn[j]);
     }
+    if (hstate) memcpy(hstate + ((size_t)i * g + (k - 1)) * r, h, sizeof(double) * (size_t)r);
     for (int v = 0; v < V; ++v) s[v] = 0.0;
     for (int a = 0; a < r; ++a) {
       const double* w2row = J->W2 + (size_t)a * V;
       for (int v = 0; v < V; ++v) s[v] += A[a] * w2row[v];
     }
-    const double* Uk = J->U + ((size_t)i * g + (k - 1)) * V;
-    for (int v = 0; v < V; ++v) s[v] = (Uk[v] + s[v]) / J->T;
-    const double lse = logsumexp(s, V);
-    for (int v = 0; v < V; ++v)
-      key[v] = s[v] + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)k,
-                                                    ORACLE_PURPOSE_DRAFT, (uint32_t)v));
-    double margin = 0.0;
-    const int xk = argmax_fp32(key, V, &margin);
-    const size_t o = (size_t)i * g + (k - 1);
-    J->x[o] = xk;
-    J->logp[o] = s[xk] - lse;
-    J->lse[o] = lse;
-    if (J->margin) J->margin[o] = margin;
-    if (J->scores) memcpy(J->scores + o * V, s, sizeof(double) * (size_t)V);
-    prev = xk;
+    prev = draft_sample(J, i, k, s, key);
   }
   free(h);
   free(hn);
@@ -254,6 +247,7 @@ static void draft_rnn_one(const draft_job* J, const double* Wh, const double* Q,
 typedef struct {
   draft_job base;
   const double *Wh, *Q;
+  double* hstate;  // optional [n_req, gamma, r]: the state h_k of every step
 } draft_rnn_job;
 
 typedef struct {
@@ -299,19 +293,19 @@ static void draft_fn(const void* job, int i, double* a, double* b) {
 
 static void draft_rnn_fn(const void* job, int i, double* a, double* b) {
   const draft_rnn_job* J = (const draft_rnn_job*)job;
-  draft_rnn_one(&J->base, J->Wh, J->Q, i, a, b);
+  draft_rnn_one(&J->base, J->Wh, J->Q, J->hstate, i, a, b);
 }
 
 int oracle_draft_rnn(int n_req, const int32_t* req_ids, int gamma, int V, int r, double T,
                      uint64_t seed, const double* U, const double* W1, const double* W2,
                      const double* Wh, const double* Q, const int32_t* x0, int32_t* x, double* logp,
-                     double* lse, double* scores, double* margin, int nthreads) {
+                     double* lse, double* scores, double* margin, double* hstate, int nthreads) {
   if (n_req < 0 || gamma < 1 || V < 1 || r < 1 || !(T > 0.0)) return 1;
   for (int i = 0; i < n_req; ++i)
     if (x0[i] < 0 || x0[i] >= V) return 2;
   draft_rnn_job J = {{n_req, gamma, V, r, T, seed, req_ids, U, W1, W2, x0, x, logp, lse, scores,
                       margin},
-                     Wh, Q};
+                     Wh, Q, hstate};
   run_parallel(&J, n_req, nthreads, (size_t)V, draft_rnn_fn);
   return 0;
 }

@@ -20,8 +20,9 @@ MUTATIONS = [
      "for (int round = 0; round < 9; ++round)"),
     ("uniform off by one step", "return ((double)(w >> 9) * 2.0 + 1.0) * 0x1p-24;",
      "return ((double)(w >> 9) * 2.0 + 2.0) * 0x1p-24;"),
-    ("anchor ignored", "int32_t prev = J->x0[i];", "int32_t prev = 0;"),
-    ("previous token not advanced", "    prev = xk;", "    prev = prev;"),
+    ("anchor ignored", "  int32_t prev = J->x0[i];\n  for (int k = 1;", "  int32_t prev = 0;\n  for (int k = 1;"),
+    ("previous token not advanced", "oracle_markov_bias(J->W1, J->W2, J->V, J->r, prev, s);\n    prev = draft_sample(",
+     "oracle_markov_bias(J->W1, J->W2, J->V, J->r, prev, s);\n    (void)draft_sample("),
     ("temperature dropped", "s[v] = (Uk[v] + s[v]) / J->T;", "s[v] = (Uk[v] + s[v]);"),
     ("bias sign", "out[v] += a * w2row[v];", "out[v] -= a * w2row[v];"),
     ("accept comparison reversed", "if (!((float)lhs < (float)rhs)) break;",
@@ -62,8 +63,11 @@ MUTATIONS = [
      "for (int a = 0; a < r; ++a) z += h[a] * Wh[(size_t)j * r + a];"),
     ("RNN operand not rounded to bf16", "      A[j] = oracle_round_bf16(hn[j]);", "      A[j] = hn[j];"),
     ("draft stream keyed by the wrong position",
-     "(J->seed, req, (uint32_t)k,\n                                                    ORACLE_PURPOSE_DRAFT",
-     "(J->seed, req, (uint32_t)(k + 1),\n                                                    ORACLE_PURPOSE_DRAFT"),
+     "(J->seed, req, (uint32_t)k,\n                                                  ORACLE_PURPOSE_DRAFT",
+     "(J->seed, req, (uint32_t)(k + 1),\n                                                  ORACLE_PURPOSE_DRAFT"),
+    ("RNN anchor ignored", "  int32_t prev = J->x0[i];\n  double* h", "  int32_t prev = 0;\n  double* h"),
+    ("RNN previous token not advanced", "    }\n    prev = draft_sample(J, i, k, s, key);",
+     "    }\n    (void)draft_sample(J, i, k, s, key);"),
 ]
 
 

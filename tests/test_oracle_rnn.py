@@ -68,3 +68,22 @@ def test_state_is_carried_through_wh():
     out = oracle.draft_rnn(rng.normal(0, 1, size=(1, 2, V)), np.zeros((V, r)), W2, np.zeros((r, r)), Q,
                            [x0], 1.0, 99)
     assert out["x"][0, 1] == 6
+
+
+def test_state_output_is_the_recurrence():
+    # want_state returns h_k; with W2 = 0 the tokens are the plain Gumbel argmax of
+    # U, so the states can be checked step by step against tanh of the recurrence
+    rng = np.random.default_rng(3)
+    n, g, V, r = 3, 4, 50, 6
+    U = rng.normal(0, 1, size=(n, g, V))
+    W1 = rng.normal(0, 0.7, size=(V, r))
+    Wh = rng.normal(0, 0.4, size=(r, r))
+    Q = rng.normal(0, 0.5, size=(n, g, r))
+    x0 = rng.integers(0, V, size=n)
+    out = oracle.draft_rnn(U, W1, np.zeros((r, V)), Wh, Q, x0, 1.0, 11, want_state=True)
+    for i in range(n):
+        h, prev = np.zeros(r), x0[i]
+        for k in range(g):
+            h = np.tanh(W1[prev] + h @ Wh + Q[i, k])
+            np.testing.assert_allclose(out["h"][i, k], h, rtol=0, atol=1e-12)
+            prev = out["x"][i, k]
