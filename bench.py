@@ -204,13 +204,14 @@ class Round:
     """Device buffers of one round and the three C-ABI calls on one stream."""
 
     def __init__(self, w: workload.Workload, seed: int, device, scheduler: str = "alg1",
-                 verify_layout: str = "padded"):
+                 verify_layout: str = "padded", head: str = "markov"):
         import speculative_decoding_draft_05_gb300 as dspark
 
         self.dspark = dspark
         self.w, self.seed, self.device = w, seed, device
         self.scheduler = scheduler
         self.packed = verify_layout == "packed"
+        self.rnn = workload.rnn_inputs(w, seed=seed, device=device) if head == "rnn" else None
         inp = workload.generate(w, seed=seed, device=device)
         self.inp = inp
         R, g, V = w.R, w.gamma, w.V
@@ -227,8 +228,9 @@ class Round:
         self.cstar = torch.empty(R, g, dtype=f32, device=device)
         self.lse_t = torch.empty(R, g + 1, dtype=f32, device=device)
         u8 = torch.uint8
-        self.ws_d = torch.empty(dspark.draft_workspace_bytes(R, g, V, w.r, w.torch_dtype), dtype=u8,
-                                device=device)
+        ws_draft = (dspark.draft_rnn_workspace_bytes(R, g, V, w.r) if head == "rnn"
+                    else dspark.draft_workspace_bytes(R, g, V, w.r, w.torch_dtype))
+        self.ws_d = torch.empty(ws_draft, dtype=u8, device=device)
         self.ws_s = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
         self.ws_s2 = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
         self.K = torch.empty(1, dtype=i32, device=device)
@@ -267,12 +269,20 @@ class Round:
 
         return workload.target_logits(w, inp["U"], self.seed, bias_rows=bias_rows)
 
-    def draft(self, seed=None):
+    def draft(self, seed=None, U=None, W1=None, W2=None, x0=None, Wh=None, Q=None):
         i = self.inp
         seed = self.seed if seed is None else seed
-        self.dspark.dspark_draft_sample(i["U"], i["W1"], i["W2"], i["x0"], self.w.T, seed,
-                                        x=self.x, logp=self.logp, lse=self.lse, scores=self.scores,
-                                        workspace=self.ws_d)
+        U = i["U"] if U is None else U
+        W1 = i["W1"] if W1 is None else W1
+        W2 = i["W2"] if W2 is None else W2
+        x0 = i["x0"] if x0 is None else x0
+        kw = dict(x=self.x, logp=self.logp, lse=self.lse, scores=self.scores, workspace=self.ws_d)
+        if self.rnn is not None:
+            Wh = self.rnn["Wh"] if Wh is None else Wh
+            Q = self.rnn["Q"] if Q is None else Q
+            self.dspark.dspark_draft_sample_rnn(U, W1, W2, Wh, Q, x0, self.w.T, seed, **kw)
+        else:
+            self.dspark.dspark_draft_sample(U, W1, W2, x0, self.w.T, seed, **kw)
 
     def schedule(self, conf=None, sps=None):
         d = self.dspark
@@ -294,8 +304,10 @@ class Round:
         U, W1, W2, x0, conf, sps, Z = ins[:7]
         d = self.dspark
         seed = self.seed if seed is None else seed
-        d.dspark_draft_sample(U, W1, W2, x0, self.w.T, seed, x=self.x, logp=self.logp, lse=self.lse,
-                              scores=self.scores, workspace=self.ws_d)
+        if self.rnn is not None:
+            self.draft(seed, U, W1, W2, x0, ins[-2], ins[-1])
+        else:
+            self.draft(seed, U, W1, W2, x0)
         self.schedule(conf, sps)
         if self.packed:
             d.dspark_verify_packed(self.x, self.logp, self.lse, self.scores, Z, ins[7], self.ell,
@@ -309,9 +321,11 @@ class Round:
 
     def input_tensors(self):
         i = self.inp
-        if self.packed:
-            return [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"], self.Zp, self.offsets]
-        return [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"], self.Z]
+        ins = [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"]]
+        ins += [self.Zp, self.offsets] if self.packed else [self.Z]
+        if self.rnn is not None:
+            ins += [self.rnn["Wh"], self.rnn["Q"]]
+        return ins
 
     def result_tensors(self):
         return [self.tokens, self.n_emit, self.n_acc, self.cstar, self.ell]
@@ -324,12 +338,22 @@ def draft_tile_bytes(w: workload.Workload) -> int:
     return w.R * w.V * (e + 4) + w.r * w.V * e + w.R * w.r * e
 
 
+def round_bytes(w: workload.Workload, ell) -> int:
+    """Algorithmic HBM bytes of one round: the W2 transpose (read + write), gamma
+    draft steps, and verify -- the Z rows of the scheduled positions and of the
+    drawn token (sum(l) + R rows) and the draft scores of the scheduled rows."""
+    e = 4 if w.dtype == "f32" else 2
+    rows = int(ell.sum().item())
+    return (2 * w.r * w.V * e + w.gamma * draft_tile_bytes(w)
+            + (rows + w.R) * w.V * e + rows * w.V * 4)
+
+
 def draft_tile_flops(w: workload.Workload) -> int:
     return 2 * w.R * w.r * w.V
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-def oracle_sample_round(w, inp_cpu, req, seed, nthreads, scheduler="alg1"):
+def oracle_sample_round(w, inp_cpu, req, seed, nthreads, scheduler="alg1", head="markov"):
     """Time one oracle round on the requests `req` (draft + full schedule + verify)."""
     import oracle
 
@@ -337,7 +361,12 @@ def oracle_sample_round(w, inp_cpu, req, seed, nthreads, scheduler="alg1"):
     W1, W2 = inp_cpu["W1_64"], inp_cpu["W2_64"]
     x0 = inp_cpu["x0"].numpy()[req]
     t0 = time.perf_counter()
-    od = oracle.draft(f64(inp_cpu["U"][req]), W1, W2, x0, w.T, seed, req_ids=req, nthreads=nthreads)
+    if head == "rnn":
+        rin = workload.rnn_inputs(w, seed=seed, device="cpu")
+        od = oracle.draft_rnn(f64(inp_cpu["U"][req]), W1, W2, f64(rin["Wh"]), f64(rin["Q"][req]), x0, w.T,
+                              seed, req_ids=req, nthreads=nthreads)
+    else:
+        od = oracle.draft(f64(inp_cpu["U"][req]), W1, W2, x0, w.T, seed, req_ids=req, nthreads=nthreads)
     t_draft = time.perf_counter() - t0
     # target stand-in for the sampled requests, from the oracle's own draft (untimed)
     if w.z_bias:
@@ -401,11 +430,11 @@ def run_reference(args, w, rank, world):
     n = max(1, sample_size(w, nthreads, target_s=120.0 / max(1, args.steps + args.warmup)))
     req = list(range(n))
     for _ in range(args.warmup):
-        oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler)
+        oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler, args.head)
     times = []
     emitted = 0
     for _ in range(args.steps):
-        t, e = oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler)
+        t, e = oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler, args.head)
         times.append(t)
         emitted += e
     tot = sum(times)
@@ -415,7 +444,7 @@ def run_reference(args, w, rank, world):
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": dict(workload.describe(w), seed=args.seed, scheduler=args.scheduler,
-                           sample_requests=n),
+                           head=args.head, sample_requests=n),
             "cpu_baseline": {"value": value, "unit": "positions/s", "cores": nthreads,
                              "kind": "oracle",
                              "sample": f"{n} of {w.R} requests per step (all positions, full V) "
@@ -436,7 +465,8 @@ def run_ours(args, w, rank, world, local):
     init_dist(world, "nccl")
     dspark.binding.load()
     stream = torch.cuda.current_stream(device)
-    rnd = Round(w, args.seed, device, scheduler=args.scheduler, verify_layout=args.verify_layout)
+    rnd = Round(w, args.seed, device, scheduler=args.scheduler, verify_layout=args.verify_layout,
+                head=args.head)
     seeds = [args.seed + i for i in range(args.steps)]  # one Philox key per round
     for i in range(args.warmup):
         rnd.step(args.seed + i)
@@ -551,6 +581,10 @@ def run_ours(args, w, rank, world, local):
                 "tensor": {"achieved_tflops": draft_tile_flops(w) / avg_tile_s / 1e12,
                            "peak_tflops": bf16_peak,
                            "frac": draft_tile_flops(w) / avg_tile_s / 1e12 / bf16_peak}}
+    rb = round_bytes(w, rnd.ell)
+    round_roof = {"bound": "hbm", "algorithmic_bytes": rb,
+                  "achieved": rb / (ms_max / args.steps / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                  "frac": rb / (ms_max / args.steps / 1e3) / 1e9 / hbm_peak}
     kernels = {k: {"ms_per_launch": v[0] / max(1, v[1]), "launches": v[1],
                    "share": v[0] / max(1e-9, sum(x[0] for kk, x in prof.items() if not kk.startswith("_")))}
                for k, v in prof.items() if not k.startswith("_")}
@@ -566,13 +600,13 @@ def run_ours(args, w, rank, world, local):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
                 if w.dtype == "bf16" else "f32", "data": "synthetic",
                 "config": dict(workload.describe(w), seed=args.seed, scheduler=args.scheduler,
-                               verify_layout=args.verify_layout,
+                               verify_layout=args.verify_layout, head=args.head,
                                parallelism="replicas" if world > 1 else "single",
                                l2="inputs larger than L2 (U %.2f GB, scores %.2f GB, Z %.2f GB > 129 MB)" % (
                                    w.R * w.gamma * w.V * (2 if w.dtype == "bf16" else 4) / 1e9,
                                    w.R * w.gamma * w.V * 4 / 1e9,
                                    rnd.input_tensors()[6].numel() * rnd.input_tensors()[6].element_size() / 1e9)),
-                "roofline": roofline, "cpu_baseline": out,
+                "roofline": roofline, "round_roofline": round_roof, "cpu_baseline": out,
                 "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": launches, "clocks": clocks.summary(),
@@ -597,6 +631,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scheduler", choices=["alg1", "zos"], default="alg1",
                     help="alg1: Algorithm 1 (default); zos: zero-overhead capacity + top-K")
+    ap.add_argument("--head", choices=["markov", "rnn"], default="markov",
+                    help="draft head: markov (default) or the RNN head")
     ap.add_argument("--verify-layout", choices=["padded", "packed"], default="padded",
                     help="target logits padded [R, gamma+1, V] (default) or packed rows + offsets")
     ap.add_argument("--R", type=int, default=None, help="override the workload's request count")

@@ -115,6 +115,31 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dspark_draft_sample_rnn -- the draft with the RNN head instead of the Markov
+ * head ([summary] §3.1: the alternative sequential head keeps a state across
+ * the block and also takes the backbone's hidden state).  Read as an Elman
+ * recurrence in the Markov head's rank-r space:
+ *   h_0 = 0,  h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k)   (fp32 state),
+ *   B_k = bf16(h_k) W2                                       (bf16 contraction),
+ * then s_k, lse_k, x_k, logp_k exactly as dspark_draft_sample.  With Wh = 0
+ * and Q = 0 it is dspark_draft_sample with W1 replaced by bf16(tanh(W1)).
+ *
+ * Wh [r, r] bf16 (row a, column j: h_{k-1}[a]'s weight on h_k[j]);
+ * Q  [R, gamma, r] float: the backbone hidden state of each position,
+ *    projected into the head's space;
+ * other arguments and outputs as dspark_draft_sample (bf16 only; r a multiple
+ * of 64, at most 256).
+ * workspace: >= dspark_draft_rnn_workspace_bytes(R, gamma, V, r) bytes,
+ *   256-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t dspark_draft_rnn_workspace_bytes(int R, int gamma, int V, int r);
+int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const void* Wh,
+                            const float* Q, const int32_t* x0, int dtype, int R, int gamma, int V,
+                            int r, float temperature, uint64_t seed, int32_t* x, float* logp,
+                            float* lse, float* scores, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ------------------------------------------------------------------------
  * dspark_schedule -- hardware-aware prefix scheduler, Algorithm 1
  * ([summary] §3.2.2).
  *   a_{r,j} = prod_{i<=j} c_{r,i}   (sequential fp32 product; c clamped to [0,1])

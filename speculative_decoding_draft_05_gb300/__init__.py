@@ -8,6 +8,8 @@ from . import workload  # noqa: F401
 from .binding import (  # noqa: F401
     DSparkError,
     dspark_draft_sample,
+    dspark_draft_sample_rnn,
+    draft_rnn_workspace_bytes,
     dspark_profile_start,
     dspark_profile_stop,
     dspark_read_device_status,
@@ -26,6 +28,8 @@ from .binding import (  # noqa: F401
 
 __all__ = [
     "dspark_draft_sample",
+    "dspark_draft_sample_rnn",
+    "draft_rnn_workspace_bytes",
     "dspark_schedule",
     "dspark_schedule_capacity",
     "dspark_schedule_topk",

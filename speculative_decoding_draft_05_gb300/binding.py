@@ -53,6 +53,10 @@ def load() -> ctypes.CDLL:
     L.dspark_draft_workspace_bytes.restype = SZ
     L.dspark_draft_sample.argtypes = [P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P, P, SZ, P]
     L.dspark_draft_sample.restype = I
+    L.dspark_draft_rnn_workspace_bytes.argtypes = [I, I, I, I]
+    L.dspark_draft_rnn_workspace_bytes.restype = SZ
+    L.dspark_draft_sample_rnn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P, P, SZ, P]
+    L.dspark_draft_sample_rnn.restype = I
     L.dspark_schedule_workspace_bytes.argtypes = [I, I]
     L.dspark_schedule_workspace_bytes.restype = SZ
     L.dspark_sts_workspace_bytes.argtypes = [I, I, I]
@@ -193,6 +197,35 @@ def dspark_draft_sample(U, W1, W2, x0, temperature: float, seed: int, *, x=None,
         _dev(logp, "logp", torch.float32, (R, g)), _dev(lse, "lse", torch.float32, (R, g)),
         _dev(scores, "scores", torch.float32, (R, g, V)), ws.data_ptr(), ws.numel(), _stream(stream))
     _check("dspark_draft_sample", st)
+    return dict(x=x, logp=logp, lse=lse, scores=scores, workspace=ws)
+
+
+def draft_rnn_workspace_bytes(R: int, gamma: int, V: int, r: int) -> int:
+    return int(load().dspark_draft_rnn_workspace_bytes(R, gamma, V, r))
+
+
+def dspark_draft_sample_rnn(U, W1, W2, Wh, Q, x0, temperature: float, seed: int, *, x=None,
+                            logp=None, lse=None, scores=None, workspace=None, stream=None) -> dict:
+    """Draft with the RNN head.  U [R, gamma, V], W1 [V, r], W2 [r, V], Wh [r, r] (bf16),
+    Q [R, gamma, r] float32, x0 [R] int32."""
+    L = load()
+    R, g, V = U.shape
+    r = W1.shape[1]
+    dt = U.dtype
+    dev = U.device
+    x = torch.empty(R, g, dtype=torch.int32, device=dev) if x is None else x
+    logp = torch.empty(R, g, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(R, g, dtype=torch.float32, device=dev) if lse is None else lse
+    scores = torch.empty(R, g, V, dtype=torch.float32, device=dev) if scores is None else scores
+    ws = _workspace(draft_rnn_workspace_bytes(R, g, V, r), dev, workspace)
+    st = L.dspark_draft_sample_rnn(
+        _dev(U, "U", dt), _dev(W1, "W1", dt, (V, r)), _dev(W2, "W2", dt, (r, V)),
+        _dev(Wh, "Wh", dt, (r, r)), _dev(Q, "Q", torch.float32, (R, g, r)),
+        _dev(x0, "x0", torch.int32, (R,)), _dtype_code(U), R, g, V, r, float(temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(x, "x", torch.int32, (R, g)),
+        _dev(logp, "logp", torch.float32, (R, g)), _dev(lse, "lse", torch.float32, (R, g)),
+        _dev(scores, "scores", torch.float32, (R, g, V)), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check("dspark_draft_sample_rnn", st)
     return dict(x=x, logp=logp, lse=lse, scores=scores, workspace=ws)
 
 

@@ -202,6 +202,87 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   return DSPARK_OK;
 }
 
+// The RNN head's extra scratch after the draft workspace: the state h [R, r]
+// fp32 and the A rows [R padded to 128, r] bf16.
+struct RnnWorkspace {
+  size_t h, A, total;
+};
+static RnnWorkspace rnn_workspace_layout(int R, int gamma, int V, int r) {
+  RnnWorkspace w;
+  w.h = align256(draft_workspace_layout(R, gamma, V, r, DSPARK_BF16).total);
+  w.A = align256(w.h + (size_t)R * r * sizeof(float));
+  w.total = align256(w.A + ((size_t)R + 127) / 128 * 128 * r * 2);
+  return w;
+}
+
+size_t dspark_draft_rnn_workspace_bytes(int R, int gamma, int V, int r) {
+  if (R <= 0 || gamma <= 0 || V <= 0 || r <= 0) return 0;
+  return rnn_workspace_layout(R, gamma, V, r).total;
+}
+
+int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const void* Wh,
+                            const float* Q, const int32_t* x0, int dtype, int R, int gamma, int V,
+                            int r, float temperature, uint64_t seed, int32_t* x, float* logp,
+                            float* lse, float* scores, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!U || !W1 || !W2 || !Wh || !Q || !x0 || !x || !logp || !lse || !scores)
+    return DSPARK_ERR_INVALID_ARG;
+  if (r <= 0) return DSPARK_ERR_INVALID_ARG;
+  int st = check_common(R, gamma, V, temperature, dtype);
+  if (st != DSPARK_OK) return st;
+  if (dtype != DSPARK_BF16 || r > 256 || r % 64 != 0 || !draft_tc_supported(R, V, r))
+    return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(scores))
+    return DSPARK_ERR_INVALID_ARG;
+  const DraftWorkspace L = draft_workspace_layout(R, gamma, V, r, dtype);
+  const RnnWorkspace LR = rnn_workspace_layout(R, gamma, V, r);
+  if (!workspace || workspace_bytes < LR.total || ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  int* status = (int*)(ws + L.status);
+  float* h = (float*)(ws + LR.h);
+  void* A = ws + LR.A;
+  const int n_parts = draft_tc_parts(R, V);
+  DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index), n_parts};
+  DraftPartials p2{(float4*)(ws + L.stats2), (int*)(ws + L.index2), n_parts};
+  const float invT = 1.0f / temperature;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e == cudaSuccess)  // A's rows past R stay zero: the contraction reads whole 128-row tiles
+    e = cudaMemsetAsync(A, 0, ((size_t)R + 127) / 128 * 128 * r * 2, s);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_rnn reset");
+  void* W2T = ws + L.w2t;
+  prof_begin(kKindPrepare, s);
+  e = launch_transpose_w2(W2, r, V, W2T, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
+  DraftTcPlan plan;
+  e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
+  if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
+  uint32_t* gthr = (uint32_t*)(ws + L.gthr);
+  e = cudaMemsetAsync(gthr, 0, 2 * (size_t)R * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "draft key reset");
+  const DraftPartials buf[2] = {p, p2};
+  for (int k = 1; k <= gamma; ++k) {
+    prof_begin(kKindPrepare, s);
+    e = launch_rnn_state(k, x0, W1, Wh, Q, buf[(k + 1) & 1], R, gamma, V, r, h, A, x, logp, lse,
+                         status, s);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "rnn_state");
+    prof_begin(kKindDraftTile, s);
+    e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], gthr, x,
+                             logp, lse, status, s, A);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "draft_step");
+  }
+  prof_begin(kKindDraftCombine, s);
+  e = launch_draft_combine(buf[gamma & 1], R, gamma, V, r, gamma, W1, dtype, nullptr, x, logp, lse,
+                           status, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
+  return DSPARK_OK;
+}
+
 size_t dspark_schedule_workspace_bytes(int R, int gamma) {
   if (R <= 0 || gamma <= 0) return 0;
   return 256 + align256(schedule_sorted_bytes(R, gamma));

@@ -253,6 +253,7 @@ struct Params {
   uint64_t seed;
   const int32_t* x0;             // anchors (step 1)
   const __nv_bfloat16* W1;       // [V, r]
+  const __nv_bfloat16* A_src;    // [R, r] precomputed A rows (RNN head), or nullptr
   const float4* prev_stats;      // step k-1 partials (k > 1)
   const int* prev_index;
   float4* pstats;                // this step's partials
@@ -430,7 +431,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     // in flight at once (two memory round trips for up to 40 parts, where
     // holding every part of every row at once would need too many registers).
     int xps[8];
-    if (p.k == 1) {
+    if (p.A_src) {  // the A rows come precomputed (RNN head); x_{k-1} is stored elsewhere
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xps[i] = 0;
+    } else if (p.k == 1) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int arow = m_tile * kTileM + warp * 8 + i;
@@ -499,7 +503,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       }
       gv[i] = make_uint4(0u, 0u, 0u, 0u);
       if (arow < p.R && lane < p.r / 8)  // 16 bytes = 8 of the row's r bf16 per lane
-        gv[i] = __ldg(reinterpret_cast<const uint4*>(p.W1 + (size_t)xp * p.r) + lane);
+        gv[i] = __ldg(reinterpret_cast<const uint4*>(
+                          p.A_src ? p.A_src + (size_t)arow * p.r : p.W1 + (size_t)xp * p.r) +
+                      lane);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -831,7 +837,7 @@ cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStr
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
                                  const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s) {
+                                 float* lse, int* status, cudaStream_t s, const void* A_src) {
   const int Mt = (plan.R + kTileM - 1) / kTileM;
   const int n_tiles = (plan.V + kTileN - 1) / kTileN;
   const int slots = draft_tc_parts(plan.R, plan.V);
@@ -850,6 +856,7 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.seed = seed;
   p.x0 = x0;
   p.W1 = (const __nv_bfloat16*)W1;
+  p.A_src = (const __nv_bfloat16*)A_src;
   p.prev_stats = prev.stats;
   p.prev_index = prev.index;
   p.pstats = cur.stats;

@@ -51,7 +51,15 @@ cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStr
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
                                  const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s);
+                                 float* lse, int* status, cudaStream_t s,
+                                 const void* A_src = nullptr);
+// RNN head, step k: x_{k-1} (anchor for k = 1, else the merge of `prev`, whose
+// x/logp/lse it also stores), h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k) in
+// place in h [R, r] (fp32), and A [R, r] = bf16(h_k) for the contraction.
+cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const void* Wh,
+                             const float* Q, const DraftPartials& prev, int R, int gamma, int V,
+                             int r, float* h, void* A, int32_t* x, float* logp, float* lse,
+                             int* status, cudaStream_t s);
 bool draft_tc_supported(int R, int V, int r);
 int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path
 

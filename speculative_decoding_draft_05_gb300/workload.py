@@ -164,6 +164,16 @@ def step_rate_table(w: Workload, device="cpu") -> torch.Tensor:
     return (1.0 / t).contiguous()
 
 
+def rnn_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """Inputs of the RNN draft head: Wh [r, r] ~ N(0, (0.5 / sqrt(r))^2) in the
+    workload dtype (a contractive recurrence), and the backbone hidden state
+    projected into the head's space, Q [R, gamma, r] ~ N(0, 0.5^2) (float32)."""
+    g = _gen(device, seed, "rnn")
+    Wh = (torch.randn(w.r, w.r, generator=g, device=device) * (0.5 / w.r ** 0.5)).to(w.torch_dtype)
+    Q = torch.randn(w.R, w.gamma, w.r, generator=g, device=device) * 0.5
+    return dict(Wh=Wh.contiguous(), Q=Q.contiguous())
+
+
 def generate(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
     """U, W1, W2, x0, conf, sps for workload ``w`` (dtype ``w.torch_dtype`` for U/W1/W2)."""
     dt = w.torch_dtype

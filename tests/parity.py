@@ -23,7 +23,8 @@ def f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def close(gpu, ref, dtype, what):
+def close(gpu, ref, dtype, what, extra=None):
+    """extra: an optional per-element absolute allowance (same shape), added to the tolerance."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     assert gpu.shape == ref.shape, what
@@ -32,21 +33,25 @@ def close(gpu, ref, dtype, what):
     g, r = gpu[~nan_g], ref[~nan_r]
     if g.size == 0:
         return
+    ex = 0.0 if extra is None else np.broadcast_to(np.asarray(extra, np.float64), gpu.shape)[~nan_g]
     if dtype == "f32":
-        err = np.abs(g - r).max()
-        assert err <= F32_ATOL, f"{what}: max abs error {err:.3g} > {F32_ATOL}"
+        err = (np.abs(g - r) - ex).max()
+        assert err <= F32_ATOL, f"{what}: max abs error beyond the allowance {err:.3g} > {F32_ATOL}"
     else:
-        bad = np.abs(g - r) > BF16_RTOL * np.abs(r) + BF16_ATOL
+        bad = np.abs(g - r) > BF16_RTOL * np.abs(r) + BF16_ATOL + ex
         assert not bad.any(), (f"{what}: {bad.sum()} values outside rtol {BF16_RTOL}; "
                                f"worst {np.abs(g - r)[bad].max():.3g}")
 
 
-def compare_draft(gd, od, dtype, scores_ref=None, scores_gpu=None):
+def compare_draft(gd, od, dtype, scores_ref=None, scores_gpu=None, tie=TIE, score_extra=None):
     """Compare draft outputs request by request.
 
     At a request's first token mismatch (allowed only at a near tie) the rest of
     that request is not compared: lse is still compared at that position (same
-    distribution), logp and later positions are not.  Returns the exempt set.
+    distribution), logp and later positions are not.  tie is a scalar or an
+    [n, gamma] array of per-position ties.  score_extra [n, gamma, V]
+    is an optional absolute allowance on the scores (and, through its row
+    maximum, on lse, logp and ln p^d).  Returns the exempt set.
     """
     gx = gd["x"]
     n, g = gx.shape
@@ -56,20 +61,25 @@ def compare_draft(gd, od, dtype, scores_ref=None, scores_gpu=None):
     for i in range(n):
         for k in range(g):
             if gx[i, k] != od["x"][i, k]:
-                assert od["margin"][i, k] < TIE, (
+                t = tie[i, k] if np.ndim(tie) else tie
+                assert od["margin"][i, k] < t, (
                     f"draft token differs at request {i} position {k + 1}: gpu {gx[i, k]} oracle "
                     f"{od['x'][i, k]} with margin {od['margin'][i, k]:.3g}")
                 exempt.add(i)
                 m_lse[i, k + 1:] = False
                 m_logp[i, k:] = False
                 break
-    close(gd["lse"][m_lse], od["lse"][m_lse], dtype, "lse")
-    close(gd["logp"][m_logp], od["logp"][m_logp], dtype, "logp")
+    row_ex = None if score_extra is None else np.asarray(score_extra).max(axis=-1)
+    close(gd["lse"][m_lse], od["lse"][m_lse], dtype, "lse", None if row_ex is None else row_ex[m_lse])
+    close(gd["logp"][m_logp], od["logp"][m_logp], dtype, "logp",
+          None if row_ex is None else 2 * row_ex[m_logp])
     if scores_ref is not None:
-        close(scores_gpu[m_lse], scores_ref[m_lse], dtype, "scores")
+        ex = None if score_extra is None else score_extra[m_lse]
+        close(scores_gpu[m_lse], scores_ref[m_lse], dtype, "scores", ex)
         pd_g = np.exp(scores_gpu[m_lse] - gd["lse"][m_lse][:, None])
         pd_o = np.exp(scores_ref[m_lse] - od["lse"][m_lse][:, None])
-        close(pd_g, pd_o, dtype, "p^d")
+        # |d ln p^d| <= |ds| + |d lse|: a relative allowance on p^d
+        close(pd_g, pd_o, dtype, "p^d", None if ex is None else pd_o * (np.expm1(ex + row_ex[m_lse][:, None])))
     return exempt
 
 
