@@ -587,7 +587,7 @@ def run_ours(args, w, rank, world, local):
                   "frac": rb / (ms_max / args.steps / 1e3) / 1e9 / hbm_peak}
     kernels = {k: {"ms_per_launch": v[0] / max(1, v[1]), "launches": v[1],
                    "share": v[0] / max(1e-9, sum(x[0] for kk, x in prof.items() if not kk.startswith("_")))}
-               for k, v in prof.items() if not k.startswith("_")}
+               for k, v in prof.items() if not k.startswith("_") and v[1] > 0}
     launches = sum(v[1] for k, v in prof.items() if not k.startswith("_"))
 
     out = None

@@ -128,7 +128,7 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
  * Q  [R, gamma, r] float: the backbone hidden state of each position,
  *    projected into the head's space;
  * other arguments and outputs as dspark_draft_sample (bf16 only; r a multiple
- * of 64, at most 256).
+ * of 64, at most 256; Wh and Q 16-byte aligned, else DSPARK_ERR_INVALID_ARG).
  * workspace: >= dspark_draft_rnn_workspace_bytes(R, gamma, V, r) bytes,
  *   256-byte aligned.
  * ---------------------------------------------------------------------- */
@@ -350,7 +350,8 @@ enum {
   DSPARK_KERNEL_SCHEDULE = 3,
   DSPARK_KERNEL_VERIFY_ROWS = 4,
   DSPARK_KERNEL_VERIFY_FINISH = 5,
-  DSPARK_KERNEL_KINDS = 6
+  DSPARK_KERNEL_RNN_STATE = 6,      /* RNN head: state update (gamma launches) */
+  DSPARK_KERNEL_KINDS = 7
 };
 int dspark_profile_start(void);
 int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches);

@@ -345,7 +345,8 @@ def dspark_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     return int(out.value)
 
 
-KERNEL_KINDS = ["prepare", "draft_tile", "draft_combine", "schedule", "verify_rows", "verify_finish"]
+KERNEL_KINDS = ["prepare", "draft_tile", "draft_combine", "schedule", "verify_rows", "verify_finish",
+                "rnn_state"]
 
 
 def dspark_profile_start() -> None:

@@ -202,15 +202,15 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   return DSPARK_OK;
 }
 
-// The RNN head's extra scratch after the draft workspace: the state h [R, r]
-// fp32 and the A rows [R padded to 128, r] bf16.
+// The RNN head's extra scratch after the draft workspace: the state h [2][R, r]
+// fp32 (double-buffered across steps) and the A rows [R padded to 128, r] bf16.
 struct RnnWorkspace {
   size_t h, A, total;
 };
 static RnnWorkspace rnn_workspace_layout(int R, int gamma, int V, int r) {
   RnnWorkspace w;
   w.h = align256(draft_workspace_layout(R, gamma, V, r, DSPARK_BF16).total);
-  w.A = align256(w.h + (size_t)R * r * sizeof(float));
+  w.A = align256(w.h + 2 * (size_t)R * r * sizeof(float));
   w.total = align256(w.A + ((size_t)R + 127) / 128 * 128 * r * 2);
   return w;
 }
@@ -230,14 +230,15 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
   if (r <= 0) return DSPARK_ERR_INVALID_ARG;
   int st = check_common(R, gamma, V, temperature, dtype);
   if (st != DSPARK_OK) return st;
-  if (dtype != DSPARK_BF16 || r > 256 || r % 64 != 0 || !draft_tc_supported(R, V, r))
-    return DSPARK_ERR_UNSUPPORTED;
-  if (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(scores))
+  if (dtype != DSPARK_BF16 || r > 256 || r % 64 != 0 || V % 8 != 0) return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(scores) || !aligned16(Wh) ||
+      !aligned16(Q))
     return DSPARK_ERR_INVALID_ARG;
   const DraftWorkspace L = draft_workspace_layout(R, gamma, V, r, dtype);
   const RnnWorkspace LR = rnn_workspace_layout(R, gamma, V, r);
   if (!workspace || workspace_bytes < LR.total || ((uintptr_t)workspace & 255u))
     return DSPARK_ERR_WORKSPACE;
+  if (!draft_tc_supported(R, V, r)) return DSPARK_ERR_UNSUPPORTED;  // needs the driver's TMA encoder
   cudaStream_t s = (cudaStream_t)stream;
   char* ws = (char*)workspace;
   int* status = (int*)(ws + L.status);
@@ -264,9 +265,10 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
   if (e != cudaSuccess) return cuda_fail(e, "draft key reset");
   const DraftPartials buf[2] = {p, p2};
   for (int k = 1; k <= gamma; ++k) {
-    prof_begin(kKindPrepare, s);
-    e = launch_rnn_state(k, x0, W1, Wh, Q, buf[(k + 1) & 1], R, gamma, V, r, h, A, x, logp, lse,
-                         status, s);
+    prof_begin(kKindRnnState, s);
+    e = launch_rnn_state(k, x0, W1, Wh, Q, buf[(k + 1) & 1], R, gamma, V, r,
+                         h + (size_t)((k + 1) & 1) * R * r, h + (size_t)(k & 1) * R * r, A, x, logp,
+                         lse, status, s);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "rnn_state");
     prof_begin(kKindDraftTile, s);

@@ -204,6 +204,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (the three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 1 + (w >> 9) 2^-23 as a float in [1, 2): the funnel shift of (0x7F : w) by 9
+// places w's top 23 bits under the exponent field of 1.0f.
+__device__ __forceinline__ float unit_float(uint32_t w) {
+  return __uint_as_float(__funnelshift_r(w, 0x7Fu, 9));
+}
+
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -212,38 +225,43 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 // returns the candidate mask and sets st = sum exp(s - mx).  Element i can beat
 // the running best key b only if 1 - u_i < y_i = exp(s_i - b); with
 // f_i = 1 + (w_i >> 9) 2^-23 = u_i + 1 - 2^-24 that is f_i > 2 - 2^-24 - y_i,
-// tested conservatively as f_i >= fl(2 - 1.001 y_i) (kf = 1.001 exp(mx - b)).
-// The scores are read back from the row's staged block (128-byte swizzle), one
-// 16-byte quad at a time.  MASKED: only the first nvalid columns take part.
+// tested conservatively as fl(f_i + 1.001 y_i) >= 2 (kf = 1.001 exp(mx - b);
+// one rounding of the same inequality, and it admits every element that
+// f_i >= fl(2 - 1.001 y_i) admits).  The arithmetic runs on float pairs
+// (one packed FMA or add for two elements).  The scores are read back from the
+// row's staged block (128-byte swizzle), one 16-byte quad at a time.  MASKED:
+// only the first nvalid columns take part.
 template <bool MASKED>
 __device__ __forceinline__ uint32_t filter_pass(const uint8_t* srow, int lane,
                                                 const PhiloxStream& rng, int col0, float mxl,
                                                 float kf, int nvalid, float& st) {
   const float L2E = 1.4426950408889634f;
-  float sum = 0.0f;
+  const float2 l2e = make_float2(L2E, L2E), nmx = make_float2(-mxl, -mxl), k2 = make_float2(kf, kf);
+  float2 sum01 = make_float2(0.0f, 0.0f), sum23 = make_float2(0.0f, 0.0f);
   uint32_t cand = 0;
 #pragma unroll 2
   for (int q4 = 0; q4 < 8; ++q4) {
     const float4 sv = *(const float4*)(srow + ((q4 ^ (lane & 7)) << 4));
     const uint4 w4 = rng.quad((uint32_t)((col0 >> 2) + q4));
-    const float sq[4] = {sv.x, sv.y, sv.z, sv.w};
-    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+    const float2 a01 = __ffma2_rn(make_float2(sv.x, sv.y), l2e, nmx);
+    const float2 a23 = __ffma2_rn(make_float2(sv.z, sv.w), l2e, nmx);
+    float e[4] = {ex2_approx(a01.x), ex2_approx(a01.y), ex2_approx(a23.x), ex2_approx(a23.y)};
+    if (MASKED) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = 4 * q4 + j;
-      const float e = ex2_approx(fmaf(sq[j], L2E, -mxl));
-      const float f = __uint_as_float(0x3F800000u | (wv[j] >> 9));
-      const bool c = f >= fmaf(-e, kf, 2.0f);
-      if (MASKED) {
-        sum += i < nvalid ? e : 0.0f;
-        cand |= (c && i < nvalid) ? (1u << i) : 0u;
-      } else {
-        sum += e;
-        cand |= c ? (1u << i) : 0u;
-      }
+      for (int j = 0; j < 4; ++j)
+        if (4 * q4 + j >= nvalid) e[j] = 0.0f;  // then f + 0 < 2: never a candidate
     }
+    const float2 e01 = make_float2(e[0], e[1]), e23 = make_float2(e[2], e[3]);
+    const float2 d01 = __ffma2_rn(e01, k2, make_float2(unit_float(w4.x), unit_float(w4.y)));
+    const float2 d23 = __ffma2_rn(e23, k2, make_float2(unit_float(w4.z), unit_float(w4.w)));
+    sum01 = __fadd2_rn(sum01, e01);
+    sum23 = __fadd2_rn(sum23, e23);
+    cand |= d01.x >= 2.0f ? 1u << (4 * q4) : 0u;
+    cand |= d01.y >= 2.0f ? 1u << (4 * q4 + 1) : 0u;
+    cand |= d23.x >= 2.0f ? 1u << (4 * q4 + 2) : 0u;
+    cand |= d23.y >= 2.0f ? 1u << (4 * q4 + 3) : 0u;
   }
-  st = sum;
+  st = (sum01.x + sum01.y) + (sum23.x + sum23.y);
   return cand;
 }
 
@@ -559,12 +577,17 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       if (lane == 0) mbar_arrive(&bar_acc_empty[buf]);
 
       float s[32];
+      {
+        const float2 invT2 = make_float2(p.invT, p.invT);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float u0 = __uint_as_float(upk[i] << 16);
-        const float u1 = __uint_as_float(upk[i] & 0xffff0000u);
-        s[2 * i] = (u0 + __uint_as_float(acc[2 * i])) * p.invT;
-        s[2 * i + 1] = (u1 + __uint_as_float(acc[2 * i + 1])) * p.invT;
+        for (int i = 0; i < 16; ++i) {  // (u + acc) / T on float pairs
+          const float2 u2 = make_float2(__uint_as_float(upk[i] << 16),
+                                        __uint_as_float(upk[i] & 0xffff0000u));
+          const float2 a2 = make_float2(__uint_as_float(acc[2 * i]), __uint_as_float(acc[2 * i + 1]));
+          const float2 s2 = __fmul2_rn(__fadd2_rn(u2, a2), invT2);
+          s[2 * i] = s2.x;
+          s[2 * i + 1] = s2.y;
+        }
       }
 
       // Stage s (128-byte rows, 128-byte swizzle) and store it with TMA.
@@ -593,9 +616,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           for (int i = 0; i < 32; ++i)
             if (i >= nvalid) s[i] = -INFINITY;
         }
-        float mx = s[0];
+        float mx = fmax3(s[0], s[1], s[2]);
 #pragma unroll
-        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
+        for (int i = 3; i < 31; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
+        mx = fmaxf(mx, s[31]);
         // Threshold: the best key this row has reached so far in any of the
         // CTA's four column groups (shared memory) or in any CTA of this step
         // (global, raised with atomicMax).  Every published key is one an

@@ -54,12 +54,14 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
                                  float* lse, int* status, cudaStream_t s,
                                  const void* A_src = nullptr);
 // RNN head, step k: x_{k-1} (anchor for k = 1, else the merge of `prev`, whose
-// x/logp/lse it also stores), h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k) in
-// place in h [R, r] (fp32), and A [R, r] = bf16(h_k) for the contraction.
+// x/logp/lse it also stores), h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k) from
+// h_prev into h_next ([R, r] fp32 each; h_prev unread for k = 1), and
+// A [R, r] = bf16(h_k) for the contraction.  r a multiple of 64, at most 256;
+// Wh 16-byte aligned.
 cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const void* Wh,
                              const float* Q, const DraftPartials& prev, int R, int gamma, int V,
-                             int r, float* h, void* A, int32_t* x, float* logp, float* lse,
-                             int* status, cudaStream_t s);
+                             int r, const float* h_prev, float* h_next, void* A, int32_t* x,
+                             float* logp, float* lse, int* status, cudaStream_t s);
 bool draft_tc_supported(int R, int V, int r);
 int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path
 
@@ -138,7 +140,8 @@ enum KernelKind {
   kKindSchedule = 3,  // both scheduler launches
   kKindVerifyRows = 4,
   kKindVerifyFinish = 5,
-  kKindCount = 6
+  kKindRnnState = 6,  // RNN head: state update before each draft step
+  kKindCount = 7
 };
 
 }  // namespace dspark

@@ -11,9 +11,12 @@
 // stores x, logp, lse of step k-1), then updates the state in fp32 and writes
 // its bf16 rounding (nearest, ties to even) as the step's A rows.
 //
-// One CTA of kRnnThreads >= r threads takes kRnnRows rows: warp i merges row
-// i, then thread j forms element j of every row's new state, streaming
-// column j of Wh (coalesced across threads) once for all kRnnRows rows.
+// Grid: (row blocks of kRnnRows) x (column blocks of kRnnCols).  A CTA stages
+// its column block of Wh (r x 64 bf16, 32 KB) and its rows' previous states
+// (fp32) in shared memory; warp i merges row i's partials of step k-1, then
+// lane l forms state columns c0 + 2l, c0 + 2l + 1 of row i.  The state is
+// double-buffered (step k reads h_{k-1}, writes h_k) because the CTAs of one
+// row read all of h_{k-1} while each writes only its own columns.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -23,22 +26,56 @@ namespace dspark {
 
 namespace {
 
-constexpr int kRnnThreads = 256;  // >= r (r <= 256)
-constexpr int kRnnRows = 4;
+constexpr int kRnnThreads = 256;
+constexpr int kRnnRows = kRnnThreads / 32;  // one row per warp
+constexpr int kRnnCols = 64;                // two columns per lane
+constexpr int kRnnMaxR = 256;
 
 __global__ void __launch_bounds__(kRnnThreads)
 rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __restrict__ W1,
                  const __nv_bfloat16* __restrict__ Wh, const float* __restrict__ Q,
                  const float4* __restrict__ prev_stats, const int* __restrict__ prev_index,
-                 int n_parts, int R, int gamma, int V, int r, float* __restrict__ h,
-                 __nv_bfloat16* __restrict__ A, int32_t* __restrict__ x, float* __restrict__ logp,
-                 float* __restrict__ lse, int* __restrict__ status) {
+                 int n_parts, int R, int gamma, int V, int r, const float* __restrict__ h_prev,
+                 float* __restrict__ h_next, __nv_bfloat16* __restrict__ A, int32_t* __restrict__ x,
+                 float* __restrict__ logp, float* __restrict__ lse, int* __restrict__ status) {
   __shared__ int s_x[kRnnRows];
-  __shared__ float s_h[kRnnRows][256];
+  __shared__ float s_h[kRnnRows][kRnnMaxR];
+  __shared__ __align__(16) __nv_bfloat162 s_w[kRnnMaxR][kRnnCols / 2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.x * kRnnRows;
-  if (warp < kRnnRows) {
-    const int row = row0 + warp;
+  const int row0 = blockIdx.x * kRnnRows, c0 = blockIdx.y * kRnnCols;
+  constexpr int kLoads = kRnnMaxR * 8 / kRnnThreads;  // 16-byte Wh vectors (and h values) per thread
+  // Every global load of the prologue is issued before the first use, so the
+  // CTA waits for one round of memory latency rather than one per load.
+  uint4 wv[kLoads];
+  float hv[kLoads];
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int v = threadIdx.x + u * kRnnThreads;  // Wh[:, c0 : c0 + 64] as r rows of 8 vectors
+    if (v < r * 8) wv[u] = __ldg((const uint4*)(Wh + (size_t)(v >> 3) * r + c0) + (v & 7));
+    const int i = v / r, row = row0 + i;  // previous states of the CTA's rows
+    hv[u] = (v < kRnnRows * r && k > 1 && row < R) ? h_prev[(size_t)row * r + (v - i * r)] : 0.0f;
+  }
+  const int row = row0 + warp;
+  const int j = c0 + 2 * lane;
+  float2 q = make_float2(0.0f, 0.0f);
+  if (row < R) q = *(const float2*)(Q + ((size_t)row * gamma + (k - 1)) * r + j);
+  // The previous step's partials of this warp's row (at most 2 per lane issued at once).
+  float4 ps[2];
+  int pi[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int t = lane + 32 * u;
+    const bool use = k > 1 && row < R && t < n_parts;
+    ps[u] = use ? prev_stats[(size_t)row * n_parts + t] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+    pi[u] = use ? prev_index[(size_t)row * n_parts + t] : 0x7fffffff;
+  }
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int v = threadIdx.x + u * kRnnThreads;
+    if (v < r * 8) *(uint4*)&s_w[v >> 3][(v & 7) * 4] = wv[u];
+    if (v < kRnnRows * r) s_h[v / r][v % r] = hv[u];
+  }
+  {
     int xp = 0;
     if (row < R) {
       if (k == 1) {
@@ -47,13 +84,14 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
         float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
         int idx = 0x7fffffff;
         for (int t = lane; t < n_parts; t += 32) {
-          const float4 q = prev_stats[(size_t)row * n_parts + t];
-          const int qi = prev_index[(size_t)row * n_parts + t];
-          lse_merge(m, S, q.x, q.y);
-          if (better(q.z, qi, key, idx)) {
-            key = q.z;
+          const int u = (t - lane) >> 5;
+          const float4 qs = u < 2 ? ps[u] : prev_stats[(size_t)row * n_parts + t];
+          const int qi = u < 2 ? pi[u] : prev_index[(size_t)row * n_parts + t];
+          lse_merge(m, S, qs.x, qs.y);
+          if (better(qs.z, qi, key, idx)) {
+            key = qs.z;
             idx = qi;
-            sv = q.w;
+            sv = qs.w;
           }
         }
         warp_lse(m, S);
@@ -69,7 +107,7 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
           }
         }
         xp = idx;
-        if (lane == 0) {
+        if (lane == 0 && blockIdx.y == 0) {  // one CTA per row stores step k-1
           const float l = m + logf(S);
           const size_t o = (size_t)row * gamma + (k - 2);
           x[o] = idx;
@@ -84,47 +122,34 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
     }
     if (lane == 0) s_x[warp] = xp;
   }
-  for (int i = 0; i < kRnnRows; ++i) {
-    const int row = row0 + i;
-    if (threadIdx.x < r) s_h[i][threadIdx.x] = (row < R && k > 1) ? h[(size_t)row * r + threadIdx.x] : 0.0f;
-  }
   __syncthreads();
-  const int j = threadIdx.x;
-  if (j >= r) return;
-  float z[kRnnRows];
-#pragma unroll
-  for (int i = 0; i < kRnnRows; ++i) {
-    const int row = row0 + i;
-    z[i] = row < R ? __bfloat162float(W1[(size_t)s_x[i] * r + j]) +
-                         Q[((size_t)row * gamma + (k - 1)) * r + j]
-                   : 0.0f;
-  }
+  if (row >= R) return;
+  const float2 w1 = __bfloat1622float2(*(const __nv_bfloat162*)(W1 + (size_t)s_x[warp] * r + j));
+  float z0 = w1.x + q.x, z1 = w1.y + q.y;
+  const float* hr = s_h[warp];
+#pragma unroll 8
   for (int a = 0; a < r; ++a) {
-    const float w = __bfloat162float(Wh[(size_t)a * r + j]);
-#pragma unroll
-    for (int i = 0; i < kRnnRows; ++i) z[i] = fmaf(s_h[i][a], w, z[i]);
+    const float hv = hr[a];
+    const float2 wv = __bfloat1622float2(s_w[a][lane]);
+    z0 = fmaf(hv, wv.x, z0);
+    z1 = fmaf(hv, wv.y, z1);
   }
-#pragma unroll
-  for (int i = 0; i < kRnnRows; ++i) {
-    const int row = row0 + i;
-    if (row < R) {
-      const float hn = tanhf(z[i]);
-      h[(size_t)row * r + j] = hn;
-      A[(size_t)row * r + j] = __float2bfloat16_rn(hn);
-    }
-  }
+  const float h0 = tanhf(z0), h1 = tanhf(z1);
+  *(float2*)(h_next + (size_t)row * r + j) = make_float2(h0, h1);
+  *(__nv_bfloat162*)(A + (size_t)row * r + j) = __floats2bfloat162_rn(h0, h1);
 }
 
 }  // namespace
 
 cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const void* Wh,
                              const float* Q, const DraftPartials& prev, int R, int gamma, int V,
-                             int r, float* h, void* A, int32_t* x, float* logp, float* lse,
-                             int* status, cudaStream_t s) {
-  if (r > kRnnThreads) return cudaErrorInvalidValue;
-  rnn_state_kernel<<<(R + kRnnRows - 1) / kRnnRows, kRnnThreads, 0, s>>>(
+                             int r, const float* h_prev, float* h_next, void* A, int32_t* x,
+                             float* logp, float* lse, int* status, cudaStream_t s) {
+  if (r > kRnnMaxR || r % kRnnCols != 0) return cudaErrorInvalidValue;
+  const dim3 grid((R + kRnnRows - 1) / kRnnRows, r / kRnnCols);
+  rnn_state_kernel<<<grid, kRnnThreads, 0, s>>>(
       k, x0, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)Wh, Q, prev.stats, prev.index,
-      prev.n_parts, R, gamma, V, r, h, (__nv_bfloat16*)A, x, logp, lse, status);
+      prev.n_parts, R, gamma, V, r, h_prev, h_next, (__nv_bfloat16*)A, x, logp, lse, status);
   return cudaGetLastError();
 }
 

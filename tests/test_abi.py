@@ -108,3 +108,28 @@ def test_zero_overhead_schedule_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.dspark_schedule_topk(16, 16, 0, 4, 16, 256, 256, None) == 1
     assert lib.dspark_schedule_topk(16, 16, 4, 65, 16, 256, 1 << 20, None) == 2
     assert lib.dspark_schedule_topk(16, 16, 4, 4, 16, 256, 8, None) == 3
+
+
+def _draft_rnn(lib, **kw):
+    a = dict(U=16, W1=16, W2=16, Wh=16, Q=16, x0=16, dtype=1, R=4, gamma=4, V=1024, r=64, T=1.0, seed=0,
+             x=16, logp=16, lse=16, scores=16, ws=256, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.dspark_draft_sample_rnn(a["U"], a["W1"], a["W2"], a["Wh"], a["Q"], a["x0"], a["dtype"],
+                                       a["R"], a["gamma"], a["V"], a["r"], a["T"], a["seed"], a["x"],
+                                       a["logp"], a["lse"], a["scores"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_rnn_draft_rejects_bad_arguments_on_the_host(lib):
+    # Every case fails validation before any CUDA call (pointers are never dereferenced).
+    assert lib.dspark_draft_rnn_workspace_bytes(4, 4, 1024, 64) > lib.dspark_draft_workspace_bytes(4, 4, 1024, 64, 1)
+    assert lib.dspark_draft_rnn_workspace_bytes(0, 4, 1024, 64) == 0
+    assert _draft_rnn(lib, Wh=None) == 1
+    assert _draft_rnn(lib, Q=None) == 1
+    assert _draft_rnn(lib, T=0.0) == 1
+    assert _draft_rnn(lib, dtype=0) == 2  # fp32: the RNN head is bf16 only
+    assert _draft_rnn(lib, r=96) == 2
+    assert _draft_rnn(lib, r=320) == 2
+    assert _draft_rnn(lib, Wh=24) == 1  # not 16-byte aligned
+    assert _draft_rnn(lib, Q=8) == 1
+    assert _draft_rnn(lib, ws=None) == 3
+    assert _draft_rnn(lib, wsb=16) == 3
