@@ -396,11 +396,12 @@ def oracle_inputs(w, seed, device):
     return cpu
 
 
-def sample_size(w, nthreads, target_s=12.0):
-    """Requests per oracle sample: about target_s seconds of work on nthreads."""
-    per_req = 2.0 * w.r * w.V * w.gamma * 1.2e-9 + w.gamma * w.V * 4e-7  # ~s per request, one core
-    n = int(max(1, min(w.R, round(target_s * nthreads / max(per_req, 1e-6)))))
-    return n
+def sample_size(w, inp, seed, nthreads, target_s=12.0, scheduler="alg1", head="markov"):
+    """Requests per oracle sample: about target_s seconds of work on nthreads, scaled
+    from a timed probe of one request per thread (the host's speed is not assumed)."""
+    n0 = max(1, min(w.R, nthreads))
+    t0, _ = oracle_sample_round(w, inp, list(range(n0)), seed, nthreads, scheduler, head)
+    return int(max(1, min(w.R, round(target_s * n0 / max(t0, 1e-6)))))
 
 
 def cpu_baseline(w, seed, device, nthreads):
@@ -408,7 +409,7 @@ def cpu_baseline(w, seed, device, nthreads):
 
     oracle.build()
     inp = oracle_inputs(w, seed, device)
-    n = sample_size(w, nthreads)
+    n = sample_size(w, inp, seed, nthreads)
     req = list(range(n))
     t, _ = oracle_sample_round(w, inp, req, seed, nthreads)
     return {"value": n * w.gamma / t, "unit": "positions/s", "cores": nthreads, "kind": "oracle",
@@ -427,7 +428,8 @@ def run_reference(args, w, rank, world):
     nthreads = os.cpu_count() or 1
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     inp = oracle_inputs(w, args.seed, device)
-    n = max(1, sample_size(w, nthreads, target_s=120.0 / max(1, args.steps + args.warmup)))
+    n = sample_size(w, inp, args.seed, nthreads, target_s=120.0 / max(1, args.steps + args.warmup),
+                    scheduler=args.scheduler, head=args.head)
     req = list(range(n))
     for _ in range(args.warmup):
         oracle_sample_round(w, inp, req, args.seed, nthreads, args.scheduler, args.head)

@@ -212,6 +212,7 @@ schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double
   // before it B = R + i and tau = R + P_i; after it B = R + i + 1.
   const long long tau0 = (long long)R << 48;
   long long run = run0;
+  int first_fail = n + 1;  // this thread's first non-improving candidate (1-based)
 #pragma unroll
   for (int e = 0; e < kPerThread; ++e) {
     const int i = base + e;
@@ -219,9 +220,12 @@ schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double
       const long long tau_prev = tau0 + run;
       run += fixed_survival(k[e]);
       if (!exact_greater(tau0 + run, sps[R + i + 1], tau_prev, sps[R + i], status))
-        atomicMin(&stop_at, i + 1);
+        first_fail = min(first_fail, i + 1);
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first_fail = min(first_fail, __shfl_xor_sync(0xffffffffu, first_fail, o));
+  if (lane == 0 && first_fail <= n) atomicMin(&stop_at, first_fail);  // one per warp
   __syncthreads();
   const int taken = stop_at - 1;  // candidates 0..taken-1 were taken
 #pragma unroll
