@@ -234,6 +234,9 @@ class Round:
         self.ws_s = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
         self.ws_s2 = torch.empty(dspark.schedule_workspace_bytes(R, g), dtype=u8, device=device)
         self.K = torch.empty(1, dtype=i32, device=device)
+        # The schedule reads only the confidences and the step-rate table, not the
+        # drafted tokens, so it runs on a side stream beside the draft.
+        self.side = torch.cuda.Stream(device) if torch.cuda.is_available() else None
         self.ws_v = torch.empty(dspark.verify_workspace_bytes(R, g, V), dtype=u8, device=device)
         # Target logits: the workload's target stand-in carries the Markov bias
         # along the draft's own tokens; run the (deterministic) draft once, untimed.
@@ -304,11 +307,15 @@ class Round:
         U, W1, W2, x0, conf, sps, Z = ins[:7]
         d = self.dspark
         seed = self.seed if seed is None else seed
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)  # the round's inputs are in place
+        with torch.cuda.stream(self.side):
+            self.schedule(conf, sps)
         if self.rnn is not None:
             self.draft(seed, U, W1, W2, x0, ins[-2], ins[-1])
         else:
             self.draft(seed, U, W1, W2, x0)
-        self.schedule(conf, sps)
+        main.wait_stream(self.side)  # verify needs l
         if self.packed:
             d.dspark_verify_packed(self.x, self.logp, self.lse, self.scores, Z, ins[7], self.ell,
                                    self.w.T, seed, n_acc=self.n_acc, tokens=self.tokens,

@@ -467,14 +467,20 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
         thr = warp_max(best);
       }
       if (have) {
-        // candidate iff f_i >= fl(2 - 1.001 exp(z_i / T - b)), f_i = 1 + (w_i >> 9) 2^-23
-        const float c0 = -thr * L2E;
+        // candidate iff fl(f_i + 1.001 exp(z_i / T - b)) >= 2, f_i = 1 + (w_i >> 9) 2^-23:
+        // one rounding of f_i >= 2 - 1.001 exp(z_i / T - b), on float pairs
+        const float2 it2 = make_float2(invT_l2e, invT_l2e), c02 = make_float2(-thr * L2E, -thr * L2E);
+        const float2 k2 = make_float2(1.001f, 1.001f);
         uint32_t cand = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float y = ex2_approx(fmaf(e[i], invT_l2e, c0));
-          const float f = __uint_as_float(0x3F800000u | (w[i] >> 9));
-          cand |= (f >= fmaf(-1.001f, y, 2.0f)) ? (1u << i) : 0u;
+        for (int i = 0; i < 8; i += 2) {
+          const float2 a = __ffma2_rn(make_float2(e[i], e[i + 1]), it2, c02);
+          const float2 y = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          const float2 f = make_float2(__uint_as_float(__funnelshift_r(w[i], 0x7Fu, 9)),
+                                       __uint_as_float(__funnelshift_r(w[i + 1], 0x7Fu, 9)));
+          const float2 d = __ffma2_rn(y, k2, f);
+          cand |= d.x >= 2.0f ? (1u << i) : 0u;
+          cand |= d.y >= 2.0f ? (2u << i) : 0u;
         }
         if (cand) {
 #pragma unroll
