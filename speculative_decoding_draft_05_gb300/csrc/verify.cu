@@ -237,9 +237,14 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
   constexpr int kRowUnroll = row_unroll<T>();  // 64 bytes of Z per thread in flight
   const int n_rows = *count;
   const int groups = V >> 3;
+  // Equal waves: with w = ceil(rows / grid) rows per CTA, only the first
+  // ceil(rows / w) CTAs take rows, so every working CTA takes w or w - 1 and no
+  // last wave runs part-empty (1088 rows on 304 CTAs: 272 CTAs x 4 rows).
+  const int waves = n_rows > 0 ? (n_rows + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  const int stride = (n_rows + waves - 1) / waves;
   uint32_t item = (int)blockIdx.x < n_rows ? list[blockIdx.x] : 0u;
-  for (int i = blockIdx.x; i < n_rows; i += gridDim.x) {
-    const uint32_t item_next = i + (int)gridDim.x < n_rows ? list[i + gridDim.x] : 0u;
+  for (int i = blockIdx.x; i < n_rows && (int)blockIdx.x < stride; i += stride) {
+    const uint32_t item_next = i + stride < n_rows ? list[i + stride] : 0u;
     const int r = (int)(item / (uint32_t)gamma), j = (int)(item - (uint32_t)r * gamma) + 1;
     const size_t rj = (size_t)r * gamma + (j - 1);
     const T* z = Z + zr.row(r, j) * V;
