@@ -343,6 +343,55 @@ __device__ __forceinline__ int leading_accepts(const int* __restrict__ acc_ws, i
   return n;
 }
 
+// Philox4x32-10 round keys of one seed, passed by value as a kernel parameter:
+// the rounds read them as constant-bank operands rather than holding 20
+// registers (the draw kernel runs at 48 registers per thread).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys K;
+  uint32_t k0 = (uint32_t)(seed & 0xffffffffu), k1 = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    K.k0[i] = k0;
+    K.k1[i] = k1;
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+  return K;
+}
+
+// The same words as PhiloxStream (one (request, position, purpose), varying first
+// counter word q), with the round keys taken from a PhiloxKeys parameter.
+struct KeyedPhilox {
+  uint32_t a1, b_hi, b_lo, pk1;
+  __device__ __forceinline__ KeyedPhilox(const PhiloxKeys& K, uint32_t request, uint32_t position,
+                                         uint32_t purpose) {
+    const unsigned long long p1 = (unsigned long long)kPhiloxM1 * request;
+    const uint32_t a0 = (uint32_t)(p1 >> 32) ^ position ^ K.k0[0];
+    a1 = (uint32_t)p1;
+    const unsigned long long pb = (unsigned long long)kPhiloxM0 * a0;
+    b_hi = (uint32_t)(pb >> 32);
+    b_lo = (uint32_t)pb;
+    pk1 = purpose ^ K.k1[0];
+  }
+  __device__ __forceinline__ uint4 quad(const PhiloxKeys& K, uint32_t q) const {
+    const unsigned long long p0 = (unsigned long long)kPhiloxM0 * q;
+    const uint32_t c2 = (uint32_t)(p0 >> 32) ^ pk1;
+    const uint32_t c3 = (uint32_t)p0;
+    const unsigned long long p1 = (unsigned long long)kPhiloxM1 * c2;
+    uint4 c = make_uint4((uint32_t)(p1 >> 32) ^ a1 ^ K.k0[1], (uint32_t)p1, b_hi ^ c3 ^ K.k1[1], b_lo);
+#pragma unroll
+    for (int i = 2; i < 10; ++i) {
+      const unsigned long long m0 = (unsigned long long)kPhiloxM0 * c.x;
+      const unsigned long long m1 = (unsigned long long)kPhiloxM1 * c.z;
+      c = make_uint4((uint32_t)(m1 >> 32) ^ c.y ^ K.k0[i], (uint32_t)m1,
+                     (uint32_t)(m0 >> 32) ^ c.w ^ K.k1[i], (uint32_t)m0);
+    }
+    return c;
+  }
+};
+
 constexpr int kDrawThreads = 256;
 constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 ids)
 
@@ -359,7 +408,7 @@ template <typename T>
 __global__ void __launch_bounds__(kDrawThreads, 5)
 verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
                    const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
-                   float invT, uint64_t seed, const float* __restrict__ lse_t_ws,
+                   float invT, const PhiloxKeys keys, const float* __restrict__ lse_t_ws,
                    const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks,
                    ZRows zr) {
   __shared__ float rk[kDrawThreads / 32];
@@ -381,7 +430,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   const int groups = V >> 3;
   const int g0 = chunk * kDrawGroups, g1 = min(groups, g0 + kDrawGroups);
   const float L2E = 1.4426950408889634f;
-  const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
+  const KeyedPhilox rng(keys, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
   // best/idx: this thread's argmax; a lane publishes its best key into the
   // CTA's threshold whenever it beats the threshold it filtered against.
   float best = -INFINITY;
@@ -398,7 +447,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
         float e[8], sc[8];
         load8(z, g, e);
         load8(srow, g, sc);
-        const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
+        const uint4 w0 = rng.quad(keys, 2 * g), w1 = rng.quad(keys, 2 * g + 1);
         const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         const float thr = ord_key(*cta_best);
         const float kb = thr == -INFINITY ? INFINITY : ex2_approx(-thr * L2E) * 1.001f;
@@ -436,7 +485,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
       uint32_t w[8];
       if (have) {
         load8(z, g, e);
-        const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
+        const uint4 w0 = rng.quad(keys, 2 * g), w1 = rng.quad(keys, 2 * g + 1);
         w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
         w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
       }
@@ -624,15 +673,15 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
   dim3 grid(chunks, R);
   if (dtype == DSPARK_BF16) {
     verify_draw_kernel<__nv_bfloat16><<<grid, kDrawThreads, 0, s>>>(
-        lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials,
-        chunks, zr);
+        lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
+        partials, chunks, zr);
     verify_emit_kernel<__nv_bfloat16><<<R, kVerifyThreads, 0, s>>>(
         x, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials, chunks,
         n_acc, tokens, n_emit, cstar, lse_t, zr);
   } else {
     verify_draw_kernel<float><<<grid, kDrawThreads, 0, s>>>(lse, scores, (const float*)Z, ell, gamma,
-                                                            V, invT, seed, lse_t_ws, acc_ws,
-                                                            partials, chunks, zr);
+                                                            V, invT, philox_keys(seed), lse_t_ws,
+                                                            acc_ws, partials, chunks, zr);
     verify_emit_kernel<float><<<R, kVerifyThreads, 0, s>>>(x, (const float*)Z, ell, gamma, V, invT,
                                                            seed, lse_t_ws, acc_ws, partials, chunks,
                                                            n_acc, tokens, n_emit, cstar, lse_t, zr);
