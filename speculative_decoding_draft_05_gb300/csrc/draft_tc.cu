@@ -838,13 +838,11 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, 
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(draft_step_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // Once per process (thread-safe initialisation of a function-local static).
+  static const cudaError_t attr_err =
+      cudaFuncSetAttribute(draft_step_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (attr_err != cudaSuccess) return attr_err;
   plan->R = R;
   plan->gamma = gamma;
   plan->V = V;

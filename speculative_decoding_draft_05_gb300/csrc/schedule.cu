@@ -392,14 +392,11 @@ cudaError_t launch_schedule_rank(const float* conf, int R, int gamma, unsigned l
   const int n = R * gamma;
   if (n > kMaxCandidates) return cudaErrorInvalidValue;
   const size_t smem = (size_t)n * sizeof(unsigned long long);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(schedule_rank_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kMaxCandidates * sizeof(unsigned long long)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // Once per process (thread-safe initialisation of a function-local static).
+  static const cudaError_t attr_err =
+      cudaFuncSetAttribute(schedule_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(kMaxCandidates * sizeof(unsigned long long)));
+  if (attr_err != cudaSuccess) return attr_err;
   int blocks = (n + 31) / 32;  // 32 candidates per CTA pass
   const int sms = sm_count_sched();
   if (blocks > sms) blocks = sms;
@@ -413,13 +410,11 @@ cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double*
                                  cudaStream_t s) {
   if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
   const size_t smem = kMaxCandidates * sizeof(unsigned long long);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(schedule_scan_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // Once per process (thread-safe initialisation of a function-local static).
+  static const cudaError_t attr_err =
+      cudaFuncSetAttribute(schedule_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (attr_err != cudaSuccess) return attr_err;
   schedule_scan_kernel<<<1, kSchedThreads, smem, s>>>(sorted, sps, R, gamma, ell, diag, status);
   return cudaGetLastError();
 }
@@ -429,13 +424,11 @@ cudaError_t launch_schedule_capacity(const unsigned long long* sorted, const dou
                                      cudaStream_t s) {
   if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
   const size_t smem = kMaxCandidates * sizeof(unsigned long long);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(schedule_capacity_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // Once per process (thread-safe initialisation of a function-local static).
+  static const cudaError_t attr_err =
+      cudaFuncSetAttribute(schedule_capacity_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (attr_err != cudaSuccess) return attr_err;
   schedule_capacity_kernel<<<1, kSchedThreads, smem, s>>>(sorted, sps, R, gamma, K, diag, status);
   return cudaGetLastError();
 }

@@ -179,3 +179,36 @@ def test_replay_is_deterministic():
         assert (a[5][k] == b[5][k]).all()
     for k in ["tokens", "n_acc", "cstar"]:
         assert np.array_equal(a[7][k], b[7][k], equal_nan=True)
+
+
+def test_target_equal_to_draft_accepts_every_token():
+    # The degenerate case p^t = p^d ([summary] §3, rejection sampling): every
+    # scheduled token is accepted (ln u < 0 = ln p^t - ln p^d) and
+    # c* = sum min(p^d, p^t) = 1.  fp32 path, fed the oracle's draft, with the
+    # target rows j <= gamma equal to the oracle's draft scores times T; the
+    # bonus row is an ordinary logit row, so the bonus draw is compared too.
+    w = TINY.resized(name="tiny_same_r64_g4_v1024", R=64, T=0.8)
+    seed = 9
+    inp = workload.generate(w, seed=seed, device="cpu")
+    W1, W2 = f64(inp["W1"]), f64(inp["W2"])
+    od = oracle.draft(f64(inp["U"]), W1, W2, inp["x0"].numpy(), w.T, seed)
+    Z = np.empty((w.R, w.gamma + 1, w.V), dtype=np.float32)
+    Z[:, : w.gamma] = (od["scores"] * w.T).astype(np.float32)
+    Z[:, w.gamma] = inp["U"][:, -1].numpy()
+    ell = np.full(w.R, w.gamma, dtype=np.int32)
+    ell[::7] = np.arange(len(ell[::7])) % (w.gamma + 1)  # some shorter prefixes
+    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], Z.astype(np.float64), ell, w.T, seed)
+    assert (ov["n_acc"] == ell).all()
+    dev = torch.device("cuda")
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    gv = dspark.dspark_verify(t(od["x"], torch.int32), t(od["logp"], torch.float32),
+                              t(od["lse"], torch.float32), t(od["scores"], torch.float32),
+                              t(Z, torch.float32), t(ell, torch.int32), w.T, seed)
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in gv.items() if isinstance(v, torch.Tensor) and k != "workspace"}
+    assert (g["n_acc"] == ell).all()
+    assert (g["n_emit"] == ell + 1).all()
+    for i in range(w.R):
+        assert np.abs(g["cstar"][i, : ell[i]] - 1.0).max(initial=0.0) < 1e-5
+        assert np.isnan(g["cstar"][i, ell[i]:]).all()
+    assert (g["tokens"] == ov["tokens"]).all()  # accepted drafts, then the bonus draw from p^t
