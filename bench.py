@@ -375,23 +375,35 @@ def oracle_sample_round(w, inp_cpu, req, seed, nthreads, scheduler="alg1", head=
     else:
         od = oracle.draft(f64(inp_cpu["U"][req]), W1, W2, x0, w.T, seed, req_ids=req, nthreads=nthreads)
     t_draft = time.perf_counter() - t0
-    # target stand-in for the sampled requests, from the oracle's own draft (untimed)
-    if w.z_bias:
-        prev = np.concatenate([x0[:, None], od["x"]], axis=1)
-        bias = oracle.markov_bias(W1, W2, prev.reshape(-1)).reshape(len(req), w.gamma + 1, w.V)
-        Z = workload.target_logits(w, inp_cpu["U"][req], seed,
-                                   bias_rows=lambda i: torch.from_numpy(bias[i]), requests=req)
-    else:
-        Z = workload.target_logits(w, inp_cpu["U"][req], seed, requests=req)
     t0 = time.perf_counter()
     conf = inp_cpu["conf"].numpy()
     if scheduler == "zos":
         ell = oracle.schedule_topk(conf, oracle.schedule_capacity(conf, inp_cpu["sps"].numpy())["K"])
     else:
         ell = oracle.schedule(conf, inp_cpu["sps"].numpy())["ell"]
-    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), ell[req], w.T, seed,
+    t_sched = time.perf_counter() - t0
+    # Target stand-in for the sampled requests, from the oracle's own draft (untimed).
+    # Verify reads rows j <= l_r + 1 only, so only those get the Markov bias (the
+    # others are never read); the bias rows are kept compact, one request at a time.
+    ls = np.asarray(ell)[req]
+    if w.z_bias:
+        prev = np.concatenate([x0[:, None], od["x"]], axis=1)  # [n, gamma + 1]
+        first = np.concatenate([[0], np.cumsum(ls + 1)])
+        rows = np.concatenate([prev[i, : ls[i] + 1] for i in range(len(req))])
+        compact = oracle.markov_bias(W1, W2, rows)
+
+        def bias_rows(i):
+            b = torch.zeros(w.gamma + 1, w.V, dtype=torch.float64)
+            b[: ls[i] + 1] = torch.from_numpy(compact[first[i]:first[i + 1]])
+            return b
+
+        Z = workload.target_logits(w, inp_cpu["U"][req], seed, bias_rows=bias_rows, requests=req)
+    else:
+        Z = workload.target_logits(w, inp_cpu["U"][req], seed, requests=req)
+    t0 = time.perf_counter()
+    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), ls, w.T, seed,
                        req_ids=req, nthreads=nthreads)
-    t_rest = time.perf_counter() - t0
+    t_rest = time.perf_counter() - t0 + t_sched
     return t_draft + t_rest, int(ov["n_emit"].sum())
 
 
@@ -403,12 +415,15 @@ def oracle_inputs(w, seed, device):
     return cpu
 
 
-def sample_size(w, inp, seed, nthreads, target_s=12.0, scheduler="alg1", head="markov"):
-    """Requests per oracle sample: about target_s seconds of work on nthreads, scaled
-    from a timed probe of one request per thread (the host's speed is not assumed)."""
+def sample_size(w, inp, seed, nthreads, target_s=20.0, scheduler="alg1", head="markov"):
+    """Requests per oracle sample: about target_s seconds of wall time on nthreads
+    (the timed round plus building its target stand-in), scaled from a probe of
+    one request per thread (the host's speed is not assumed)."""
     n0 = max(1, min(w.R, nthreads))
-    t0, _ = oracle_sample_round(w, inp, list(range(n0)), seed, nthreads, scheduler, head)
-    return int(max(1, min(w.R, round(target_s * n0 / max(t0, 1e-6)))))
+    t0 = time.perf_counter()
+    oracle_sample_round(w, inp, list(range(n0)), seed, nthreads, scheduler, head)
+    wall = time.perf_counter() - t0
+    return int(max(1, min(w.R, round(target_s * n0 / max(wall, 1e-6)))))
 
 
 def cpu_baseline(w, seed, device, nthreads):
@@ -435,7 +450,7 @@ def run_reference(args, w, rank, world):
     nthreads = os.cpu_count() or 1
     device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     inp = oracle_inputs(w, args.seed, device)
-    n = sample_size(w, inp, args.seed, nthreads, target_s=120.0 / max(1, args.steps + args.warmup),
+    n = sample_size(w, inp, args.seed, nthreads, target_s=100.0 / max(1, args.steps + args.warmup),
                     scheduler=args.scheduler, head=args.head)
     req = list(range(n))
     for _ in range(args.warmup):
