@@ -67,3 +67,36 @@ def test_rnn_draft_matches_the_oracle(w):
     mk = dspark.dspark_draft_sample(inp["U"].to(dev), inp["W1"].to(dev), inp["W2"].to(dev),
                                     inp["x0"].to(dev), w.T, seed)
     assert (mk["x"].cpu().numpy() != g["x"]).any()
+
+
+@pytest.mark.parametrize("name", ["verify_r512_g16_v151936", "qwen3_r64_g16_v151936"])
+def test_rnn_draft_full_size_sampled(name):
+    # The RNN draft at a workload's full size, in the launch configuration the
+    # benchmark times (bench.py --head rnn): the oracle recomputes a sample of
+    # requests one by one (first, middle, last and two random ones); every row's
+    # p^d is normalised and every token is in range.
+    w = W[name]
+    seed = 0
+    dev = torch.device("cuda")
+    inp = workload.generate(w, seed=seed, device=dev)
+    rin = workload.rnn_inputs(w, seed=seed, device=dev)
+    gd = dspark.dspark_draft_sample_rnn(inp["U"], inp["W1"], inp["W2"], rin["Wh"], rin["Q"], inp["x0"], w.T,
+                                        seed)
+    torch.cuda.synchronize()
+    assert dspark.dspark_read_device_status(gd["workspace"]) == 0
+    rng = np.random.default_rng(0)
+    req = sorted({0, w.R // 2, w.R - 1, *rng.integers(0, w.R, size=2).tolist()})
+    od = oracle.draft_rnn(f64(inp["U"][req]), f64(inp["W1"]), f64(inp["W2"]), f64(rin["Wh"]), f64(rin["Q"][req]),
+                          inp["x0"].cpu().numpy()[req], w.T, seed, req_ids=req, want_state=True)
+    extra = _straddle_allowance(od["h"], f64(inp["W2"]), w.T)
+    tie = np.maximum(RNN_TIE, 2 * extra.max(axis=-1))
+    take = lambda t: t[req].cpu().numpy()
+    g = {k: take(gd[k]) for k in ["x", "logp", "lse"]}
+    exempt = compare_draft(g, od, w.dtype, scores_ref=od["scores"], scores_gpu=take(gd["scores"]), tie=tie,
+                           score_extra=extra)
+    assert len(exempt) <= 1, exempt
+    x = gd["x"].cpu().numpy()
+    assert ((x >= 0) & (x < w.V)).all()
+    step = max(1, w.R // 8)
+    pd = torch.exp(gd["scores"][::step] - gd["lse"][::step, :, None]).sum(-1)
+    assert torch.allclose(pd, torch.ones_like(pd), atol=1e-4)
