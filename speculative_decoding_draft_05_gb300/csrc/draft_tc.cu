@@ -301,6 +301,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
   uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
+  // The next step may be scheduled as soon as SMs free up: its CTAs set up and
+  // prefetch W2 until their griddepcontrol.wait, which waits for this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x % p.Mt;
   const int slot = blockIdx.x / p.Mt;
@@ -434,6 +437,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY, best_s = 0.0f;
     int best_i = 0x7fffffff;
     bool ok = true;
+    // Everything below reads or writes what the previous step (launched as this
+    // grid's programmatic primary) wrote or reads: wait for its completion.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (slot == 0 && cgrp == 0 && row_ok) p.gthr_next[row] = 0u;
 
     if (lane == 0 && n_units > 0) {
@@ -889,6 +895,20 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.logp = logp;
   p.lse = lse;
   p.status = status;
+  if (k >= 2 && !A_src) {
+    // Programmatic dependent launch on the previous draft step (see the kernel).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(Mt * slots);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, draft_step_tc_kernel, maps[0], maps[1], maps[2], p);
+  }
   draft_step_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(maps[0], maps[1], maps[2], p);
   return cudaGetLastError();
 }

@@ -42,7 +42,7 @@ def test_our_arm_line():
         assert k in d, k
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
     assert d["scaling"] == "weak" and d["vs_baseline"] is None
-    assert d["config"]["workload"] == "qwen3_r64_g16_v151936" and "l2" in d["config"]
+    assert d["config"]["workload"].startswith("qwen3_r64_g16_v151936") and "l2" in d["config"]
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
