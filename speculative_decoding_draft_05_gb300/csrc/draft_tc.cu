@@ -895,8 +895,10 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.logp = logp;
   p.lse = lse;
   p.status = status;
-  if (k >= 2 && !A_src) {
-    // Programmatic dependent launch on the previous draft step (see the kernel).
+  if (k >= 2 || A_src) {
+    // Programmatic dependent launch on the previous kernel: the previous draft
+    // step, or (RNN head) the state update of this step, which itself follows
+    // the W2 transpose in stream order (see the kernel).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(Mt * slots);
     cfg.blockDim = dim3(kThreads);

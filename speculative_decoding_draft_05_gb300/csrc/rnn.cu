@@ -41,24 +41,35 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
   __shared__ int s_x[kRnnRows];
   __shared__ float s_h[kRnnRows][kRnnMaxR];
   __shared__ __align__(16) __nv_bfloat162 s_w[kRnnMaxR][kRnnCols / 2];
+  // The draft step that follows may be scheduled as SMs free up (it prefetches
+  // W2 and waits for this grid before reading A).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = blockIdx.x * kRnnRows, c0 = blockIdx.y * kRnnCols;
   constexpr int kLoads = kRnnMaxR * 8 / kRnnThreads;  // 16-byte Wh vectors (and h values) per thread
   // Every global load of the prologue is issued before the first use, so the
-  // CTA waits for one round of memory latency rather than one per load.
+  // CTA waits for one round of memory latency rather than one per load.  The
+  // inputs (Wh, Q) are read first; when this kernel is launched as the
+  // programmatic dependent of the previous draft step, the rest (the previous
+  // state and partials, which that step's grid follows) only after its wait.
   uint4 wv[kLoads];
   float hv[kLoads];
 #pragma unroll
   for (int u = 0; u < kLoads; ++u) {
     const int v = threadIdx.x + u * kRnnThreads;  // Wh[:, c0 : c0 + 64] as r rows of 8 vectors
     if (v < r * 8) wv[u] = __ldg((const uint4*)(Wh + (size_t)(v >> 3) * r + c0) + (v & 7));
-    const int i = v / r, row = row0 + i;  // previous states of the CTA's rows
-    hv[u] = (v < kRnnRows * r && k > 1 && row < R) ? h_prev[(size_t)row * r + (v - i * r)] : 0.0f;
   }
   const int row = row0 + warp;
   const int j = c0 + 2 * lane;
   float2 q = make_float2(0.0f, 0.0f);
   if (row < R) q = *(const float2*)(Q + ((size_t)row * gamma + (k - 1)) * r + j);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const int v = threadIdx.x + u * kRnnThreads;
+    const int i = v / r, hrow = row0 + i;  // previous states of the CTA's rows
+    hv[u] = (v < kRnnRows * r && k > 1 && hrow < R) ? h_prev[(size_t)hrow * r + (v - i * r)] : 0.0f;
+  }
   // The previous step's partials of this warp's row (at most 2 per lane issued at once).
   float4 ps[2];
   int pi[2];
@@ -147,10 +158,19 @@ cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const voi
                              float* logp, float* lse, int* status, cudaStream_t s) {
   if (r > kRnnMaxR || r % kRnnCols != 0) return cudaErrorInvalidValue;
   const dim3 grid((R + kRnnRows - 1) / kRnnRows, r / kRnnCols);
-  rnn_state_kernel<<<grid, kRnnThreads, 0, s>>>(
-      k, x0, (const __nv_bfloat16*)W1, (const __nv_bfloat16*)Wh, Q, prev.stats, prev.index,
-      prev.n_parts, R, gamma, V, r, h_prev, h_next, (__nv_bfloat16*)A, x, logp, lse, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kRnnThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = k >= 2 ? 1 : 0;  // step 1 follows the W2 transpose: an ordinary launch
+  return cudaLaunchKernelEx(&cfg, rnn_state_kernel, k, x0, (const __nv_bfloat16*)W1,
+                            (const __nv_bfloat16*)Wh, Q, (const float4*)prev.stats,
+                            (const int*)prev.index, prev.n_parts, R, gamma, V, r, h_prev, h_next,
+                            (__nv_bfloat16*)A, x, logp, lse, status);
 }
 
 }  // namespace dspark
