@@ -415,7 +415,7 @@ def oracle_inputs(w, seed, device):
     return cpu
 
 
-def sample_size(w, inp, seed, nthreads, target_s=20.0, scheduler="alg1", head="markov"):
+def sample_size(w, inp, seed, nthreads, target_s=28.0, scheduler="alg1", head="markov"):
     """Requests per oracle sample: about target_s seconds of wall time on nthreads
     (the timed round plus building its target stand-in), scaled from a probe of
     one request per thread (the host's speed is not assumed)."""
