@@ -605,6 +605,24 @@ def run_ours(args, w, rank, world, local):
                 "tensor": {"achieved_tflops": draft_tile_flops(w) / avg_tile_s / 1e12,
                            "peak_tflops": bf16_peak,
                            "frac": draft_tile_flops(w) / avg_tile_s / 1e12 / bf16_peak}}
+    # Ceiling for the draft step's traffic mix: a contiguous stream of one step's
+    # elements, bf16 in and fp32 out (U -> the scores buffer), timed the same way.
+    if w.dtype == "bf16":
+        n_el = w.R * w.V
+        src, dst = rnd.inp["U"].view(-1)[:n_el], rnd.scores.view(-1)[:n_el]
+        for _ in range(3):
+            dspark.dspark_stream_probe(src, dst)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record()
+        for _ in range(20):
+            dspark.dspark_stream_probe(src, dst)
+        p1.record()
+        torch.cuda.synchronize(device)
+        t_probe = p0.elapsed_time(p1) / 20 / 1e3
+        roofline["stream_probe"] = {"elements": n_el, "us": t_probe * 1e6,
+                                    "gbs": 6 * n_el / t_probe / 1e9,
+                                    "draft_step_us": avg_tile_s * 1e6,
+                                    "probe_over_draft": t_probe / avg_tile_s}
     rb = round_bytes(w, rnd.ell)
     round_roof = {"bound": "hbm", "algorithmic_bytes": rb,
                   "achieved": rb / (ms_max / args.steps / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",

@@ -356,6 +356,16 @@ enum {
 int dspark_profile_start(void);
 int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches);
 
+/* ------------------------------------------------------------------------
+ * dspark_stream_probe -- a measurement aid, not part of the path: out[i] =
+ * (float)in[i] for n bf16 values, streamed contiguously in 16-byte pieces.
+ * It moves the draft step's traffic mix (2 bytes read, 4 written per element)
+ * without the draft's access pattern, so its bandwidth is a ceiling for that
+ * mix on this GPU.  in (bf16) and out (float) are device pointers, 16-byte
+ * aligned, not overlapping; n % 8 == 0 (else DSPARK_ERR_INVALID_ARG).
+ * ---------------------------------------------------------------------- */
+int dspark_stream_probe(const void* in, float* out, size_t n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     dspark_schedule_capacity,
     dspark_schedule_topk,
     dspark_schedule_threshold,
+    dspark_stream_probe,
     dspark_sts_calibrate,
     dspark_verify,
     dspark_verify_packed,
@@ -41,6 +42,7 @@ __all__ = [
     "dspark_read_device_status",
     "dspark_profile_start",
     "dspark_profile_stop",
+    "dspark_stream_probe",
     "draft_workspace_bytes",
     "schedule_workspace_bytes",
     "verify_workspace_bytes",

@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
     L.dspark_profile_start.restype = I
     L.dspark_profile_stop.argtypes = [P, P, P]
     L.dspark_profile_stop.restype = I
+    L.dspark_stream_probe.argtypes = [P, P, SZ, P]
+    L.dspark_stream_probe.restype = I
     _lib = L
     return L
 
@@ -347,6 +349,17 @@ def dspark_read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 KERNEL_KINDS = ["prepare", "draft_tile", "draft_combine", "schedule", "verify_rows", "verify_finish",
                 "rnn_state"]
+
+
+def dspark_stream_probe(inp, out, stream=None) -> None:
+    """Bandwidth probe: out[i] = float(inp[i]) for contiguous bf16 inp and float32 out
+    (a measurement aid for the draft step's 2-byte-in / 4-byte-out traffic mix)."""
+    if inp.dtype != torch.bfloat16 or out.dtype != torch.float32 or inp.numel() != out.numel():
+        raise ValueError("stream probe: bf16 input and float32 output of the same size")
+    if not (inp.is_cuda and out.is_cuda and inp.is_contiguous() and out.is_contiguous()):
+        raise ValueError("stream probe: contiguous device tensors")
+    _check("dspark_stream_probe", load().dspark_stream_probe(inp.data_ptr(), out.data_ptr(), inp.numel(),
+                                                             _stream(stream)))
 
 
 def dspark_profile_start() -> None:

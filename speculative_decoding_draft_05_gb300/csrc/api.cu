@@ -568,6 +568,14 @@ int dspark_profile_start(void) {
   return DSPARK_OK;
 }
 
+int dspark_stream_probe(const void* in, float* out, size_t n, void* stream) {
+  if (!in || !out || n == 0 || n % 8 != 0 || !aligned16(in) || !aligned16(out))
+    return DSPARK_ERR_INVALID_ARG;
+  cudaError_t e = launch_stream_probe(in, out, n, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream_probe");
+  return DSPARK_OK;
+}
+
 int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches) {
   if (!g_prof.on) return DSPARK_ERR_INVALID_ARG;
   g_prof.on = false;

@@ -132,6 +132,9 @@ cudaError_t launch_sts_calibrate(const float* conf, const uint8_t* accept, int N
 cudaError_t launch_schedule_threshold(const float* conf, const double* temps, double theta, int R,
                                       int gamma, int32_t* ell, cudaStream_t s);
 
+// Contiguous bf16 -> fp32 stream of n values (n % 8 == 0): a bandwidth probe.
+cudaError_t launch_stream_probe(const void* in, float* out, size_t n, cudaStream_t s);
+
 // Kernel kinds for the optional event timing (dspark_profile_*).
 enum KernelKind {
   kKindPrepare = 0,  // W2 transpose (bf16) or anchor gather (fp32)

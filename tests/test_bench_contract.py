@@ -46,6 +46,8 @@ def test_our_arm_line():
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    sp = rf["stream_probe"]
+    assert sp["elements"] == 8 * 151936 and sp["gbs"] > 0 and sp["us"] > 0
     e = d["e2e"]
     assert e["value"] > 0 and e["unit"] == d["unit"] and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0

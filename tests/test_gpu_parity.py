@@ -212,3 +212,13 @@ def test_target_equal_to_draft_accepts_every_token():
         assert np.abs(g["cstar"][i, : ell[i]] - 1.0).max(initial=0.0) < 1e-5
         assert np.isnan(g["cstar"][i, ell[i]:]).all()
     assert (g["tokens"] == ov["tokens"]).all()  # accepted drafts, then the bonus draw from p^t
+
+
+def test_stream_probe_converts_exactly():
+    # The bandwidth probe bench.py times: out = float(in), every element.
+    dev = torch.device("cuda")
+    x = (torch.randn(8 * 100003, device=dev) * 3).to(torch.bfloat16)
+    y = torch.full(x.shape, float("nan"), device=dev)
+    dspark.dspark_stream_probe(x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x.float())
