@@ -117,6 +117,7 @@ constexpr int kIndexThreads = 1024;
 __global__ void __launch_bounds__(kIndexThreads)
 verify_index_kernel(const int32_t* __restrict__ ell, int R, int gamma, uint32_t* __restrict__ list,
                     int* __restrict__ count, int* __restrict__ status, ZRows zr) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the row kernel may launch
   __shared__ int warp_tot[kIndexThreads / 32];
   __shared__ int carry;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -232,6 +233,10 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
                           const int* __restrict__ count, int gamma, int V, float invT,
                           uint64_t seed, float* __restrict__ cstar, float* __restrict__ lse_t_ws,
                           int* __restrict__ acc_ws, int* __restrict__ status, ZRows zr) {
+  // Launched as a programmatic dependent of the previous kernel: wait for it
+  // before anything else, then let the next kernel's launch begin.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float rm[kRowWarps], rs[kRowWarps];
   __shared__ float s_ld;
   constexpr int kRowUnroll = row_unroll<T>();  // 64 bytes of Z per thread in flight
@@ -411,6 +416,10 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
                    float invT, const PhiloxKeys keys, const float* __restrict__ lse_t_ws,
                    const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks,
                    ZRows zr) {
+  // Launched as a programmatic dependent of the previous kernel: wait for it
+  // before anything else, then let the next kernel's launch begin.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float rk[kDrawThreads / 32];
   __shared__ int ri[kDrawThreads / 32];
   __shared__ int s_n;
@@ -568,6 +577,10 @@ verify_emit_kernel(const int32_t* __restrict__ x, const T* __restrict__ Z,
                    const float2* __restrict__ partials, int n_chunks, int32_t* __restrict__ n_acc,
                    int32_t* __restrict__ tokens, int32_t* __restrict__ n_emit,
                    float* __restrict__ cstar, float* __restrict__ lse_t_out, ZRows zr) {
+  // Launched as a programmatic dependent of the previous kernel: wait for it
+  // before anything else, then let the next kernel's launch begin.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float rk[kWarps];
   __shared__ int ri[kWarps];
   __shared__ int s_n;
@@ -639,6 +652,23 @@ int verify_sm_count() {
   return n;
 }
 
+// Launch `kernel` as a programmatic dependent of the stream's previous kernel
+// (the kernel waits for it with griddepcontrol.wait at entry).
+template <typename... Params, typename... Args>
+cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t s,
+                           Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
                                const float* scores, const void* Z, int dtype, const int32_t* ell,
                                int R, int gamma, int V, float invT, uint64_t seed, float* cstar,
@@ -651,14 +681,14 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
   const int cap = 2 * verify_sm_count();  // two CTAs of 512 threads per SM
   const int grid = (int)(rows_max < cap ? rows_max : cap);
   if (dtype == DSPARK_BF16)
-    verify_rows_stream_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, s>>>(
-        x, logp, lse, scores, (const __nv_bfloat16*)Z, row_list, row_count, gamma, V, invT, seed,
-        cstar, lse_t_ws, acc_ws, status, zr);
-  else
-    verify_rows_stream_kernel<float><<<grid, kRowThreads, 0, s>>>(
-        x, logp, lse, scores, (const float*)Z, row_list, row_count, gamma, V, invT, seed, cstar,
-        lse_t_ws, acc_ws, status, zr);
-  return cudaGetLastError();
+    return launch_chained(verify_rows_stream_kernel<__nv_bfloat16>, dim3(grid), dim3(kRowThreads), s,
+                          x, logp, lse, scores, (const __nv_bfloat16*)Z, (const uint32_t*)row_list,
+                          (const int*)row_count, gamma, V, invT, seed, cstar, lse_t_ws, acc_ws,
+                          status, zr);
+  return launch_chained(verify_rows_stream_kernel<float>, dim3(grid), dim3(kRowThreads), s, x, logp,
+                        lse, scores, (const float*)Z, (const uint32_t*)row_list,
+                        (const int*)row_count, gamma, V, invT, seed, cstar, lse_t_ws, acc_ws, status,
+                        zr);
 }
 
 int verify_draw_chunks(int V) { return ((V >> 3) + kDrawGroups - 1) / kDrawGroups; }
@@ -671,22 +701,23 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
                                  ZRows zr, cudaStream_t s) {
   const int chunks = verify_draw_chunks(V);
   dim3 grid(chunks, R);
+  cudaError_t e;
   if (dtype == DSPARK_BF16) {
-    verify_draw_kernel<__nv_bfloat16><<<grid, kDrawThreads, 0, s>>>(
-        lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
-        partials, chunks, zr);
-    verify_emit_kernel<__nv_bfloat16><<<R, kVerifyThreads, 0, s>>>(
-        x, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials, chunks,
-        n_acc, tokens, n_emit, cstar, lse_t, zr);
-  } else {
-    verify_draw_kernel<float><<<grid, kDrawThreads, 0, s>>>(lse, scores, (const float*)Z, ell, gamma,
-                                                            V, invT, philox_keys(seed), lse_t_ws,
-                                                            acc_ws, partials, chunks, zr);
-    verify_emit_kernel<float><<<R, kVerifyThreads, 0, s>>>(x, (const float*)Z, ell, gamma, V, invT,
-                                                           seed, lse_t_ws, acc_ws, partials, chunks,
-                                                           n_acc, tokens, n_emit, cstar, lse_t, zr);
+    e = launch_chained(verify_draw_kernel<__nv_bfloat16>, grid, dim3(kDrawThreads), s, lse, scores,
+                       (const __nv_bfloat16*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws,
+                       acc_ws, partials, chunks, zr);
+    if (e != cudaSuccess) return e;
+    return launch_chained(verify_emit_kernel<__nv_bfloat16>, dim3(R), dim3(kVerifyThreads), s, x,
+                          (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws,
+                          (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
   }
-  return cudaGetLastError();
+  e = launch_chained(verify_draw_kernel<float>, grid, dim3(kDrawThreads), s, lse, scores,
+                     (const float*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
+                     partials, chunks, zr);
+  if (e != cudaSuccess) return e;
+  return launch_chained(verify_emit_kernel<float>, dim3(R), dim3(kVerifyThreads), s, x,
+                        (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws,
+                        (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
 }
 
 }  // namespace dspark
