@@ -46,10 +46,6 @@ __device__ __forceinline__ unsigned long long sort_key(float a, int j, int r) {
          ((unsigned long long)(unsigned)j << 16) | (unsigned long long)(unsigned)r;
 }
 
-__device__ __forceinline__ float key_survival(unsigned long long key) {
-  return __uint_as_float(~(unsigned)(key >> 32));
-}
-
 // a * 2^48 rounded to nearest, ties to even, for a in [0, 1], in integer
 // arithmetic: a = m 2^(E - 150) with a 24-bit m (E = 0: m 2^-149).
 __device__ __forceinline__ long long fixed_survival(unsigned long long key) {
