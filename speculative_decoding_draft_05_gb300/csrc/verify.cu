@@ -216,9 +216,9 @@ template <> struct Raw8<float> {
 // CTA per row at a time (rows i = CTA, CTA + grid, ...), two CTAs of 512
 // threads per SM.  Pass 1 streams Z_j from HBM (64 bytes of Z in flight per
 // thread) into an online (max, sum exp) of Z_j / T; pass 2 streams
-// Z_j again -- from L2, which holds the rows in flight (2 per SM, 46 MB at
+// Z_j again -- from L2, which holds the rows in flight (2 per SM, 92 MB at
 // V = 151,936) -- with the draft scores (streaming loads, read once) into
-// sum_v min(p^d, p^t).  So HBM sees Z and the scores once.  The row's list
+// sum_v min(p^d, p^t).  So HBM sees Z and the scores about once.  The row's list
 // entry is loaded a row ahead and its scalars (x_j, the draft LSE, logp_j,
 // then the logit Z_j[x_j]) one pass ahead of their use.
 constexpr int kRowThreads = 512;
@@ -400,6 +400,26 @@ struct KeyedPhilox {
 constexpr int kDrawThreads = 256;
 constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 ids)
 
+// The residual row of the rejection draw, element by element.  With
+// a = z/T - LSE^t = ln p^t(v) and delta = ln p^t(v) - ln p^d(v) written as
+//   delta = (z/T - s) - (LSE^t - lse^d),
+// both differences in parentheses are single roundings of small numbers when
+// the two distributions nearly agree, so delta keeps its relative precision
+// where p^t - p^d cancels.  The residual is max(0, p^t - p^d) =
+// p^t (1 - e^-delta) for delta > 0 and zero otherwise, and its log-weight
+// a + ln(1 - e^-delta) is evaluated without the cancelling subtraction.
+// Explicitly rounded operations: the filter and the exact key see the same
+// a and delta.
+__device__ __forceinline__ void residual_terms(float z, float s, float invT, float Lt, float dL,
+                                               float& a, float& delta) {
+  a = __fmaf_rn(z, invT, -Lt);
+  delta = __fsub_rn(__fmaf_rn(z, invT, -s), dL);
+}
+
+__device__ __forceinline__ float residual_key(float a, float delta, uint32_t w) {
+  return __fadd_rn(__fadd_rn(a, logf(-expm1f(-delta))), gumbel(w));
+}
+
 // Gumbel-max over one chunk of the drawn row, with an exact-preserving filter:
 // element v can beat the running best key b only if -ln u_v < w_v exp(-b),
 // where w_v is its weight (the p^t mass for the bonus draw, the residual for
@@ -450,34 +470,49 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
     const float* srow = scores + ((size_t)r * gamma + (row - 1)) * V;
     const float ld = lse[(size_t)r * gamma + (row - 1)];
     const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+    const float dL = __fsub_rn(Lt, ld);
     for (int it = 0; it < iters; ++it) {
       const int g = g0 + it * kDrawThreads + threadIdx.x;
-      if (g < g1) {
-        float e[8], sc[8];
+      const bool have = g < g1;
+      float e[8], sc[8];
+      if (have) {
         load8(z, g, e);
         load8(srow, g, sc);
-        const uint4 w0 = rng.quad(keys, 2 * g), w1 = rng.quad(keys, 2 * g + 1);
-        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        const float thr = ord_key(*cta_best);
-        const float kb = thr == -INFINITY ? INFINITY : ex2_approx(-thr * L2E) * 1.001f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = sc[i] = 0.0f;
+      }
+      const uint4 w0 = rng.quad(keys, 2 * g), w1 = rng.quad(keys, 2 * g + 1);
+      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const float thr = ord_key(*cta_best);
+      if (have) {
+        // Candidate test, conservative for the exact key residual_key(a, delta, w):
+        //   key >= b  implies  1 - u < e^(a - b) (1 - e^-delta)  (up to roundings
+        //   far below the 0.1% slack), and 1 - e^-delta <= gb =
+        //   min(delta, 1 - ex2(-delta log2 e) + 2^-20): delta is an exact upper
+        //   bound, and 2^-20 covers the approximate ex2's absolute error on [0, 1].
+        const float nb = -thr * L2E;
         uint32_t cand = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float ra = __expf(e[i] * invT - Lt) - __expf(sc[i] - ld);  // approximate residual
+          float a, dt;
+          residual_terms(e[i], sc[i], invT, Lt, dL, a, dt);
+          const float y = ex2_approx(__fmaf_rn(a, L2E, nb));
+          const float gb = fminf(dt, __fadd_rn(__fsub_rn(1.0f, ex2_approx(-dt * L2E)),
+                                               9.5367431640625e-07f));
           const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
-          cand |= (ra > -1e-6f && om < fmaxf(ra, 1e-6f) * kb) ? (1u << i) : 0u;
+          cand |= (dt > 0.0f && om < y * gb * 1.001f) ? (1u << i) : 0u;
         }
         if (cand) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             if (!(cand & (1u << i))) continue;
-            const float res = expf(e[i] * invT - Lt) - expf(sc[i] - ld);
-            if (res > 0.0f) {
-              const float key = __fadd_rn(logf(res), gumbel(w[i]));
-              if (better(key, 8 * g + i, best, idx)) {
-                best = key;
-                idx = 8 * g + i;
-              }
+            float a, dt;  // the same explicitly rounded a and delta as the test above
+            residual_terms(e[i], sc[i], invT, Lt, dL, a, dt);
+            const float key = residual_key(a, dt, w[i]);
+            if (better(key, 8 * g + i, best, idx)) {
+              best = key;
+              idx = 8 * g + i;
             }
           }
           if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
@@ -537,8 +572,8 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
         uint32_t cand = 0;
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
-          const float2 a = __ffma2_rn(make_float2(e[i], e[i + 1]), it2, c02);
-          const float2 y = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          const float2 av = __ffma2_rn(make_float2(e[i], e[i + 1]), it2, c02);
+          const float2 y = make_float2(ex2_approx(av.x), ex2_approx(av.y));
           const float2 f = make_float2(__uint_as_float(__funnelshift_r(w[i], 0x7Fu, 9)),
                                        __uint_as_float(__funnelshift_r(w[i + 1], 0x7Fu, 9)));
           const float2 d = __ffma2_rn(y, k2, f);
