@@ -311,8 +311,11 @@ int dspark_verify_packed(const int32_t* x, const float* logp, const float* lse,
  *   problems return DSPARK_ERR_UNSUPPORTED, with the reason in
  *   dspark_last_error(), before anything is enqueued.
  * - The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and caches it; make that
- *   first call before any stream capture.
+ *   (cudaGetSymbolAddress, with that device current) and caches it together
+ *   with the id of the current context; make that first call before any
+ *   stream capture.  After cudaDeviceReset (a new primary context, where the
+ *   module may load elsewhere) the next call sees a new context id and looks
+ *   the address up again: make that call outside stream capture too.
  * - It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * - Every call shares the one array, which keeps the previous call's
  *   contents; the call clears the status word itself.  Calls whose work
@@ -332,6 +335,13 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
  * that used it) to *out after synchronising `stream`.  *out is a HOST pointer.
  * Returns DSPARK_OK, or DSPARK_ERR_CUDA if the copy failed. */
 int dspark_read_device_status(const void* workspace, void* stream, int32_t* out);
+
+/* ========================================================================
+ * Diagnostics and measurement aids.  Not part of the method and outside the
+ * draft -> schedule -> verify contract: a caller of the path needs none of
+ * them.  They exist for benchmarks and for testing the library's own error
+ * paths, and make the same ownership promises (no allocation, caller buffers).
+ * ======================================================================== */
 
 /* ------------------------------------------------------------------------
  * Optional per-kernel timing (for benchmarks; not thread-safe).
@@ -357,14 +367,34 @@ int dspark_profile_start(void);
 int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches);
 
 /* ------------------------------------------------------------------------
- * dspark_stream_probe -- a measurement aid, not part of the path: out[i] =
- * (float)in[i] for n bf16 values, streamed contiguously in 16-byte pieces.
- * It moves the draft step's traffic mix (2 bytes read, 4 written per element)
- * without the draft's access pattern, so its bandwidth is a ceiling for that
- * mix on this GPU.  in (bf16) and out (float) are device pointers, 16-byte
- * aligned, not overlapping; n % 8 == 0 (else DSPARK_ERR_INVALID_ARG).
+ * dspark_stream_probe -- a bandwidth probe: out[i] = (float)in[i] for n bf16
+ * values, streamed contiguously in 16-byte pieces.  It moves the draft step's
+ * traffic mix (2 bytes read, 4 written per element) without the draft's
+ * access pattern, so its bandwidth is a ceiling for that mix on this GPU.
+ * in (bf16) and out (float) are device pointers, 16-byte aligned, not
+ * overlapping; n % 8 == 0 (else DSPARK_ERR_INVALID_ARG).
  * ---------------------------------------------------------------------- */
 int dspark_stream_probe(const void* in, float* out, size_t n, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dspark_selftest_draft_timeout -- exercises the tensor-core draft's bounded
+ * device waits.  It enqueues draft step k = 1 of dspark_draft_sample (bf16,
+ * temperature 1, seed 0) with the W2 operand loads withheld, so that the
+ * contraction's wait for its first operand chunk can never complete, and with
+ * every device wait limited to wait_cycles SM clocks (1000 .. 4e9; the
+ * library's own limit is 4e9, about 2 s).  The kernel then gives up: the role
+ * that timed out raises the CTA's abort flag, the others see it, every copy
+ * already issued is waited for (also bounded), tensor memory is freed, and
+ * DSPARK_DEV_TIMEOUT is set in the status word of `workspace`.  The context
+ * stays usable.  Arguments, layouts and workspace as dspark_draft_sample
+ * (dtype bf16, r a multiple of 64); x, logp, lse and scores receive
+ * unspecified values.
+ * ---------------------------------------------------------------------- */
+int dspark_selftest_draft_timeout(const void* U, const void* W1, const void* W2,
+                                  const int32_t* x0, int R, int gamma, int V, int r,
+                                  long long wait_cycles, int32_t* x, float* logp, float* lse,
+                                  float* scores, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

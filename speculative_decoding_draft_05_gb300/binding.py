@@ -86,6 +86,9 @@ def load() -> ctypes.CDLL:
     L.dspark_profile_stop.restype = I
     L.dspark_stream_probe.argtypes = [P, P, SZ, P]
     L.dspark_stream_probe.restype = I
+    L.dspark_selftest_draft_timeout.argtypes = [P, P, P, P, I, I, I, I, ctypes.c_longlong, P, P, P, P,
+                                                P, SZ, P]
+    L.dspark_selftest_draft_timeout.restype = I
     _lib = L
     return L
 
@@ -377,3 +380,27 @@ def dspark_profile_stop() -> dict:
     out = {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}
     out["_timed_launches"] = int(timed.value)
     return out
+
+
+def dspark_selftest_draft_timeout(U, W1, W2, x0, wait_cycles: int, *, workspace=None,
+                                  stream=None) -> torch.Tensor:
+    """Diagnostic: the tensor-core draft's step 1 with its W2 loads withheld and
+    every device wait limited to ``wait_cycles`` SM clocks, so that the bounded
+    waits run out.  Returns the workspace (its status word then carries
+    DEV_TIMEOUT; read it with dspark_read_device_status)."""
+    L = load()
+    R, g, V = U.shape
+    r = W1.shape[1]
+    dev = U.device
+    x = torch.empty(R, g, dtype=torch.int32, device=dev)
+    logp = torch.empty(R, g, dtype=torch.float32, device=dev)
+    lse = torch.empty(R, g, dtype=torch.float32, device=dev)
+    scores = torch.empty(R, g, V, dtype=torch.float32, device=dev)
+    ws = _workspace(draft_workspace_bytes(R, g, V, r, torch.bfloat16), dev, workspace)
+    st = L.dspark_selftest_draft_timeout(
+        _dev(U, "U", torch.bfloat16, (R, g, V)), _dev(W1, "W1", torch.bfloat16, (V, r)),
+        _dev(W2, "W2", torch.bfloat16, (r, V)), _dev(x0, "x0", torch.int32, (R,)), R, g, V, r,
+        int(wait_cycles), x.data_ptr(), logp.data_ptr(), lse.data_ptr(), scores.data_ptr(),
+        ws.data_ptr(), ws.numel(), _stream(stream))
+    _check("dspark_selftest_draft_timeout", st)
+    return ws

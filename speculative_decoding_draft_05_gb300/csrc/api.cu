@@ -1,5 +1,6 @@
 // api.cu -- the C-ABI of libdspark.so (declared in include/dspark.h): argument
 // checks, workspace layout, and the launch sequence of each call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdio.h>
@@ -504,7 +505,39 @@ int dspark_read_device_status(const void* workspace, void* stream, int32_t* out)
 // cudaGetSymbolAddress returns for the current device.
 static __device__ __align__(256) unsigned char g_verify_noalloc_scratch[DSPARK_VERIFY_NOALLOC_SCRATCH_BYTES];
 static std::mutex g_noalloc_mu;
+// Per device: the address and the id of the context it was looked up in.  A
+// cudaDeviceReset ends the primary context; the next one loads the module
+// again, possibly elsewhere, so the address is looked up again when the
+// current context's id differs.
 static void* g_noalloc_addr[64] = {};
+static unsigned long long g_noalloc_ctx[64] = {};
+
+typedef CUresult (*PFN_ctx_get_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long*);
+
+// Id of the current context (0 if the driver cannot tell): two driver calls,
+// no synchronisation, allowed during stream capture.
+static unsigned long long current_ctx_id() {
+  static PFN_ctx_get_current get_current = nullptr;
+  static PFN_ctx_get_id get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = (PFN_ctx_get_current)f;
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = (PFN_ctx_get_id)f;
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 static int noalloc_scratch(void** out) {
   int dev = 0;
@@ -514,12 +547,16 @@ static int noalloc_scratch(void** out) {
     snprintf(g_last_error, sizeof(g_last_error), "dspark_verify_noalloc: device %d not supported", dev);
     return DSPARK_ERR_UNSUPPORTED;
   }
+  // Before the device's first runtime call there is no current context (id
+  // 0): the lookup creates it, and its id is recorded afterwards.
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
+  const unsigned long long ctx = current_ctx_id();
+  if (!g_noalloc_addr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_verify_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "verify_noalloc scratch address");
     g_noalloc_addr[dev] = p;
+    g_noalloc_ctx[dev] = ctx != 0 ? ctx : current_ctx_id();
   }
   *out = g_noalloc_addr[dev];
   return DSPARK_OK;
@@ -552,6 +589,40 @@ int dspark_verify_noalloc(const int32_t* x, const float* logp, const float* lse,
   return verify_enqueue(x, logp, lse, scores, Z, dtype, ell, R, gamma, V, temperature, seed, n_acc,
                         tokens, n_emit, cstar, lse_t, scratch, ZRows{nullptr, gamma, 0},
                         (cudaStream_t)stream, "verify_noalloc");
+}
+
+int dspark_selftest_draft_timeout(const void* U, const void* W1, const void* W2,
+                                  const int32_t* x0, int R, int gamma, int V, int r,
+                                  long long wait_cycles, int32_t* x, float* logp, float* lse,
+                                  float* scores, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!U || !W1 || !W2 || !x0 || !x || !logp || !lse || !scores) return DSPARK_ERR_INVALID_ARG;
+  if (wait_cycles < 1000 || wait_cycles > 4000000000ll) return DSPARK_ERR_INVALID_ARG;
+  int st = check_common(R, gamma, V, 1.0f, DSPARK_BF16);
+  if (st != DSPARK_OK) return st;
+  if (!aligned16(U) || !aligned16(W1) || !aligned16(W2) || !aligned16(scores))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!draft_tc_supported(R, V, r)) return DSPARK_ERR_UNSUPPORTED;
+  const DraftWorkspace L = draft_workspace_layout(R, gamma, V, r, DSPARK_BF16);
+  if (!workspace || workspace_bytes < L.total || ((uintptr_t)workspace & 255u))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  char* ws = (char*)workspace;
+  int* status = (int*)(ws + L.status);
+  const int n_parts = draft_tc_parts(R, V);
+  DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index), n_parts};
+  DraftPartials p2{(float4*)(ws + L.stats2), (int*)(ws + L.index2), n_parts};
+  uint32_t* gthr = (uint32_t*)(ws + L.gthr);
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(gthr, 0, 2 * (size_t)R * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest reset");
+  DraftTcPlan plan;
+  e = prepare_draft_tc(&plan, U, ws + L.w2t, R, gamma, V, r, scores);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest tensor maps");
+  e = launch_draft_step_tc(plan, 1, 1.0f, 0, x0, W1, p2, p, gthr, x, logp, lse, status, s, nullptr,
+                           wait_cycles, true);
+  if (e != cudaSuccess) return cuda_fail(e, "selftest draft_step");
+  return DSPARK_OK;
 }
 
 int dspark_profile_start(void) {

@@ -221,6 +221,15 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+
+// Bit k of the candidate mask for d = fl(f + kf e) >= 1: d >= 2 exactly when
+// bit 30, the top bit of the exponent, is set (d is never negative).  k is a
+// constant after unrolling, so this is a shift and an and-or.
+__device__ __forceinline__ uint32_t cand_bit(float d, int k) {
+  const uint32_t b = __float_as_uint(d);
+  return k <= 30 ? (b >> (30 - k)) & (1u << k) : (b << 1) & 0x80000000u;
+}
+
 // Pass 1 of the draft epilogue over one warp's 32 columns of a row, branch-free:
 // returns the candidate mask and sets st = sum exp(s - mx).  Element i can beat
 // the running best key b only if 1 - u_i < y_i = exp(s_i - b); with
@@ -229,8 +238,9 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 // one rounding of the same inequality, and it admits every element that
 // f_i >= fl(2 - 1.001 y_i) admits).  The arithmetic runs on float pairs
 // (one packed FMA or add for two elements).  The scores are read back from the
-// row's staged block (128-byte swizzle), one 16-byte quad at a time.  MASKED:
-// only the first nvalid columns take part.
+// row's staged block (128-byte swizzle), one 16-byte quad at a time; the
+// eight quads are unrolled so that every mask bit and address is a constant
+// offset.  MASKED: only the first nvalid columns take part.
 template <bool MASKED>
 __device__ __forceinline__ uint32_t filter_pass(const uint8_t* srow, int lane,
                                                 const PhiloxStream& rng, int col0, float mxl,
@@ -239,10 +249,12 @@ __device__ __forceinline__ uint32_t filter_pass(const uint8_t* srow, int lane,
   const float2 l2e = make_float2(L2E, L2E), nmx = make_float2(-mxl, -mxl), k2 = make_float2(kf, kf);
   float2 sum01 = make_float2(0.0f, 0.0f), sum23 = make_float2(0.0f, 0.0f);
   uint32_t cand = 0;
-#pragma unroll 2
+  const uint32_t sw = (uint32_t)(lane & 7) << 4;  // the row's 128-byte swizzle
+  const uint32_t q0 = (uint32_t)col0 >> 2;
+#pragma unroll
   for (int q4 = 0; q4 < 8; ++q4) {
-    const float4 sv = *(const float4*)(srow + ((q4 ^ (lane & 7)) << 4));
-    const uint4 w4 = rng.quad((uint32_t)((col0 >> 2) + q4));
+    const float4 sv = *(const float4*)(srow + (((uint32_t)q4 << 4) ^ sw));
+    const uint4 w4 = rng.quad(q0 + (uint32_t)q4);
     const float2 a01 = __ffma2_rn(make_float2(sv.x, sv.y), l2e, nmx);
     const float2 a23 = __ffma2_rn(make_float2(sv.z, sv.w), l2e, nmx);
     float e[4] = {ex2_approx(a01.x), ex2_approx(a01.y), ex2_approx(a23.x), ex2_approx(a23.y)};
@@ -256,10 +268,8 @@ __device__ __forceinline__ uint32_t filter_pass(const uint8_t* srow, int lane,
     const float2 d23 = __ffma2_rn(e23, k2, make_float2(unit_float(w4.z), unit_float(w4.w)));
     sum01 = __fadd2_rn(sum01, e01);
     sum23 = __fadd2_rn(sum23, e23);
-    cand |= d01.x >= 2.0f ? 1u << (4 * q4) : 0u;
-    cand |= d01.y >= 2.0f ? 1u << (4 * q4 + 1) : 0u;
-    cand |= d23.x >= 2.0f ? 1u << (4 * q4 + 2) : 0u;
-    cand |= d23.y >= 2.0f ? 1u << (4 * q4 + 3) : 0u;
+    cand |= cand_bit(d01.x, 4 * q4) | cand_bit(d01.y, 4 * q4 + 1) | cand_bit(d23.x, 4 * q4 + 2) |
+            cand_bit(d23.y, 4 * q4 + 3);
   }
   st = (sum01.x + sum01.y) + (sum23.x + sum23.y);
   return cand;
@@ -282,6 +292,8 @@ struct Params {
   float* logp;
   float* lse;
   int* status;
+  long long wait_budget;  // SM clocks each bounded wait may take
+  int withhold_w2;        // diagnostic: the producer issues no W2 loads, so the waits run out
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -337,7 +349,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_units > 0) {
+    if (lane == 0 && n_units > 0 && !p.withhold_w2) {
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -345,7 +357,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       for (int u = 0; u < n_units && ok; ++u) {
         const int n = slot + u * p.slots;
         for (int c = 0; c < n_chunks; ++c) {
-          if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag)) {
+          if (!mbar_wait(&bar_empty[stage], phase ^ 1u, abort_flag, p.wait_budget)) {
             ok = false;
             break;
           }
@@ -366,9 +378,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         for (int i = 0; i < kStages && i < issued; ++i) {
           s = (s + kStages - 1) % kStages;
           if (s == kStages - 1) ph ^= 1;
-          const long long t1 = clock64();
-          while (!mbar_try_wait(&bar_full[s], ph) && clock64() - t1 < kWaitBudget) {
-          }
+          mbar_drain(&bar_full[s], ph, p.wait_budget);
         }
       }
     }
@@ -378,19 +388,19 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       const uint32_t idesc = make_idesc(kTileM, kTileN);
       int stage = 0;
       uint32_t phase = 0;
-      bool ok = mbar_wait(bar_a, 0, abort_flag);
+      bool ok = mbar_wait(bar_a, 0, abort_flag, p.wait_budget);
       tc_fence_after();
       for (int u = 0; u < n_units && ok; ++u) {
         const int buf = u & 1;
         const uint32_t acc_phase = (u >> 1) & 1;
-        if (!mbar_wait(&bar_acc_empty[buf], acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait(&bar_acc_empty[buf], acc_phase ^ 1u, abort_flag, p.wait_budget)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
         for (int c = 0; c < n_chunks; ++c) {
-          if (!mbar_wait(&bar_full[stage], phase, abort_flag)) {
+          if (!mbar_wait(&bar_full[stage], phase, abort_flag, p.wait_budget)) {
             ok = false;
             break;
           }
@@ -416,9 +426,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       }
       // All MMAs done before TMEM is freed.
       tc_commit(bar_drain);
-      const long long t0 = clock64();
-      while (!mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitBudget) {
-      }
+      mbar_drain(bar_drain, 0, p.wait_budget);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -436,7 +444,6 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     const PhiloxStream rng(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT);
     float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY, best_s = 0.0f;
     int best_i = 0x7fffffff;
-    bool ok = true;
     // Everything below reads or writes what the previous step (launched as this
     // grid's programmatic primary) wrote or reads: wait for its completion.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -446,6 +453,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       mbar_expect_tx(&bar_u[warp], kUBoxBytes);
       tma_load_3d(ubox, &tmU, slot * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
     }
+    // U loads of this warp issued so far and those waited for (equal on exit
+    // unless a wait failed: the one in flight must land before the CTA exits).
+    int u_issued = n_units > 0 ? 1 : 0, u_landed = 0;
     // A tile: rows m_tile*128 + 8 warp .. +7 get W1[x_{k-1}], written straight into
     // the K-major 128-byte-swizzled layout the MMA reads (zero rows past R).
     // x_{k-1} is the anchor for k = 1, else the combine of step k-1's partials;
@@ -551,7 +561,11 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       const uint32_t gkey = row_ok ? __ldcg(p.gthr_cur + row) : 0u;
 
       // U block of this warp: row `lane`, 32 bf16 (64-byte rows, 64-byte swizzle).
-      ok = ok && mbar_wait(&bar_u[warp], u & 1, abort_flag);
+      // Waits are decided warp-wide; on a failed one the warp leaves the loop
+      // (every epilogue warp still reaches the merge barrier below).
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_u[warp], u & 1, abort_flag, p.wait_budget)))
+        break;
+      u_landed = u + 1;
       uint32_t upk[16];
       {
         const uint32_t* rowp = (const uint32_t*)(ubox + lane * 64);
@@ -566,14 +580,18 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         }
       }
       __syncwarp();
-      if (lane == 0 && u + 1 < n_units && ok) {
-        fence_proxy_async();
-        mbar_expect_tx(&bar_u[warp], kUBoxBytes);
-        tma_load_3d(ubox, &tmU, (n + p.slots) * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
+      if (u + 1 < n_units) {
+        if (lane == 0) {
+          fence_proxy_async();
+          mbar_expect_tx(&bar_u[warp], kUBoxBytes);
+          tma_load_3d(ubox, &tmU, (n + p.slots) * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
+        }
+        u_issued = u + 2;
       }
 
       // Accumulator columns of this warp.
-      ok = ok && mbar_wait(&bar_acc_full[buf], acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_acc_full[buf], acc_phase, abort_flag, p.wait_budget)))
+        break;
       tc_fence_after();
       uint32_t acc[32];
       tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kTileN + cgrp * 32),
@@ -706,7 +724,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       p.pstats[o] = make_float4(m, S, bk, bs);
       p.pindex[o] = bi;
     }
-    if (lane == 0) bulk_wait0();
+    if (lane == 0) {
+      if (u_issued > u_landed) mbar_drain(&bar_u[warp], (uint32_t)(u_issued - 1) & 1u, p.wait_budget);
+      bulk_wait0();
+    }
   }
 
   tc_fence_before();
@@ -865,7 +886,8 @@ cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStr
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
                                  const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s, const void* A_src) {
+                                 float* lse, int* status, cudaStream_t s, const void* A_src,
+                                 long long wait_budget, bool withhold_w2) {
   const int Mt = (plan.R + kTileM - 1) / kTileM;
   const int n_tiles = (plan.V + kTileN - 1) / kTileN;
   const int slots = draft_tc_parts(plan.R, plan.V);
@@ -895,6 +917,8 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.logp = logp;
   p.lse = lse;
   p.status = status;
+  p.wait_budget = wait_budget > 0 ? wait_budget : kWaitBudget;
+  p.withhold_w2 = withhold_w2 ? 1 : 0;
   if (k >= 2 || A_src) {
     // Programmatic dependent launch on the previous kernel: the previous draft
     // step, or (RNN head) the state update of this step, which itself follows

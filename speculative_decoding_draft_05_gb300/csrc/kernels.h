@@ -52,7 +52,8 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
                                  const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
                                  float* lse, int* status, cudaStream_t s,
-                                 const void* A_src = nullptr);
+                                 const void* A_src = nullptr, long long wait_budget = 0,
+                                 bool withhold_w2 = false);
 // RNN head, step k: x_{k-1} (anchor for k = 1, else the merge of `prev`, whose
 // x/logp/lse it also stores), h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k) from
 // h_prev into h_next ([R, r] fp32 each; h_prev unread for k = 1), and

@@ -6,7 +6,7 @@
 
 namespace dspark {
 
-constexpr long long kWaitBudget = 4000000000ll;  // SM clocks (~2 s) for every bounded wait
+constexpr long long kWaitBudget = 4000000000ll;  // SM clocks (~2 s): the default bounded-wait limit
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -39,19 +39,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `parity` to complete.  Returns false (and
-// raises the CTA's abort flag) if the budget runs out or another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// raises the CTA's abort flag) if `budget` SM clocks pass or another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          long long budget) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitBudget) {
+      if (clock64() - t0 > budget) {
         *abort_flag = 1;
         return false;
       }
     }
+  }
+}
+
+// Bounded wait without the abort flag, for draining copies already in flight.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < budget) {
   }
 }
 
