@@ -258,10 +258,11 @@ class Round:
             del self.Z
             torch.cuda.synchronize(device)
 
-    def _target_logits(self):
+    def _target_logits(self, seed=None, out=None):
         w, inp = self.w, self.inp
+        seed = self.seed if seed is None else seed
         if not w.z_bias:
-            return workload.target_logits(w, inp["U"], self.seed)
+            return workload.target_logits(w, inp["U"], seed, out=out)
         W1f = inp["W1"].float()
         W2f = inp["W2"].float()
         x0, x = inp["x0"], self.x
@@ -270,7 +271,20 @@ class Round:
             prev = torch.cat([x0[i:i + 1].long(), x[i].long()])
             return W1f[prev] @ W2f
 
-        return workload.target_logits(w, inp["U"], self.seed, bias_rows=bias_rows)
+        return workload.target_logits(w, inp["U"], seed, bias_rows=bias_rows, out=out)
+
+    def reseed(self, seed: int):
+        """New round inputs for `seed` (untimed): U, x0 and c drawn from that seed,
+        the draft head's weights kept, and the target stand-in rebuilt along the
+        draft's tokens under that seed's Philox key.  Buffers are reused."""
+        new = workload.generate(self.w, seed=seed, device=self.device, weights_seed=self.seed)
+        for k in ("U", "x0", "conf"):
+            self.inp[k].copy_(new[k])
+        del new
+        self.draft(seed)
+        torch.cuda.synchronize(self.device)
+        self._target_logits(seed, out=self.Z)
+        torch.cuda.synchronize(self.device)
 
     def draft(self, seed=None, U=None, W1=None, W2=None, x0=None, Wh=None, Q=None):
         i = self.inp
@@ -357,6 +371,46 @@ def round_bytes(w: workload.Workload, ell) -> int:
 
 def draft_tile_flops(w: workload.Workload) -> int:
     return 2 * w.R * w.r * w.V
+
+
+def verify_rows_bytes(w: workload.Workload, rows: int) -> int:
+    """Algorithmic bytes of the verify row kernel over `rows` scheduled rows: each
+    row's target logits once from HBM (its second pass hits L2) and its draft
+    scores once."""
+    e = 4 if w.dtype == "f32" else 2
+    return rows * w.V * (e + 4)
+
+
+def verify_draw_bytes(w: workload.Workload, residual_rows: int) -> int:
+    """Algorithmic bytes of the draw (+ emit): one target row per request, plus the
+    draft scores of the rows drawn from a residual."""
+    e = 4 if w.dtype == "f32" else 2
+    return w.R * w.V * e + residual_rows * w.V * 4
+
+
+def kernel_rooflines(w, prof, rows_per_round: int, residual_per_round: float, hbm_peak: float,
+                     rnn: bool):
+    """Per-kernel algorithmic bytes per launch / event-timed launch / measured HBM
+    peak, for the verify kernels and (RNN head) the state update."""
+    out = {}
+
+    def entry(kind, nbytes, extra):
+        ms, n = prof.get(kind, (0.0, 0))
+        if n <= 0 or ms <= 0:
+            return
+        t = ms / n / 1e3
+        out[kind] = dict(extra, bytes_per_launch=int(nbytes), us_per_launch=t * 1e6,
+                         achieved_gbs=nbytes / t / 1e9, frac=nbytes / t / 1e9 / hbm_peak, bound="hbm")
+
+    entry("verify_rows", verify_rows_bytes(w, rows_per_round), {"rows": rows_per_round})
+    entry("verify_finish", verify_draw_bytes(w, residual_per_round),
+          {"residual_rows": residual_per_round, "bonus_rows": w.R - residual_per_round})
+    if rnn:
+        # h_{k-1} read, h_k written (fp32), the A rows written (bf16), Wh, Q_k
+        e = 2
+        nbytes = w.R * w.r * (4 + 4 + e + 4) + w.r * w.r * e
+        entry("rnn_state", nbytes, {"note": "latency/instruction-bound: 2 R r^2 FLOP per step"})
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -479,6 +533,67 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_seeds(args, w, rank, world, local):
+    """Rounds with seeds 0..N-1, each on its own inputs (U, x0, c and the target
+    stand-in regenerated untimed on the device; the draft head's weights from
+    seed 0), one round timed per seed with CUDA events.  Reports summed
+    positions over summed round time, and accepted tokens/s (emitted tokens,
+    the bonus or correction token included, over the same time)."""
+    import speculative_decoding_draft_05_gb300 as dspark
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("no CUDA device: the library has no CPU path")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    dspark.binding.load()
+    stream = torch.cuda.current_stream(device)
+    rnd = Round(w, 0, device, scheduler=args.scheduler, verify_layout="padded", head=args.head)
+    for i in range(args.warmup):
+        rnd.step(0)
+    torch.cuda.synchronize(device)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per_seed = []
+    emitted = 0
+    with ClockSampler(local) as clocks:
+        for sd in range(args.seeds):
+            if sd > 0:
+                rnd.reseed(sd)
+            barrier(world)
+            torch.cuda.synchronize(device)
+            ev0.record(stream)
+            rnd.step(sd)
+            ev1.record(stream)
+            torch.cuda.synchronize(device)
+            per_seed.append(ev0.elapsed_time(ev1))
+            emitted += int(rnd.n_emit.sum().item())
+            for ws in (rnd.ws_d, rnd.ws_s, rnd.ws_v):
+                assert dspark.dspark_read_device_status(ws) == 0, f"device status at seed {sd}"
+    ms = max_over_ranks(sum(per_seed), world, device)
+    positions = w.R * w.gamma * len(per_seed) * world
+    value = positions / (ms / 1e3)
+    accepted = sum_over_ranks(float(emitted), world, device) / (ms / 1e3)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world,
+                "steps": len(per_seed), "warmup": args.warmup, "ms_per_step": ms / len(per_seed),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+                "mode": f"seeds 0..{len(per_seed) - 1}, one round each on its own inputs",
+                "config": dict(workload.describe(w), seeds=len(per_seed), scheduler=args.scheduler,
+                               head=args.head, weights_seed=0,
+                               l2="inputs larger than L2 (regenerated between rounds)"),
+                "accepted_tokens_per_s": accepted, "emitted_tokens": emitted,
+                "ms_per_round": {"min": min(per_seed), "median": statistics.median(per_seed),
+                                 "max": max(per_seed)},
+                "clocks": clocks.summary()}
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def run_ours(args, w, rank, world, local):
     import speculative_decoding_draft_05_gb300 as dspark
 
@@ -526,9 +641,11 @@ def run_ours(args, w, rank, world, local):
     value = positions / (ms_max / 1e3)
     # tokens emitted by those rounds (deterministic: replay the same seeds, untimed)
     emitted = 0
+    residual_rows = 0
     for sd in seeds:
         rnd.step(sd)
         emitted += int(rnd.n_emit.sum().item())
+        residual_rows += int((rnd.n_acc < rnd.ell).sum().item())
     accepted = sum_over_ranks(float(emitted), world, device) / (ms_max / 1e3)
 
     # ---- e2e through the C-ABI with pinned host buffers: every step copies its
@@ -623,6 +740,32 @@ def run_ours(args, w, rank, world, local):
                                     "gbs": 6 * n_el / t_probe / 1e9,
                                     "draft_step_us": avg_tile_s * 1e6,
                                     "probe_over_draft": t_probe / avg_tile_s}
+    k_roof = kernel_rooflines(w, prof, int(rnd.ell.sum().item()), residual_rows / len(seeds), hbm_peak,
+                              args.head == "rnn")
+    # Full-block verify over this round's own buffers, outside the timed regions:
+    # the first (up to) 64 requests with l = gamma, so that the row kernel streams
+    # every position even where the workload's schedule keeps nothing.
+    vprobe = None
+    if not rnd.packed:
+        n = min(64, w.R)
+        ell_full = torch.full((n,), w.gamma, dtype=torch.int32, device=device)
+        vo = dict(n_acc=torch.empty_like(rnd.n_acc[:n]), tokens=torch.empty_like(rnd.tokens[:n]),
+                  n_emit=torch.empty_like(rnd.n_emit[:n]), cstar=torch.empty_like(rnd.cstar[:n]),
+                  lse_t=torch.empty_like(rnd.lse_t[:n]), workspace=rnd.ws_v)
+        args_v = (rnd.x[:n], rnd.logp[:n], rnd.lse[:n], rnd.scores[:n], rnd.Z[:n], ell_full, w.T, args.seed)
+        for _ in range(2):
+            dspark.dspark_verify(*args_v, **vo)
+        torch.cuda.synchronize(device)
+        dspark.dspark_profile_start()
+        for _ in range(5):
+            dspark.dspark_verify(*args_v, **vo)
+        vp = dspark.dspark_profile_stop()
+        ms_r, n_r = vp["verify_rows"]
+        t_r = ms_r / max(1, n_r) / 1e3
+        nb = verify_rows_bytes(w, n * w.gamma)
+        vprobe = {"requests": n, "rows": n * w.gamma, "bytes_per_launch": nb, "us_per_launch": t_r * 1e6,
+                  "achieved_gbs": nb / t_r / 1e9, "frac": nb / t_r / 1e9 / hbm_peak, "peak": hbm_peak,
+                  "note": "extra call outside the timed regions; not part of value"}
     rb = round_bytes(w, rnd.ell)
     round_roof = {"bound": "hbm", "algorithmic_bytes": rb,
                   "achieved": rb / (ms_max / args.steps / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
@@ -648,7 +791,8 @@ def run_ours(args, w, rank, world, local):
                                    w.R * w.gamma * w.V * (2 if w.dtype == "bf16" else 4) / 1e9,
                                    w.R * w.gamma * w.V * 4 / 1e9,
                                    rnd.input_tensors()[6].numel() * rnd.input_tensors()[6].element_size() / 1e9)),
-                "roofline": roofline, "round_roofline": round_roof, "cpu_baseline": out,
+                "roofline": roofline, "round_roofline": round_roof, "kernels_roofline": k_roof,
+                "verify_rows_probe": vprobe, "cpu_baseline": out,
                 "e2e": {"value": e2e_value, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "steps": e2e_steps},
                 "gpu_launches": launches, "clocks": clocks.summary(),
@@ -679,6 +823,9 @@ def main(argv=None):
                     help="target logits padded [R, gamma+1, V] (default) or packed rows + offsets")
     ap.add_argument("--R", type=int, default=None, help="override the workload's request count")
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
+    ap.add_argument("--seeds", type=int, default=0,
+                    help="N > 0: N rounds with seeds 0..N-1, each on its own regenerated inputs "
+                         "(the serving workload's 100-seed report)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -689,6 +836,9 @@ def main(argv=None):
         w = w.resized(**over)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
+        return
+    if args.seeds > 0:
+        run_seeds(args, w, rank, world, local)
         return
     run_ours(args, w, rank, world, local)
 

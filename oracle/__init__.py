@@ -23,7 +23,8 @@ Function-level citations are in the C file; the summary:
 * ``verify``    -- standard rejection sampling (DSpark summary, opening bullets
                    and §3), soft label c* (DSpark summary §3.2.1).
 
-Parity status of each function and its pins are listed in the design doc.
+Each function's pins (closed forms, brute force, golden values, planted mistakes)
+are the tests/test_oracle_*.py files.
 """
 from __future__ import annotations
 

@@ -174,13 +174,18 @@ def rnn_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tens
     return dict(Wh=Wh.contiguous(), Q=Q.contiguous())
 
 
-def generate(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
-    """U, W1, W2, x0, conf, sps for workload ``w`` (dtype ``w.torch_dtype`` for U/W1/W2)."""
+def generate(w: Workload, seed: int = 0, device="cpu",
+             weights_seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """U, W1, W2, x0, conf, sps for workload ``w`` (dtype ``w.torch_dtype`` for U/W1/W2).
+
+    The draft head's weights W1, W2 come from ``weights_seed`` when it is given
+    (a serving run keeps one head while every round draws new U, x0 and c),
+    else from ``seed``."""
     dt = w.torch_dtype
     U = torch.empty(w.R, w.gamma, w.V, dtype=dt, device=device)
     for r in range(w.R):
         U[r] = _draw_logit_rows(w, w.gamma, _gen(device, seed, "U", r), device).to(dt)
-    gw = _gen(device, seed, "W")
+    gw = _gen(device, seed if weights_seed is None else weights_seed, "W")
     W1 = (torch.randn(w.V, w.r, generator=gw, device=device) * w.w_std).to(dt).contiguous()
     W2 = (torch.randn(w.r, w.V, generator=gw, device=device) * w.w_std).to(dt).contiguous()
     x0 = torch.randint(0, w.V, (w.R,), generator=_gen(device, seed, "x0"), device=device,

@@ -52,3 +52,20 @@ def test_our_arm_line():
     assert e["value"] > 0 and e["unit"] == d["unit"] and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    kr = d["kernels_roofline"]
+    for k in ("verify_rows", "verify_finish"):  # full blocks at this workload: both run
+        assert kr[k]["bytes_per_launch"] > 0 and kr[k]["us_per_launch"] > 0
+        assert abs(kr[k]["frac"] - kr[k]["achieved_gbs"] / rf["peak"]) < 1e-9
+    assert kr["verify_rows"]["rows"] == 8 * 4
+    vp = d["verify_rows_probe"]
+    assert vp["requests"] == 8 and vp["rows"] == 32 and vp["bytes_per_launch"] == 32 * 151936 * 6
+    assert vp["us_per_launch"] > 0 and vp["frac"] > 0
+
+
+@pytest.mark.gpu
+def test_seeds_mode_line():
+    # The serving report: rounds with seeds 0..N-1, each on its own inputs.
+    d = _run(["--workload", "serving_r1024_g16_v129280", "--R", "16", "--seeds", "3", "--warmup", "3"], 600)
+    assert d["steps"] == 3 and d["config"]["seeds"] == 3 and d["value"] > 0
+    assert d["accepted_tokens_per_s"] > 0 and 3 * 16 <= d["emitted_tokens"] <= 3 * 16 * 17
+    assert d["ms_per_round"]["min"] <= d["ms_per_step"] <= d["ms_per_round"]["max"] + 1e-9

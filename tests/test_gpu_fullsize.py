@@ -24,14 +24,12 @@ def sampled_requests(R, n_random=2, seed=0):
     return sorted(s)
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_round_sampled(name):
-    w = workload.WORKLOADS[name]
-    seed = 0
+def round_sampled(w, seed, req, weights_seed=None):
+    """One full-size round on the GPU; the oracle recomputes requests `req` and the
+    whole schedule.  Returns what the comparisons need."""
     dev = torch.device("cuda")
-    inp = workload.generate(w, seed=seed, device=dev)
+    inp = workload.generate(w, seed=seed, device=dev, weights_seed=weights_seed)
     gd = dspark.dspark_draft_sample(inp["U"], inp["W1"], inp["W2"], inp["x0"], w.T, seed)
-    req = sampled_requests(w.R)
     W1, W2 = f64(inp["W1"]), f64(inp["W2"])
     x0 = inp["x0"].cpu().numpy()
     od = oracle.draft(f64(inp["U"][req]), W1, W2, x0[req], w.T, seed, req_ids=req)
@@ -62,8 +60,11 @@ def test_full_size_round_sampled(name):
     assert len(exempt) <= 1
     gvs = {k: take(gv[k]) for k in ["n_acc", "tokens", "n_emit", "cstar", "lse_t"]}
     compare_verify(gvs, ov, osch["ell"][req], w.dtype, skip=exempt)
+    return inp, gd, gs, gv, ell
 
-    # every request: output structure
+
+def check_structure(w, gd, gv, ell):
+    """Properties that hold on every request at any size."""
     x = gd["x"].cpu().numpy()
     tok = gv["tokens"].cpu().numpy()
     n = gv["n_acc"].cpu().numpy()
@@ -74,6 +75,27 @@ def test_full_size_round_sampled(name):
         assert (tok[i, :n[i]] == x[i, :n[i]]).all()
         assert 0 <= tok[i, n[i]] < w.V
         assert (tok[i, n[i] + 1:] == -1).all()
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_round_sampled(name):
+    w = workload.WORKLOADS[name]
+    inp, gd, gs, gv, ell = round_sampled(w, 0, sampled_requests(w.R))
+    check_structure(w, gd, gv, ell)
     # p^d is normalised on every row (sampled rows of the scores tensor)
     pd = torch.exp(gd["scores"][:: max(1, w.R // 8)] - gd["lse"][:: max(1, w.R // 8), :, None]).sum(-1)
     assert torch.allclose(pd, torch.ones_like(pd), atol=1e-4)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_serving_round_per_seed(seed):
+    # The serving workload's report runs 100 rounds with seeds 0..99, each on
+    # its own U, x0, c and target logits (the draft head's weights from seed 0,
+    # as in bench.py --seeds).  Seeds 0..9 at full size: two sampled requests
+    # per seed against the oracle, the whole schedule bit-exact, and the
+    # output structure on every request.
+    w = workload.WORKLOADS["serving_r1024_g16_v129280"]
+    req = sorted(set(np.random.default_rng(100 + seed).integers(0, w.R, size=2).tolist()))
+    inp, gd, gs, gv, ell = round_sampled(w, seed, req, weights_seed=0)
+    check_structure(w, gd, gv, ell)
+    assert 0 < ell.sum() < w.R * w.gamma  # the serving schedule trims: mixed prefix lengths
