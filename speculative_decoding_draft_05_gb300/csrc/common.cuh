@@ -79,6 +79,7 @@ struct PhiloxStream {
     return c;
   }
 
+
   __device__ __forceinline__ uint32_t word(uint32_t v) const {
     const uint4 w = quad(v >> 2);
     const uint32_t s = v & 3u;

@@ -89,6 +89,35 @@ def test_noalloc_verify_matches_workspace_verify_twice(w):
     assert (ref["n_acc"] < ell).any()  # rejections (residual draws) were exercised
 
 
+def test_noalloc_verify_matches_the_oracle_twice():
+    # Self-standing parity: the no-alloc entry point fed the oracle's draft
+    # outputs (rounded to fp32) and target logits built along the oracle's
+    # tokens, against the oracle's verify, on two calls in a row.
+    import oracle
+    from parity import compare_verify, f64, oracle_target_bias
+
+    w = workload.WORKLOADS["serving_r1024_g16_v129280"].resized(name="noalloc_oracle_r40_g4_v2056", R=40,
+                                                               gamma=4, V=2056, r=64)
+    inp = workload.generate(w, seed=5, device="cpu")
+    W1, W2 = f64(inp["W1"]), f64(inp["W2"])
+    L = _lib()
+    dev = torch.device("cuda")
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    ell = np.random.default_rng(1).integers(0, w.gamma + 1, size=w.R).astype(np.int32)
+    for seed in (5, 6):
+        od = oracle.draft(f64(inp["U"]), W1, W2, inp["x0"].numpy(), w.T, seed)
+        bias = oracle_target_bias(W1, W2, inp["x0"].numpy(), od["x"])
+        Z = workload.target_logits(w, inp["U"], seed, bias_rows=lambda i: torch.from_numpy(bias[i]))
+        ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), ell, w.T, seed)
+        d = dict(x=t(od["x"], torch.int32), logp=t(od["logp"], torch.float32),
+                 lse=t(od["lse"], torch.float32), scores=t(od["scores"], torch.float32))
+        got = _noalloc(L, d, Z.to(dev), t(ell, torch.int32), w.T, seed)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in got.items()}
+        ex = compare_verify(g, ov, ell, w.dtype)
+        assert len(ex) <= 1
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     L = _lib()
     R, g, V = 40000, 16, 1024  # more than 4 R (3 g + 1) bytes > 4 MiB of scratch
