@@ -9,7 +9,9 @@ builds it with gcc on first use and marshals numpy arrays through ctypes.
 Function-level citations are in the C file; the summary:
 
 * ``draft``     -- DSpark summary §3.1 and DSpark notes "DSpark 핵심 기술 1":
-                   s_k = (U_k + W1[x_{k-1}] W2) / T, lse_k, Gumbel-max x_k, logp_k.
+                   s_k = (U_k + W1[x_{k-1}] W2) / T, lse_k, x_k drawn from
+                   softmax(s_k) by two-level Gumbel-max (a group of 32 ids by
+                   its log-mass, then an id inside it), logp_k.
 * ``draft_rnn`` -- DSpark summary §3.1 (the RNN head: a state across the block
                    and the backbone hidden state; an Elman recurrence in the
                    Markov head's rank-r space).
@@ -44,6 +46,9 @@ _lib = None
 PURPOSE_DRAFT = 0
 PURPOSE_ACCEPT = 1
 PURPOSE_RESAMPLE = 2
+PURPOSE_DRAFT_GROUP = 3
+PURPOSE_RESAMPLE_GROUP = 4
+GROUP = 32  # ids per group of the two-level Gumbel-max
 
 
 def build(force: bool = False) -> str:

@@ -40,6 +40,9 @@
 #define ORACLE_PURPOSE_DRAFT 0u
 #define ORACLE_PURPOSE_ACCEPT 1u
 #define ORACLE_PURPOSE_RESAMPLE 2u
+#define ORACLE_PURPOSE_DRAFT_GROUP 3u
+#define ORACLE_PURPOSE_RESAMPLE_GROUP 4u
+#define ORACLE_GROUP 32
 
 /* ------------------------------------------------------------------------- */
 /* Philox4x32-10 (SC'11).  One round maps (c0,c1,c2,c3) with key (k0,k1) to   */
@@ -167,17 +170,63 @@ typedef struct {
 /* One draft position k of request i, shared by both heads: s holds the bias */
 /* B_k on entry and the scores s_k = (U_k + B_k) / T on return; the token is  */
 /* the Gumbel argmax of s_k, its log-probability s_k[x] - lse(s_k).           */
+/* ------------------------------------------------------------------------- */
+/* Two-level Gumbel-max: draw v with probability proportional to e^{lw[v]}    */
+/* (lw[v] = -inf for weight zero).  The ids are cut into groups of 32         */
+/* consecutive ids (the last one possibly shorter).  Stage 1 draws a group j  */
+/* by Gumbel-max over the groups' log-masses                                  */
+/*   L_j = log sum_{v in j} e^{lw[v]},  key_j = L_j + G(seed, req, pos, pg, j); */
+/* stage 2 draws v inside that group by Gumbel-max over                       */
+/*   lw[v] + G(seed, req, pos, pe, v).                                        */
+/* P(v) = P(group of v) P(v | group) = (e^{L_j} / sum_i e^{L_i}) (e^{lw[v]} /  */
+/* e^{L_j}) = e^{lw[v]} / sum_u e^{lw[u]}: the same law as one Gumbel-max over */
+/* all ids.  Both argmaxes decide on fp32-rounded keys, ties to the lowest id. */
+/* margin = the smaller of the two stages' top-1 minus top-2 key gaps.        */
+/* gkey holds ceil(V/32) doubles.  Returns -1 if every weight is zero.        */
+/* ------------------------------------------------------------------------- */
+static int two_level_argmax(const double* lw, int V, uint64_t seed, uint32_t req, uint32_t pos,
+                            uint32_t pg, uint32_t pe, double* gkey, double* margin) {
+  const int ng = (V + ORACLE_GROUP - 1) / ORACLE_GROUP;
+  for (int j = 0; j < ng; ++j) {
+    const int a = j * ORACLE_GROUP, b = (a + ORACLE_GROUP < V) ? a + ORACLE_GROUP : V;
+    double m = -INFINITY;
+    for (int v = a; v < b; ++v)
+      if (lw[v] > m) m = lw[v];
+    if (m == -INFINITY) {
+      gkey[j] = NAN; /* no weight in this group: it cannot be drawn */
+      continue;
+    }
+    double t = 0.0;
+    for (int v = a; v < b; ++v) t += exp(lw[v] - m);
+    gkey[j] = (m + log(t)) + oracle_gumbel(oracle_rng_word(seed, req, pos, pg, (uint32_t)j));
+  }
+  double m1 = 0.0, m2 = 0.0;
+  const int j = argmax_fp32(gkey, ng, &m1);
+  if (j < 0) {
+    if (margin) *margin = 0.0;
+    return -1;
+  }
+  const int a = j * ORACLE_GROUP, n = ((a + ORACLE_GROUP < V) ? a + ORACLE_GROUP : V) - a;
+  double ekey[ORACLE_GROUP];
+  for (int t = 0; t < n; ++t)
+    ekey[t] = (lw[a + t] == -INFINITY)
+                  ? NAN
+                  : lw[a + t] + oracle_gumbel(oracle_rng_word(seed, req, pos, pe, (uint32_t)(a + t)));
+  const int t = argmax_fp32(ekey, n, &m2);
+  if (margin) *margin = m1 < m2 ? m1 : m2;
+  return a + t;
+}
+
 static int32_t draft_sample(const draft_job* J, int i, int k, double* s, double* key) {
   const int g = J->gamma, V = J->V;
   const uint32_t req = (uint32_t)J->req_ids[i];
   const double* Uk = J->U + ((size_t)i * g + (k - 1)) * V;
   for (int v = 0; v < V; ++v) s[v] = (Uk[v] + s[v]) / J->T;
   const double lse = logsumexp(s, V);
-  for (int v = 0; v < V; ++v)
-    key[v] = s[v] + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)k,
-                                                  ORACLE_PURPOSE_DRAFT, (uint32_t)v));
+  /* x_k ~ softmax(s): two-level Gumbel-max over the scores */
   double margin = 0.0;
-  const int xk = argmax_fp32(key, V, &margin);
+  const int xk = two_level_argmax(s, V, J->seed, req, (uint32_t)k, ORACLE_PURPOSE_DRAFT_GROUP,
+                                  ORACLE_PURPOSE_DRAFT, key, &margin);
   const size_t o = (size_t)i * g + (k - 1);
   J->x[o] = xk;
   J->logp[o] = s[xk] - lse;
@@ -504,9 +553,10 @@ int oracle_schedule_topk(int R, int gamma, const float* c_now, int K, int32_t* e
 /*     ln u_j < (Z_j[x_j]/T - LSE^t_j) - logp_j    (fp32 decision),          */
 /*   u_j = U01(seed, request, j, ACCEPT, 0).  n = number of leading accepts.  */
 /*   n < l: the token at row n+1 is drawn from norm(max(0, p^t - p^d)) by     */
-/*   Gumbel-max with G(seed, request, n+1, RESAMPLE, v); if that residual is  */
-/*   identically zero it is drawn from p^t instead.                           */
-/*   n = l: the bonus token at row l+1 is drawn from p^t by Gumbel-max.       */
+/*   two-level Gumbel-max (groups G(seed, request, n+1, RESAMPLE_GROUP, j),   */
+/*   ids G(seed, request, n+1, RESAMPLE, v)); if that residual is identically */
+/*   zero it is drawn from p^t instead.                                       */
+/*   n = l: the bonus token at row l+1 is drawn from p^t the same way.        */
 /*   Emitted: x_1..x_n then that token; n_emit = n + 1 ([P1] §3: tau counts   */
 /*   the bonus token).  c*_j for j > l and LSE^t_j for j > l are NaN.         */
 /* ------------------------------------------------------------------------- */
@@ -578,34 +628,28 @@ static void verify_one(const verify_job* J, int i, double* buf, double* key) {
     const double* z = Zi + (size_t)(row - 1) * V;
     const double* s = Si + (size_t)(row - 1) * V;
     const double ld = J->lse[(size_t)i * g + (row - 1)];
-    int any = 0;
+    /* log-weights of norm(max(0, p^t - p^d)) (its normaliser does not change the draw) */
     for (int v = 0; v < V; ++v) {
       const double pt = exp(z[v] / J->T - lse_t[row]);
       const double pd = exp(s[v] - ld);
       const double res = pt - pd;
-      if (res > 0.0) {
-        any = 1;
-        key[v] = log(res) + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)row,
-                                                          ORACLE_PURPOSE_RESAMPLE, (uint32_t)v));
-      } else {
-        key[v] = NAN;
-      }
+      key[v] = res > 0.0 ? log(res) : -INFINITY;
     }
     kind = 1;
-    if (!any) {
+    tok = two_level_argmax(key, V, J->seed, req, (uint32_t)row, ORACLE_PURPOSE_RESAMPLE_GROUP,
+                           ORACLE_PURPOSE_RESAMPLE, buf, &margin);
+    if (tok < 0) { /* the residual is zero everywhere: draw from p^t */
       kind = 2;
-      for (int v = 0; v < V; ++v)
-        key[v] = z[v] / J->T + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)row,
-                                                             ORACLE_PURPOSE_RESAMPLE, (uint32_t)v));
+      for (int v = 0; v < V; ++v) key[v] = z[v] / J->T;
+      tok = two_level_argmax(key, V, J->seed, req, (uint32_t)row, ORACLE_PURPOSE_RESAMPLE_GROUP,
+                             ORACLE_PURPOSE_RESAMPLE, buf, &margin);
     }
-    tok = argmax_fp32(key, V, &margin);
   } else {
     const int row = L + 1;
     const double* z = Zi + (size_t)(row - 1) * V;
-    for (int v = 0; v < V; ++v)
-      key[v] = z[v] / J->T + oracle_gumbel(oracle_rng_word(J->seed, req, (uint32_t)row,
-                                                           ORACLE_PURPOSE_RESAMPLE, (uint32_t)v));
-    tok = argmax_fp32(key, V, &margin);
+    for (int v = 0; v < V; ++v) key[v] = z[v] / J->T;  /* bonus token from p^t */
+    tok = two_level_argmax(key, V, J->seed, req, (uint32_t)row, ORACLE_PURPOSE_RESAMPLE_GROUP,
+                           ORACLE_PURPOSE_RESAMPLE, buf, &margin);
   }
   int32_t* t = J->tokens + (size_t)i * (g + 1);
   for (int j = 0; j < g + 1; ++j) t[j] = -1;

@@ -63,8 +63,15 @@ MUTATIONS = [
      "for (int a = 0; a < r; ++a) z += h[a] * Wh[(size_t)j * r + a];"),
     ("RNN operand not rounded to bf16", "      A[j] = oracle_round_bf16(hn[j]);", "      A[j] = hn[j];"),
     ("draft stream keyed by the wrong position",
-     "(J->seed, req, (uint32_t)k,\n                                                  ORACLE_PURPOSE_DRAFT",
-     "(J->seed, req, (uint32_t)(k + 1),\n                                                  ORACLE_PURPOSE_DRAFT"),
+     "two_level_argmax(s, V, J->seed, req, (uint32_t)k, ORACLE_PURPOSE_DRAFT_GROUP,",
+     "two_level_argmax(s, V, J->seed, req, (uint32_t)(k + 1), ORACLE_PURPOSE_DRAFT_GROUP,"),
+    ("group mass is the group's largest weight",
+     "gkey[j] = (m + log(t)) + oracle_gumbel(", "gkey[j] = m + oracle_gumbel("),
+    ("second stage searches the first group",
+     "const int a = j * ORACLE_GROUP, n =", "const int a = 0 * ORACLE_GROUP, n ="),
+    ("group draws keyed like the id draws",
+     "ORACLE_PURPOSE_DRAFT_GROUP,\n                                  ORACLE_PURPOSE_DRAFT, key, &margin);",
+     "ORACLE_PURPOSE_DRAFT,\n                                  ORACLE_PURPOSE_DRAFT, key, &margin);"),
     ("RNN anchor ignored", "  int32_t prev = J->x0[i];\n  double* h", "  int32_t prev = 0;\n  double* h"),
     ("RNN previous token not advanced", "    }\n    prev = draft_sample(J, i, k, s, key);",
      "    }\n    (void)draft_sample(J, i, k, s, key);"),

@@ -66,10 +66,11 @@ def test_acceptance_frequency_matches_closed_form():
     np.testing.assert_allclose(v["cstar"][:, 0], c, atol=1e-14)
 
 
+@pytest.mark.parametrize("V", [8, 80])
 @pytest.mark.parametrize("ell", [0, 1, 3])
-def test_first_emitted_token_follows_target(ell):
+def test_first_emitted_token_follows_target(ell, V):
     rng = np.random.default_rng(10 + ell)
-    n, g, V = 60000, 3, 8
+    n, g = 60000, 3
     d = _draft_fixed(n, rng.normal(0, 1.2, size=(g, V)), seed=5)
     Zrow = rng.normal(0, 1.2, size=(g + 1, V))
     Z = np.repeat(Zrow[None], n, axis=0)
@@ -169,13 +170,34 @@ def test_temperature_applies_to_target():
     assert stats.chisquare(np.bincount(v["tokens"][:, 0], minlength=V), pt * n).pvalue > 1e-4
 
 
+def _two_level(lw, seed, req, pos, pg, pe):
+    """The two-level Gumbel-max as the header states it: groups of 32 ids by
+    log-mass + G(seed, req, pos, pg, group), then ids of the winning group by
+    log-weight + G(seed, req, pos, pe, id); fp32 keys, ties to the lowest."""
+    V = len(lw)
+    gkey = []
+    for j in range((V + 31) // 32):
+        seg = lw[32 * j: 32 * j + 32]
+        if np.all(seg == -np.inf):
+            gkey.append(-np.inf)
+        else:
+            gkey.append(special.logsumexp(seg) + oracle.gumbel(oracle.rng_word(seed, req, pos, pg, j)))
+    j = int(np.argmax(np.float32(gkey)))
+    seg = range(32 * j, min(V, 32 * j + 32))
+    ekey = [lw[v] + oracle.gumbel(oracle.rng_word(seed, req, pos, pe, v)) if lw[v] > -np.inf else -np.inf
+            for v in seg]
+    return 32 * j + int(np.argmax(np.float32(ekey)))
+
+
 def test_random_stream_layout_of_each_decision():
     # The counter layout is a convention both sides implement from the header:
-    # draft draws use (seed, request, k, DRAFT, v), the accept test uses
-    # (seed, request, j, ACCEPT, 0) and the resample/bonus draw uses
-    # (seed, request, row, RESAMPLE, v).  Rebuild each decision from those streams.
+    # draft draws use groups (seed, request, k, DRAFT_GROUP, j) then ids
+    # (seed, request, k, DRAFT, v), the accept test uses (seed, request, j,
+    # ACCEPT, 0) and the resample/bonus draw uses groups (seed, request, row,
+    # RESAMPLE_GROUP, j) then ids (seed, request, row, RESAMPLE, v).  Rebuild
+    # each decision from those streams (V = 80: two full groups and a short one).
     rng = np.random.default_rng(50)
-    n, g, V, seed = 6, 2, 16, 77
+    n, g, V, seed = 6, 2, 80, 77
     rows = rng.normal(0, 1.5, size=(g, V))
     d = _draft_fixed(n, rows, seed=seed)
     Z = rng.normal(0, 1.5, size=(n, g + 1, V))
@@ -184,15 +206,13 @@ def test_random_stream_layout_of_each_decision():
                      np.zeros(n, np.int32), 1.0, seed, req_ids=req_ids)
     for i, req in enumerate(req_ids):
         for k in range(1, g + 1):
-            key = [rows[k - 1][v] + oracle.gumbel(oracle.rng_word(seed, req, k, oracle.PURPOSE_DRAFT, v))
-                   for v in range(V)]
-            assert d["x"][i, k - 1] == int(np.argmax(np.float32(key)))
+            x = _two_level(rows[k - 1], seed, req, k, oracle.PURPOSE_DRAFT_GROUP, oracle.PURPOSE_DRAFT)
+            assert d["x"][i, k - 1] == x
     v = oracle.verify(d["x"], d["logp"], d["lse"], d["scores"], Z, np.zeros(n, np.int32), 1.0, seed,
                       req_ids=req_ids)
     for i, req in enumerate(req_ids):
-        key = [Z[i, 0, u] + oracle.gumbel(oracle.rng_word(seed, req, 1, oracle.PURPOSE_RESAMPLE, u))
-               for u in range(V)]
-        assert v["tokens"][i, 0] == int(np.argmax(np.float32(key)))
+        tok = _two_level(Z[i, 0], seed, req, 1, oracle.PURPOSE_RESAMPLE_GROUP, oracle.PURPOSE_RESAMPLE)
+        assert v["tokens"][i, 0] == tok
     v = oracle.verify(d["x"], d["logp"], d["lse"], d["scores"], Z, np.full(n, g), 1.0, seed,
                       req_ids=req_ids)
     for i, req in enumerate(req_ids):
@@ -205,9 +225,8 @@ def test_random_stream_layout_of_each_decision():
             pt = special.softmax(Z[i, row - 1])
             pd = np.exp(d["scores"][i, row - 1] - d["lse"][i, row - 1])
             res = pt - pd
-            key = [np.log(res[u]) + oracle.gumbel(oracle.rng_word(seed, req, row, oracle.PURPOSE_RESAMPLE, u))
-                   if res[u] > 0 else -np.inf for u in range(V)]
+            lw = np.where(res > 0, np.log(np.where(res > 0, res, 1.0)), -np.inf)
         else:  # bonus draw at row g + 1
-            key = [Z[i, g, u] + oracle.gumbel(oracle.rng_word(seed, req, g + 1, oracle.PURPOSE_RESAMPLE, u))
-                   for u in range(V)]
-        assert v["tokens"][i, v["n_acc"][i]] == int(np.argmax(np.float32(key)))
+            lw = Z[i, g]
+        tok = _two_level(lw, seed, req, row, oracle.PURPOSE_RESAMPLE_GROUP, oracle.PURPOSE_RESAMPLE)
+        assert v["tokens"][i, v["n_acc"][i]] == tok
