@@ -32,12 +32,21 @@
  *   stream reaches them.
  * - Randomness is Philox4x32-10 (Salmon et al., SC'11), keyed by the 64-bit
  *   `seed` (key = (seed & 0xffffffff, seed >> 32)).  The draw for
- *   (request r, position p, purpose q, vocab id v) uses counter
+ *   (request r, position p, purpose q, index v) uses counter
  *   (v >> 2, p, r, q) and output word (v & 3).  Purposes: DRAFT = 0 (draft
- *   Gumbel noise, p = k), ACCEPT = 1 (accept uniform, p = j, v = 0),
- *   RESAMPLE = 2 (residual or bonus Gumbel noise, p = row).  A word w maps to
- *   u = (2 (w >> 9) + 1) 2^-24 in (0,1); Gumbel noise is G = -ln(-ln u).
- *   Argmax ties go to the lowest vocab id.
+ *   Gumbel noise of vocab id v, p = k), ACCEPT = 1 (accept uniform, p = j,
+ *   v = 0), RESAMPLE = 2 (residual or bonus Gumbel noise of vocab id v,
+ *   p = row), DRAFT_GROUP = 3 and RESAMPLE_GROUP = 4 (the same for group
+ *   index v).  A word w maps to u = (2 (w >> 9) + 1) 2^-24 in (0,1); Gumbel
+ *   noise is G = -ln(-ln u).
+ * - Every token draw is a two-level Gumbel-max over log-weights lw(v): the
+ *   vocabulary is cut into groups of 32 consecutive ids (group j = ids
+ *   32j .. 32j+31, the last one shorter when V % 32 != 0); the group is
+ *   j* = argmax_j L_j + G(.., *_GROUP, j) with L_j = log sum_{v in j} e^{lw(v)},
+ *   then the token is argmax_{v in j*} lw(v) + G(.., v).  This samples
+ *   p(v) = e^{lw(v)} / sum_u e^{lw(u)} exactly, like one Gumbel-max over all
+ *   ids, with one random word per group plus 32 for the chosen group.  Keys
+ *   are compared in fp32; ties go to the lowest group and the lowest id.
  * - Return value: a dspark_status.  Host-side argument errors are returned
  *   before anything is enqueued.  Errors found on the device (bad token ids,
  *   l_r outside [0, gamma], confidence outside [0,1]) set bits in a status
@@ -71,7 +80,15 @@ typedef enum {
 
 typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 
-enum { DSPARK_PURPOSE_DRAFT = 0, DSPARK_PURPOSE_ACCEPT = 1, DSPARK_PURPOSE_RESAMPLE = 2 };
+enum {
+  DSPARK_PURPOSE_DRAFT = 0,
+  DSPARK_PURPOSE_ACCEPT = 1,
+  DSPARK_PURPOSE_RESAMPLE = 2,
+  DSPARK_PURPOSE_DRAFT_GROUP = 3,
+  DSPARK_PURPOSE_RESAMPLE_GROUP = 4
+};
+/* Ids per group of the two-level Gumbel-max draw. */
+enum { DSPARK_GROUP = 32 };
 
 /* Device status word bits (OR-ed together). */
 enum { DSPARK_DEV_BAD_INPUT = 1, DSPARK_DEV_TIMEOUT = 2 };
@@ -90,7 +107,8 @@ int dspark_version(void);
  *                                           contraction per k, fp32 accumulate)
  *   s_k(v)  = (U_k(v) + B_k(v)) / T         -> scores[r][k-1][v]
  *   lse_k   = log sum_v exp(s_k(v))         -> lse[r][k-1]
- *   x_k     = argmax_v s_k(v) + G(seed, r, k, DRAFT, v)   -> x[r][k-1]
+ *   x_k     = two-level Gumbel-max over lw = s_k, stream (seed, r, k, DRAFT_GROUP
+ *             / DRAFT)                       -> x[r][k-1]
  *   logp_k  = s_k(x_k) - lse_k              -> logp[r][k-1]
  * so p^d_k(v) = exp(scores - lse) is the locally normalised draft
  * distribution that verification needs.
@@ -241,9 +259,12 @@ int dspark_schedule_threshold(const float* conf, const double* temps, double the
  *   accept x_j (j = 1..l, in order) iff
  *     ln u_j < (Z_j[x_j]/T - LSE^t_j) - logp_j,  u_j = U01(seed, r, j, ACCEPT, 0)
  *   n = number of leading accepts.
- *   n < l : token = argmax_v ln max(0, p^t_{n+1} - p^d_{n+1})(v) + G(seed, r, n+1, RESAMPLE, v)
- *           (if that residual is zero everywhere: argmax_v Z_{n+1}(v)/T + G)
- *   n = l : bonus token = argmax_v Z_{l+1}(v)/T + G(seed, r, l+1, RESAMPLE, v)
+ *   n < l : token drawn from norm(max(0, p^t_{n+1} - p^d_{n+1})): two-level
+ *           Gumbel-max over lw = ln max(0, p^t - p^d) (-inf where zero), stream
+ *           (seed, r, n+1, RESAMPLE_GROUP / RESAMPLE); if that residual is zero
+ *           everywhere, over lw = Z_{n+1}/T instead
+ *   n = l : bonus token: two-level Gumbel-max over lw = Z_{l+1}/T, stream
+ *           (seed, r, l+1, RESAMPLE_GROUP / RESAMPLE)
  *   Emitted tokens: x_1..x_n, token; n_emit = n + 1.
  *
  * x, logp, lse, scores   the draft's outputs (layouts as in dspark_draft_sample)

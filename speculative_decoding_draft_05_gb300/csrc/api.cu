@@ -179,8 +179,8 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
       if (e != cudaSuccess) return cuda_fail(e, "draft_step");
     }
     prof_begin(kKindDraftCombine, s);
-    e = launch_draft_combine(buf[gamma & 1], R, gamma, V, r, gamma, W1, dtype, nullptr, x, logp, lse,
-                             status, s);
+    e = launch_draft_combine(buf[gamma & 1], R, gamma, V, r, gamma, W1, dtype, nullptr, scores, seed,
+                             x, logp, lse, status, s);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
     return DSPARK_OK;
@@ -195,8 +195,8 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "draft_tile");
     prof_begin(kKindDraftCombine, s);
-    e = launch_draft_combine(p, R, gamma, V, r, k, W1, dtype, k < gamma ? A : nullptr, x, logp, lse,
-                             status, s);
+    e = launch_draft_combine(p, R, gamma, V, r, k, W1, dtype, k < gamma ? A : nullptr, scores, seed,
+                             x, logp, lse, status, s);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
   }
@@ -268,8 +268,8 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
   for (int k = 1; k <= gamma; ++k) {
     prof_begin(kKindRnnState, s);
     e = launch_rnn_state(k, x0, W1, Wh, Q, buf[(k + 1) & 1], R, gamma, V, r,
-                         h + (size_t)((k + 1) & 1) * R * r, h + (size_t)(k & 1) * R * r, A, x, logp,
-                         lse, status, s);
+                         h + (size_t)((k + 1) & 1) * R * r, h + (size_t)(k & 1) * R * r, A, scores,
+                         seed, x, logp, lse, status, s);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "rnn_state");
     prof_begin(kKindDraftTile, s);
@@ -279,8 +279,8 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
     if (e != cudaSuccess) return cuda_fail(e, "draft_step");
   }
   prof_begin(kKindDraftCombine, s);
-  e = launch_draft_combine(buf[gamma & 1], R, gamma, V, r, gamma, W1, dtype, nullptr, x, logp, lse,
-                           status, s);
+  e = launch_draft_combine(buf[gamma & 1], R, gamma, V, r, gamma, W1, dtype, nullptr, scores, seed, x,
+                           logp, lse, status, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
   return DSPARK_OK;

@@ -79,7 +79,6 @@ struct PhiloxStream {
     return c;
   }
 
-
   __device__ __forceinline__ uint32_t word(uint32_t v) const {
     const uint4 w = quad(v >> 2);
     const uint32_t s = v & 3u;
@@ -131,6 +130,41 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
       i = oi;
     }
   }
+}
+
+// Warp-level argmax carrying a value at the argmax (ties to the lower index).
+__device__ __forceinline__ void warp_argmax3(float& key, int& idx, float& val) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ok = __shfl_xor_sync(0xffffffffu, key, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    const float ov = __shfl_xor_sync(0xffffffffu, val, o);
+    if (better(ok, oi, key, idx)) {
+      key = ok;
+      idx = oi;
+      val = ov;
+    }
+  }
+}
+
+// Ids per group of the two-level Gumbel-max draw: stage 1 draws a group of
+// kGroup consecutive ids by Gumbel-max over the groups' log-masses, stage 2
+// draws an id of that group by Gumbel-max over its log-weights.
+constexpr int kGroup = DSPARK_GROUP;
+
+// Stage 2 by one warp over group j: lane t holds id v = kGroup j + t with
+// log-weight lw (`valid`: v < V and the weight is non-zero) and keys it
+// lw + G(seed, request, position, purpose, v).  Every lane returns the best
+// key, its id and its log-weight (ties to the lower id).
+__device__ __forceinline__ void group_draw_warp(float lw, bool valid, int v, uint64_t seed,
+                                                uint32_t request, uint32_t position,
+                                                uint32_t purpose, float& key, int& idx,
+                                                float& lw_best) {
+  key = valid ? __fadd_rn(lw, gumbel(rng_word(seed, request, position, purpose, (uint32_t)v)))
+              : -INFINITY;
+  idx = valid ? v : 0x7fffffff;
+  lw_best = lw;
+  warp_argmax3(key, idx, lw_best);
 }
 
 __device__ __forceinline__ float warp_max(float v) {

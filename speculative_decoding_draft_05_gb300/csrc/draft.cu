@@ -11,9 +11,12 @@
 // One draft step k is two launches:
 //   tile kernel  : B_k tile = A_k[rows] . W2[:, tile]  (A_k = W1[x_{k-1}])
 //                  s = (U_k + B_k) / T -> scores; per (row, tile) partials
-//                  (max, sum exp, best Gumbel-perturbed score, its index and s)
-//   combine      : per row, merge the tiles' partials -> lse_k, x_k, logp_k,
-//                  and gather A_{k+1} = W1[x_k] for the next step.
+//                  (max, sum exp, and stage 1 of the two-level draw: the best
+//                  group key L_j + G(DRAFT_GROUP, j) over the tile's four
+//                  32-id groups, and that group's index)
+//   combine      : per row, merge the tiles' partials -> lse_k and the drawn
+//                  group; stage 2 draws x_k inside it from the stored scores
+//                  (G(DRAFT, v)); logp_k; and gather A_{k+1} = W1[x_k].
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -41,21 +44,6 @@ constexpr int kSimtRows = 16;
 constexpr int kSimtThreads = kDraftTileN;  // one thread per vocab column of the tile
 constexpr int kMaxRank = 256;
 
-// Warp-level argmax carrying the score at the argmax.
-__device__ __forceinline__ void warp_argmax3(float& key, int& idx, float& sval) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ok = __shfl_xor_sync(0xffffffffu, key, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    const float os = __shfl_xor_sync(0xffffffffu, sval, o);
-    if (better(ok, oi, key, idx)) {
-      key = ok;
-      idx = oi;
-      sval = os;
-    }
-  }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kSimtThreads)
 draft_tile_simt_kernel(const T* __restrict__ U, const T* __restrict__ A, const T* __restrict__ W2,
@@ -63,8 +51,7 @@ draft_tile_simt_kernel(const T* __restrict__ U, const T* __restrict__ A, const T
                        float* __restrict__ scores, float4* __restrict__ pstats,
                        int* __restrict__ pindex, int n_tiles) {
   __shared__ float As[kSimtRows][kMaxRank];
-  __shared__ float red_m[4][kSimtRows], red_s[4][kSimtRows], red_k[4][kSimtRows],
-      red_v[4][kSimtRows];
+  __shared__ float red_m[4][kSimtRows], red_s[4][kSimtRows], red_k[4][kSimtRows];
   __shared__ int red_i[4][kSimtRows];
   const int tile = blockIdx.x;
   const int row0 = blockIdx.y * kSimtRows;
@@ -93,51 +80,54 @@ draft_tile_simt_kernel(const T* __restrict__ U, const T* __restrict__ A, const T
   for (int rr = 0; rr < kSimtRows; ++rr) {
     const int row = row0 + rr;
     if (row >= R) break;  // uniform across the block
-    float s = -INFINITY, key = -INFINITY;
+    float s = -INFINITY;
     if (valid) {
       const size_t o = ((size_t)row * gamma + (k - 1)) * V + v;
       s = (to_f32(U[o]) + acc[rr]) * invT;
       scores[o] = s;
-      key = __fadd_rn(s, gumbel(rng_word(seed, (uint32_t)row, (uint32_t)k, DSPARK_PURPOSE_DRAFT,
-                                         (uint32_t)v)));
     }
+    // The warp's 32 columns are one group j of the two-level draw: its
+    // log-mass L_j = m + log S and its stage-1 key L_j + G(DRAFT_GROUP, j).
     float m = valid ? s : -INFINITY, S = valid ? 1.0f : 0.0f;
     warp_lse(m, S);
-    int idx = valid ? v : 0x7fffffff;
-    float sv = s;
-    warp_argmax3(key, idx, sv);
+    const int j = (tile * kDraftTileN + warp * 32) / kGroup;
+    float key = -INFINITY;
+    if (m != -INFINITY)
+      key = __fadd_rn(__fadd_rn(m, logf(S)),
+                      gumbel(rng_word(seed, (uint32_t)row, (uint32_t)k, DSPARK_PURPOSE_DRAFT_GROUP,
+                                      (uint32_t)j)));
     if (lane == 0) {
       red_m[warp][rr] = m;
       red_s[warp][rr] = S;
       red_k[warp][rr] = key;
-      red_i[warp][rr] = idx;
-      red_v[warp][rr] = sv;
+      red_i[warp][rr] = j;
     }
   }
   __syncthreads();
   if (tid < kSimtRows && row0 + tid < R) {
     const int rr = tid;
-    float m = red_m[0][rr], S = red_s[0][rr], key = red_k[0][rr], sv = red_v[0][rr];
+    float m = red_m[0][rr], S = red_s[0][rr], key = red_k[0][rr];
     int idx = red_i[0][rr];
     for (int w = 1; w < 4; ++w) {
       lse_merge(m, S, red_m[w][rr], red_s[w][rr]);
       if (better(red_k[w][rr], red_i[w][rr], key, idx)) {
         key = red_k[w][rr];
         idx = red_i[w][rr];
-        sv = red_v[w][rr];
       }
     }
     const size_t po = (size_t)(row0 + rr) * n_tiles + tile;
-    pstats[po] = make_float4(m, S, key, sv);
+    pstats[po] = make_float4(m, S, key, 0.0f);
     pindex[po] = idx;
   }
 }
 
-// One warp per row: merge the row's tile partials, sample x_k, gather W1[x_k].
+// One warp per row: merge the row's partials (lse_k and the drawn group),
+// draw x_k inside that group from the stored scores (stage 2), gather W1[x_k].
 template <typename T>
 __global__ void draft_combine_kernel(const float4* __restrict__ pstats,
                                      const int* __restrict__ pindex, int n_tiles, int R, int gamma,
                                      int r, int k, const T* __restrict__ W1, T* __restrict__ A_next,
+                                     const float* __restrict__ scores, uint64_t seed,
                                      int32_t* __restrict__ x, float* __restrict__ logp,
                                      float* __restrict__ lse, int V, int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
@@ -145,29 +135,39 @@ __global__ void draft_combine_kernel(const float4* __restrict__ pstats,
   if (row >= R) return;
   const float4* ps = pstats + (size_t)row * n_tiles;
   const int* pi = pindex + (size_t)row * n_tiles;
-  float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
-  int idx = 0x7fffffff;
+  float m = -INFINITY, S = 0.0f, key = -INFINITY, unused = 0.0f;
+  int gj = 0x7fffffff;
   for (int t = lane; t < n_tiles; t += 32) {
     const float4 q = ps[t];
     lse_merge(m, S, q.x, q.y);
     const int qi = pi[t];
-    if (better(q.z, qi, key, idx)) {
+    if (better(q.z, qi, key, gj)) {
       key = q.z;
-      idx = qi;
-      sv = q.w;
+      gj = qi;
     }
   }
   warp_lse(m, S);
-  warp_argmax3(key, idx, sv);
-  if (idx < 0 || idx >= V) {  // every score of the row was NaN
+  warp_argmax3(key, gj, unused);
+  const int n_groups = (V + kGroup - 1) / kGroup;
+  if (gj < 0 || gj >= n_groups) {  // every score of the row was NaN
     if (lane == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
-    idx = 0;
+    gj = 0;
+  }
+  const int v = gj * kGroup + lane;
+  const bool valid = v < V;
+  const float sv = valid ? scores[((size_t)row * gamma + (k - 1)) * V + v] : 0.0f;
+  float k2, s_x;
+  int idx;
+  group_draw_warp(sv, valid, v, seed, (uint32_t)row, (uint32_t)k, DSPARK_PURPOSE_DRAFT, k2, idx, s_x);
+  if (idx < 0 || idx >= V) {  // NaN scores inside the group
+    if (lane == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
+    idx = gj * kGroup;
   }
   const float l = m + logf(S);
   if (lane == 0) {
     const size_t o = (size_t)row * gamma + (k - 1);
     x[o] = idx;
-    logp[o] = sv - l;
+    logp[o] = s_x - l;
     lse[o] = l;
   }
   if (A_next) {
@@ -203,18 +203,19 @@ cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2,
 }
 
 cudaError_t launch_draft_combine(DraftPartials p, int R, int gamma, int V, int r, int k,
-                                 const void* W1, int dtype, void* A_next, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s) {
+                                 const void* W1, int dtype, void* A_next, const float* scores,
+                                 uint64_t seed, int32_t* x, float* logp, float* lse, int* status,
+                                 cudaStream_t s) {
   const int warps = 8;
   dim3 grid((R + warps - 1) / warps);
   if (dtype == DSPARK_BF16)
     draft_combine_kernel<__nv_bfloat16><<<grid, warps * 32, 0, s>>>(
         p.stats, p.index, p.n_parts, R, gamma, r, k, (const __nv_bfloat16*)W1,
-        (__nv_bfloat16*)A_next, x, logp, lse, V, status);
+        (__nv_bfloat16*)A_next, scores, seed, x, logp, lse, V, status);
   else
-    draft_combine_kernel<float><<<grid, warps * 32, 0, s>>>(p.stats, p.index, p.n_parts, R, gamma,
-                                                            r, k, (const float*)W1, (float*)A_next,
-                                                            x, logp, lse, V, status);
+    draft_combine_kernel<float><<<grid, warps * 32, 0, s>>>(
+        p.stats, p.index, p.n_parts, R, gamma, r, k, (const float*)W1, (float*)A_next, scores, seed,
+        x, logp, lse, V, status);
   return cudaGetLastError();
 }
 

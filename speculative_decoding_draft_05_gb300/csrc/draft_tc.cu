@@ -222,59 +222,6 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 }
 
 
-// Bit k of the candidate mask for d = fl(f + kf e) >= 1: d >= 2 exactly when
-// bit 30, the top bit of the exponent, is set (d is never negative).  k is a
-// constant after unrolling, so this is a shift and an and-or.
-__device__ __forceinline__ uint32_t cand_bit(float d, int k) {
-  const uint32_t b = __float_as_uint(d);
-  return k <= 30 ? (b >> (30 - k)) & (1u << k) : (b << 1) & 0x80000000u;
-}
-
-// Pass 1 of the draft epilogue over one warp's 32 columns of a row, branch-free:
-// returns the candidate mask and sets st = sum exp(s - mx).  Element i can beat
-// the running best key b only if 1 - u_i < y_i = exp(s_i - b); with
-// f_i = 1 + (w_i >> 9) 2^-23 = u_i + 1 - 2^-24 that is f_i > 2 - 2^-24 - y_i,
-// tested conservatively as fl(f_i + 1.001 y_i) >= 2 (kf = 1.001 exp(mx - b);
-// one rounding of the same inequality, and it admits every element that
-// f_i >= fl(2 - 1.001 y_i) admits).  The arithmetic runs on float pairs
-// (one packed FMA or add for two elements).  The scores are read back from the
-// row's staged block (128-byte swizzle), one 16-byte quad at a time; the
-// eight quads are unrolled so that every mask bit and address is a constant
-// offset.  MASKED: only the first nvalid columns take part.
-template <bool MASKED>
-__device__ __forceinline__ uint32_t filter_pass(const uint8_t* srow, int lane,
-                                                const PhiloxStream& rng, int col0, float mxl,
-                                                float kf, int nvalid, float& st) {
-  const float L2E = 1.4426950408889634f;
-  const float2 l2e = make_float2(L2E, L2E), nmx = make_float2(-mxl, -mxl), k2 = make_float2(kf, kf);
-  float2 sum01 = make_float2(0.0f, 0.0f), sum23 = make_float2(0.0f, 0.0f);
-  uint32_t cand = 0;
-  const uint32_t sw = (uint32_t)(lane & 7) << 4;  // the row's 128-byte swizzle
-  const uint32_t q0 = (uint32_t)col0 >> 2;
-#pragma unroll
-  for (int q4 = 0; q4 < 8; ++q4) {
-    const float4 sv = *(const float4*)(srow + (((uint32_t)q4 << 4) ^ sw));
-    const uint4 w4 = rng.quad(q0 + (uint32_t)q4);
-    const float2 a01 = __ffma2_rn(make_float2(sv.x, sv.y), l2e, nmx);
-    const float2 a23 = __ffma2_rn(make_float2(sv.z, sv.w), l2e, nmx);
-    float e[4] = {ex2_approx(a01.x), ex2_approx(a01.y), ex2_approx(a23.x), ex2_approx(a23.y)};
-    if (MASKED) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (4 * q4 + j >= nvalid) e[j] = 0.0f;  // then f + 0 < 2: never a candidate
-    }
-    const float2 e01 = make_float2(e[0], e[1]), e23 = make_float2(e[2], e[3]);
-    const float2 d01 = __ffma2_rn(e01, k2, make_float2(unit_float(w4.x), unit_float(w4.y)));
-    const float2 d23 = __ffma2_rn(e23, k2, make_float2(unit_float(w4.z), unit_float(w4.w)));
-    sum01 = __fadd2_rn(sum01, e01);
-    sum23 = __fadd2_rn(sum23, e23);
-    cand |= cand_bit(d01.x, 4 * q4) | cand_bit(d01.y, 4 * q4 + 1) | cand_bit(d23.x, 4 * q4 + 2) |
-            cand_bit(d23.y, 4 * q4 + 3);
-  }
-  st = (sum01.x + sum01.y) + (sum23.x + sum23.y);
-  return cand;
-}
-
 struct Params {
   int R, gamma, V, r, k, Mt, slots, n_tiles, n_parts;
   float invT;
@@ -292,10 +239,12 @@ struct Params {
   float* logp;
   float* lse;
   int* status;
+  float* scores;           // [R, gamma, V]: stored by the epilogue (kStg), read by stage 2
   long long wait_budget;  // SM clocks each bounded wait may take
   int withhold_w2;        // diagnostic: the producer issues no W2 loads, so the waits run out
 };
 
+template <bool kStg>
 __global__ void __launch_bounds__(kThreads, 1)
 draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
                      const __grid_constant__ CUtensorMap tmU,
@@ -441,9 +390,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     const int kpos = p.k - 1;
     const float L2E = 1.4426950408889634f;
 
-    const PhiloxStream rng(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT);
-    float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY, best_s = 0.0f;
-    int best_i = 0x7fffffff;
+    // Stage 1 of the two-level draw: one group key per (row, 32-column group).
+    const PhiloxStream rng(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT_GROUP);
+    float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY;
+    int best_j = 0x7fffffff;
     // Everything below reads or writes what the previous step (launched as this
     // grid's programmatic primary) wrote or reads: wait for its completion.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -479,8 +429,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       const int sub = lane & 3;
       const int arow = m_tile * kTileM + warp * 8 + (lane >> 2);
       const bool ok_row = arow < p.R;
-      float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
-      int idx = 0x7fffffff;
+      float m = -INFINITY, S = 0.0f, key = -INFINITY;
+      int gj = 0x7fffffff;
       for (int t0 = sub; t0 < p.n_parts; t0 += 4 * kMergeBatch) {
         float4 q[kMergeBatch];
         int qi[kMergeBatch];
@@ -495,10 +445,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
 #pragma unroll
         for (int b = 0; b < kMergeBatch; ++b) {
           lse_merge(m, S, q[b].x, q[b].y);
-          if (better(q[b].z, qi[b], key, idx)) {
+          if (better(q[b].z, qi[b], key, gj)) {
             key = q[b].z;
-            idx = qi[b];
-            sv = q[b].w;
+            gj = qi[b];
           }
         }
       }
@@ -508,12 +457,71 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
         lse_merge(m, S, m2, s2);
         const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-        const float v2 = __shfl_xor_sync(0xffffffffu, sv, o);
-        if (better(k2, i2, key, idx)) {
+        const int i2 = __shfl_xor_sync(0xffffffffu, gj, o);
+        if (better(k2, i2, key, gj)) {
           key = k2;
-          idx = i2;
-          sv = v2;
+          gj = i2;
+        }
+      }
+      // Stage 2: x_{k-1} inside group gj, from step k-1's stored scores.  The
+      // row's four lanes take 8 ids each; each lane keys its largest score
+      // exactly, filters the other seven against it (the draft epilogue's
+      // test, on ids), and the four lanes' best keys are merged.
+      int idx = 0x7fffffff;
+      float sv = 0.0f;
+      {
+        const bool have_group = ok_row && gj >= 0 && gj < (p.V + kGroup - 1) / kGroup;
+        const int v0 = (have_group ? gj : 0) * kGroup + 8 * sub;
+        float bk = -INFINITY;
+        if (have_group && v0 < p.V) {  // V % 8 == 0: the lane's 8 ids are all valid
+          const float4* src =
+              (const float4*)(p.scores + ((size_t)arow * p.gamma + (p.k - 2)) * p.V + v0);
+          const float4 s0 = src[0], s1 = src[1];
+          const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          const uint4 w0 = rng_quad(p.seed, (uint32_t)arow, (uint32_t)(p.k - 1), DSPARK_PURPOSE_DRAFT,
+                                    (uint32_t)v0 >> 2);
+          const uint4 w1 = rng_quad(p.seed, (uint32_t)arow, (uint32_t)(p.k - 1), DSPARK_PURPOSE_DRAFT,
+                                    ((uint32_t)v0 >> 2) + 1u);
+          const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          int im = 0;
+          float sm = sc[0];
+          uint32_t wm = w[0];
+#pragma unroll
+          for (int t = 1; t < 8; ++t)
+            if (sc[t] > sm) {
+              sm = sc[t];
+              wm = w[t];
+              im = t;
+            }
+          bk = __fadd_rn(sm, gumbel(wm));
+          idx = v0 + im;
+          sv = sm;
+          const float L2E = 1.4426950408889634f;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            if (t == im) continue;
+            // element t can reach bk only if fl(f + 1.001 exp(s - bk)) >= 2
+            const float d = unit_float(w[t]) + ex2_approx((sc[t] - bk) * L2E) * 1.001f;
+            if (d >= 2.0f) {
+              const float kt = __fadd_rn(sc[t], gumbel(w[t]));
+              if (better(kt, v0 + t, bk, idx)) {
+                bk = kt;
+                idx = v0 + t;
+                sv = sc[t];
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+          const float k2 = __shfl_xor_sync(0xffffffffu, bk, o);
+          const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
+          const float v2 = __shfl_xor_sync(0xffffffffu, sv, o);
+          if (better(k2, i2, bk, idx)) {
+            bk = k2;
+            idx = i2;
+            sv = v2;
+          }
         }
       }
       if (ok_row && slot == 0 && sub == 0) {
@@ -614,8 +622,13 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         }
       }
 
-      // Stage s (128-byte rows, 128-byte swizzle) and store it with TMA.
-      if (lane == 0) bulk_wait_read0();
+      // Stage s (128-byte rows, 128-byte swizzle) and store it: with TMA
+      // (!kStg), or with coalesced 16-byte stores, lanes 8i .. 8i+7 writing one
+      // row's 128 bytes (kStg: keeps the score stores off the TMA unit, which
+      // also carries the U and W2 loads).
+      if constexpr (!kStg) {
+        if (lane == 0) bulk_wait_read0();
+      }
       __syncwarp();
       {
         uint8_t* rowp = sbox + lane * 128;
@@ -625,14 +638,30 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           *(float4*)(rowp + pc * 16) = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
         }
       }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_3d(&tmS, sbox, col0, kpos, row0);
-        bulk_commit();
+      if constexpr (kStg) {
+        __syncwarp();
+        const int c = lane & 7;
+        const int v = col0 + 4 * c;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + (lane >> 3);
+          const float4 val = *(const float4*)(sbox + rr * 128 + ((c ^ (rr & 7)) << 4));
+          if (row0 + rr < p.R && v < p.V)
+            __stcs((float4*)(p.scores + ((size_t)(row0 + rr) * p.gamma + kpos) * p.V + v), val);
+        }
+      } else {
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmS, sbox, col0, kpos, row0);
+          bulk_commit();
+        }
       }
 
-      // Running statistics of this row over its columns.
+      // Running statistics of this row over its 32 columns, which are one
+      // group j of the two-level draw: the online (max, sum exp) of the row,
+      // and stage 1 -- the group's log-mass L_j = mx + log st and its key
+      // L_j + G(seed, row, k, DRAFT_GROUP, j).
       const int nvalid = row_ok ? min(32, p.V - col0) : 0;
       if (nvalid > 0) {
         if (nvalid < 32) {  // ragged last tile: columns past V take no part
@@ -644,52 +673,42 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
 #pragma unroll
         for (int i = 3; i < 31; i += 2) mx = fmax3(mx, s[i], s[i + 1]);
         mx = fmaxf(mx, s[31]);
-        // Threshold: the best key this row has reached so far in any of the
-        // CTA's four column groups (shared memory) or in any CTA of this step
-        // (global, raised with atomicMax).  Every published key is one an
-        // element of the row reached, so a stale value is still a lower bound
-        // of the row's maximum and no barrier is needed.
+        float st;
+        {
+          const float2 l2e = make_float2(L2E, L2E), nmx = make_float2(-mx * L2E, -mx * L2E);
+          float2 sum = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float2 a2 = __ffma2_rn(make_float2(s[i], s[i + 1]), l2e, nmx);
+            sum = __fadd2_rn(sum, make_float2(ex2_approx(a2.x), ex2_approx(a2.y)));
+          }
+          st = sum.x + sum.y;
+        }
+        lse_merge(run_m, run_s, mx, st);
+        const int gj = col0 >> 5;
+        const float Lg = __fadd_rn(mx, logf(st));
+        const uint4 w4 = rng.quad((uint32_t)col0 >> 7);  // groups 4n .. 4n+3 of vocab tile n
+        const uint32_t wg = cgrp == 0 ? w4.x : cgrp == 1 ? w4.y : cgrp == 2 ? w4.z : w4.w;
+        // Threshold: the best group key this row has reached so far in any of
+        // the CTA's four column groups (shared memory) or in any CTA of this
+        // step (global, raised with atomicMax).  Every published key is one a
+        // group of the row reached, so a stale value is still a lower bound of
+        // the row's maximum and no barrier is needed.
         volatile float* rowbest = (volatile float*)(smem + kOffRowBest) + row_local * 4;
         float thr = fmaxf(best, ord_key(gkey));
 #pragma unroll
         for (int g2 = 0; g2 < 4; ++g2)
           if (g2 != cgrp) thr = fmaxf(thr, rowbest[g2]);
-        uint32_t keep = 0xffffffffu;
-        if (thr == -INFINITY) {
-          // Seed with the tile's largest score (lowest such column): every
-          // other element is then filtered against a finite key.
-          int imx = 0;
-#pragma unroll
-          for (int i = 31; i >= 0; --i)
-            if (s[i] == mx) imx = i;
-          best = __fadd_rn(mx, gumbel(rng.word((uint32_t)(col0 + imx))));
-          best_i = col0 + imx;
-          best_s = mx;
-          keep = ~(1u << imx);
-          thr = best;
-          rowbest[cgrp] = best;
-          if (best < INFINITY) atomicMax(p.gthr_cur + row, key_ord(best));
-        }
-        // Pass 1 (filter_pass): sum of exp(s - mx) and the candidate mask.
-        const float mxl = mx * L2E;
-        const float kf = ex2_approx((mx - thr) * L2E) * 1.001f;
-        float st;
-        uint32_t cand = nvalid == 32 ? filter_pass<false>(sbox + lane * 128, lane, rng, col0, mxl, kf, 32, st)
-                                     : filter_pass<true>(sbox + lane * 128, lane, rng, col0, mxl, kf, nvalid, st);
-        cand &= keep;
-        lse_merge(run_m, run_s, mx, st);
-        // Pass 2: exact keys of the (rare) candidates, in increasing vocab id.
-        while (cand) {
-          const int i = __ffs(cand) - 1;
-          cand &= cand - 1;
-          // s_i from this warp's staged score block (row `lane`, 128-byte swizzle)
-          const float si =
-              *(const float*)(sbox + lane * 128 + (((i >> 2) ^ (lane & 7)) << 4) + ((i & 3) << 2));
-          const float key = __fadd_rn(si, gumbel(rng.word((uint32_t)(col0 + i))));
-          if (better(key, col0 + i, best, best_i)) {
+        // The group can reach thr only if 1 - u < exp(Lg - thr), tested as
+        // fl(f + 1.001 exp(Lg - thr)) >= 2 (f = 1 + (w >> 9) 2^-23); with no
+        // key yet the group is keyed exactly.
+        const bool cand = thr == -INFINITY ||
+                          unit_float(wg) + ex2_approx((Lg - thr) * L2E) * 1.001f >= 2.0f;
+        if (cand) {
+          const float key = __fadd_rn(Lg, gumbel(wg));
+          if (better(key, gj, best, best_j)) {
             best = key;
-            best_i = col0 + i;
-            best_s = si;
+            best_j = gj;
           }
         }
         if (best > thr) {  // publish for the row's other groups and CTAs
@@ -704,11 +723,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     mg[(0 * 4 + cgrp) * kTileM + row_local] = run_m;
     mg[(1 * 4 + cgrp) * kTileM + row_local] = run_s;
     mg[(2 * 4 + cgrp) * kTileM + row_local] = best;
-    mg[(3 * 4 + cgrp) * kTileM + row_local] = best_s;
-    ((int*)mg)[(4 * 4 + cgrp) * kTileM + row_local] = best_i;
+    ((int*)mg)[(4 * 4 + cgrp) * kTileM + row_local] = best_j;
     named_barrier(1, kEpiWarps * 32);
     if (cgrp == 0 && row_ok && n_units > 0) {
-      float m = -INFINITY, S = 0.0f, bk = -INFINITY, bs = 0.0f;
+      float m = -INFINITY, S = 0.0f, bk = -INFINITY;
       int bi = 0x7fffffff;
       for (int g = 0; g < 4; ++g) {
         lse_merge(m, S, mg[(0 * 4 + g) * kTileM + row_local], mg[(1 * 4 + g) * kTileM + row_local]);
@@ -717,11 +735,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         if (better(k2, i2, bk, bi)) {
           bk = k2;
           bi = i2;
-          bs = mg[(3 * 4 + g) * kTileM + row_local];
         }
       }
       const size_t o = (size_t)row * p.n_parts + slot;
-      p.pstats[o] = make_float4(m, S, bk, bs);
+      p.pstats[o] = make_float4(m, S, bk, 0.0f);
       p.pindex[o] = bi;
     }
     if (lane == 0) {
@@ -866,10 +883,16 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, 
       return cudaErrorInvalidValue;
   }
   // Once per process (thread-safe initialisation of a function-local static).
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(draft_step_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
+  static const cudaError_t attr_err = [] {
+    cudaError_t e = cudaFuncSetAttribute(draft_step_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(draft_step_tc_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return e;
+  }();
   if (attr_err != cudaSuccess) return attr_err;
+  plan->scores = scores;
   plan->R = R;
   plan->gamma = gamma;
   plan->V = V;
@@ -917,26 +940,27 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.logp = logp;
   p.lse = lse;
   p.status = status;
+  p.scores = plan.scores;
   p.wait_budget = wait_budget > 0 ? wait_budget : kWaitBudget;
   p.withhold_w2 = withhold_w2 ? 1 : 0;
-  if (k >= 2 || A_src) {
-    // Programmatic dependent launch on the previous kernel: the previous draft
-    // step, or (RNN head) the state update of this step, which itself follows
-    // the W2 transpose in stream order (see the kernel).
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(Mt * slots);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, draft_step_tc_kernel, maps[0], maps[1], maps[2], p);
-  }
-  draft_step_tc_kernel<<<Mt * slots, kThreads, kSmemBytes, s>>>(maps[0], maps[1], maps[2], p);
-  return cudaGetLastError();
+  // Score stores: coalesced st.global when several row tiles share each W2
+  // tile (the TMA unit then carries U and W2 for up to Mt CTAs' worth of
+  // stores), TMA stores for a single row tile (R <= 128), where W2 dominates.
+  auto kernel = Mt > 1 ? draft_step_tc_kernel<true> : draft_step_tc_kernel<false>;
+  // Programmatic dependent launch on the previous kernel for k >= 2 (the
+  // previous draft step) and for the RNN head (the state update of this step,
+  // which itself follows the W2 transpose in stream order; see the kernel).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Mt * slots);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (k >= 2 || A_src) ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], p);
 }
 
 }  // namespace dspark

@@ -8,12 +8,13 @@
 namespace dspark {
 
 // Per-row draft partials over a subset of the vocabulary: max m, sum exp(s - m),
-// best Gumbel-perturbed score, the score at that argmax; plus the argmax index.
-// The CUDA-core path writes one part per 128-column tile, the tensor-core path
-// one part per CTA slot.
+// and stage 1 of the two-level draw: the best group key L_j + G(DRAFT_GROUP, j)
+// of the subset's 32-id groups, with that group's index j.  The CUDA-core path
+// writes one part per 128-column tile, the tensor-core path one part per CTA
+// slot.
 struct DraftPartials {
-  float4* stats;  // [R, n_parts] (m, S, best_key, s_at_best)
-  int* index;     // [R, n_parts]
+  float4* stats;  // [R, n_parts] (m, S, best group key, unused)
+  int* index;     // [R, n_parts] best group index
   int n_parts;
 };
 
@@ -38,6 +39,7 @@ cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2,
 // Tensor maps of one draft call (W2, U, scores), encoded once on the host.
 struct DraftTcPlan {
   alignas(64) unsigned char maps[3][128];
+  float* scores;
   int R, gamma, V, r;
 };
 cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, int R, int gamma,
@@ -61,14 +63,16 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
 // Wh 16-byte aligned.
 cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const void* Wh,
                              const float* Q, const DraftPartials& prev, int R, int gamma, int V,
-                             int r, const float* h_prev, float* h_next, void* A, int32_t* x,
-                             float* logp, float* lse, int* status, cudaStream_t s);
+                             int r, const float* h_prev, float* h_next, void* A,
+                             const float* scores, uint64_t seed, int32_t* x, float* logp,
+                             float* lse, int* status, cudaStream_t s);
 bool draft_tc_supported(int R, int V, int r);
 int draft_tc_parts(int R, int V);  // partials per row written by the tensor-core path
 
 cudaError_t launch_draft_combine(DraftPartials p, int R, int gamma, int V, int r, int k,
-                                 const void* W1, int dtype, void* A_next, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s);
+                                 const void* W1, int dtype, void* A_next, const float* scores,
+                                 uint64_t seed, int32_t* x, float* logp, float* lse, int* status,
+                                 cudaStream_t s);
 
 // Scheduler: rank-and-scatter sort into `sorted` (R * gamma keys), then the scan.
 size_t schedule_sorted_bytes(int R, int gamma);

@@ -7,8 +7,10 @@
 //     h_0 = 0,  h_k = tanh(W1[x_{k-1}] + h_{k-1} Wh + Q_k),  B_k = bf16(h_k) W2,
 // the bias contraction B_k is the Markov head's (draft_tc.cu, A taken from a
 // buffer instead of gathered W1 rows).  This kernel runs before each draft
-// step: it merges the previous step's per-CTA partials into x_{k-1} (and
-// stores x, logp, lse of step k-1), then updates the state in fp32 and writes
+// step: it merges the previous step's per-CTA partials into the drawn group,
+// draws x_{k-1} inside that group (stage 2 of the two-level draw, from the
+// stored scores; it stores x, logp, lse of step k-1), then updates the state
+// in fp32 and writes
 // its bf16 rounding (nearest, ties to even) as the step's A rows.
 //
 // Grid: (row blocks of kRnnRows) x (column blocks of kRnnCols).  A CTA stages
@@ -36,7 +38,8 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
                  const __nv_bfloat16* __restrict__ Wh, const float* __restrict__ Q,
                  const float4* __restrict__ prev_stats, const int* __restrict__ prev_index,
                  int n_parts, int R, int gamma, int V, int r, const float* __restrict__ h_prev,
-                 float* __restrict__ h_next, __nv_bfloat16* __restrict__ A, int32_t* __restrict__ x,
+                 float* __restrict__ h_next, __nv_bfloat16* __restrict__ A,
+                 const float* __restrict__ scores, uint64_t seed, int32_t* __restrict__ x,
                  float* __restrict__ logp, float* __restrict__ lse, int* __restrict__ status) {
   __shared__ int s_x[kRnnRows];
   __shared__ float s_h[kRnnRows][kRnnMaxR];
@@ -92,31 +95,30 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
       if (k == 1) {
         xp = x0[row];
       } else {
-        float m = -INFINITY, S = 0.0f, key = -INFINITY, sv = 0.0f;
-        int idx = 0x7fffffff;
+        // Merge step k-1's partials (lse and the drawn group), then draw x_{k-1}
+        // inside that group from the stored scores (stage 2 of the two-level draw).
+        float m = -INFINITY, S = 0.0f, key = -INFINITY, unused = 0.0f;
+        int gj = 0x7fffffff;
         for (int t = lane; t < n_parts; t += 32) {
           const int u = (t - lane) >> 5;
           const float4 qs = u < 2 ? ps[u] : prev_stats[(size_t)row * n_parts + t];
           const int qi = u < 2 ? pi[u] : prev_index[(size_t)row * n_parts + t];
           lse_merge(m, S, qs.x, qs.y);
-          if (better(qs.z, qi, key, idx)) {
+          if (better(qs.z, qi, key, gj)) {
             key = qs.z;
-            idx = qi;
-            sv = qs.w;
+            gj = qi;
           }
         }
         warp_lse(m, S);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
-          const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-          const float v2 = __shfl_xor_sync(0xffffffffu, sv, o);
-          if (better(k2, i2, key, idx)) {
-            key = k2;
-            idx = i2;
-            sv = v2;
-          }
-        }
+        warp_argmax3(key, gj, unused);
+        if (gj < 0 || gj >= (V + kGroup - 1) / kGroup) gj = 0;  // NaN scores: flagged below
+        const int v = gj * kGroup + lane;
+        const bool valid = v < V;
+        const float s_v = valid ? scores[((size_t)row * gamma + (k - 2)) * V + v] : 0.0f;
+        float k2, sv;
+        int idx;
+        group_draw_warp(s_v, valid, v, seed, (uint32_t)row, (uint32_t)(k - 1), DSPARK_PURPOSE_DRAFT, k2,
+                        idx, sv);
         xp = idx;
         if (lane == 0 && blockIdx.y == 0) {  // one CTA per row stores step k-1
           const float l = m + logf(S);
@@ -154,8 +156,9 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
 
 cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const void* Wh,
                              const float* Q, const DraftPartials& prev, int R, int gamma, int V,
-                             int r, const float* h_prev, float* h_next, void* A, int32_t* x,
-                             float* logp, float* lse, int* status, cudaStream_t s) {
+                             int r, const float* h_prev, float* h_next, void* A,
+                             const float* scores, uint64_t seed, int32_t* x, float* logp,
+                             float* lse, int* status, cudaStream_t s) {
   if (r > kRnnMaxR || r % kRnnCols != 0) return cudaErrorInvalidValue;
   const dim3 grid((R + kRnnRows - 1) / kRnnRows, r / kRnnCols);
   cudaLaunchConfig_t cfg = {};
@@ -170,7 +173,7 @@ cudaError_t launch_rnn_state(int k, const int32_t* x0, const void* W1, const voi
   return cudaLaunchKernelEx(&cfg, rnn_state_kernel, k, x0, (const __nv_bfloat16*)W1,
                             (const __nv_bfloat16*)Wh, Q, (const float4*)prev.stats,
                             (const int*)prev.index, prev.n_parts, R, gamma, V, r, h_prev, h_next,
-                            (__nv_bfloat16*)A, x, logp, lse, status);
+                            (__nv_bfloat16*)A, scores, seed, x, logp, lse, status);
 }
 
 }  // namespace dspark

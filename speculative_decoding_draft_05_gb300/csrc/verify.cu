@@ -14,11 +14,13 @@
 //                 c*_j = sum_v min(p^d_j, p^t_j), and the accept test of x_j;
 //                 Z_j is streamed twice (the second pass hits L2) and the
 //                 score row once, with several 16-byte loads in flight.
-//   verify_draw   (vocab chunks x requests) CTAs: first rejection n, then the
-//                 Gumbel-max draw from norm(max(0, p^t - p^d)) at row n + 1 or
-//                 from p^t at the bonus row l + 1, one partial per chunk;
-//   verify_emit   one CTA per request: merges the partials, writes tokens,
-//                 n_acc, n_emit and the NaN padding of c* / LSE^t beyond l.
+//   verify_draw   (vocab chunks x requests) CTAs: first rejection n, then
+//                 stage 1 of the two-level Gumbel-max draw from
+//                 norm(max(0, p^t - p^d)) at row n + 1 or from p^t at the bonus
+//                 row l + 1: the best 32-id group key per chunk;
+//   verify_emit   one CTA per request: merges the chunks into the drawn group,
+//                 draws the token inside it (stage 2), writes tokens, n_acc,
+//                 n_emit and the NaN padding of c* / LSE^t beyond l.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -350,7 +352,7 @@ __device__ __forceinline__ int leading_accepts(const int* __restrict__ acc_ws, i
 
 // Philox4x32-10 round keys of one seed, passed by value as a kernel parameter:
 // the rounds read them as constant-bank operands rather than holding 20
-// registers (the draw kernel runs at 48 registers per thread).
+// registers.
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
@@ -398,7 +400,7 @@ struct KeyedPhilox {
 };
 
 constexpr int kDrawThreads = 256;
-constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 ids)
+constexpr int kDrawChunkGroups = 512;  // 32-id groups per draw CTA (16384 ids)
 
 // The residual row of the rejection draw, element by element.  With
 // a = z/T - LSE^t = ln p^t(v) and delta = ln p^t(v) - ln p^d(v) written as
@@ -408,29 +410,118 @@ constexpr int kDrawGroups = 2048;  // groups of 8 vocab ids per draw CTA (16384 
 // where p^t - p^d cancels.  The residual is max(0, p^t - p^d) =
 // p^t (1 - e^-delta) for delta > 0 and zero otherwise, and its log-weight
 // a + ln(1 - e^-delta) is evaluated without the cancelling subtraction.
-// Explicitly rounded operations: the filter and the exact key see the same
-// a and delta.
+// Explicitly rounded operations: every evaluation sees the same a and delta.
 __device__ __forceinline__ void residual_terms(float z, float s, float invT, float Lt, float dL,
                                                float& a, float& delta) {
   a = __fmaf_rn(z, invT, -Lt);
   delta = __fsub_rn(__fmaf_rn(z, invT, -s), dL);
 }
 
-__device__ __forceinline__ float residual_key(float a, float delta, uint32_t w) {
-  return __fadd_rn(__fadd_rn(a, logf(-expm1f(-delta))), gumbel(w));
+__device__ __forceinline__ float residual_lw(float a, float delta) {
+  return __fadd_rn(a, logf(-expm1f(-delta)));
 }
 
-// Gumbel-max over one chunk of the drawn row, with an exact-preserving filter:
-// element v can beat the running best key b only if -ln u_v < w_v exp(-b),
-// where w_v is its weight (the p^t mass for the bonus draw, the residual for
-// the rejection draw).  Since -ln u >= 1 - u, elements with 1 - u_v >= w_v e^-b
-// (0.1% slack) are skipped without the logarithms.  b is the best key any
-// warp of the CTA has reached so far (shared memory, raised with atomicMax in
-// key_ord form; a stale value is still a lower bound of the chunk's maximum).
-// Writes the chunk's (best key, index) partial.
-// Five CTAs per SM (48 registers): the draw is latency-bound per warp.
+// Log-mass of one 32-id group of the drawn row: log sum_v e^{lw(v)} over its
+// ids (the last group of a row may hold fewer: nv, a multiple of 8), with lw
+// = z/T (bonus draw, and the residual-free fallback) or the residual's
+// log-weight.  -inf when every weight of the group is zero.  The raw loads of
+// the group stay in registers and are unpacked twice (the maximum, then the
+// sum), so the group needs no array of its values.
 template <typename T>
-__global__ void __launch_bounds__(kDrawThreads, 5)
+__device__ __forceinline__ float group_log_mass(const T* __restrict__ z, const float* __restrict__ srow,
+                                                int v0, int nv, bool residual, float invT, float Lt,
+                                                float dL) {
+  const float L2E = 1.4426950408889634f;
+  const int g0 = v0 >> 3;  // first 8-id chunk
+  if (!residual) {
+    Raw8<T> raw[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (8 * c < nv) raw[c].load(z, g0 + c);
+    float m = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (8 * c < nv) {
+        float e[8];
+        raw[c].unpack(e);
+        m = fmaxf(m, fmaxf(fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])),
+                           fmaxf(fmaxf(e[4], e[5]), fmaxf(e[6], e[7]))));
+      }
+    m *= invT;  // T > 0: the largest z/T is the largest z, scaled
+    float S = 0.0f;
+    const float nm = -m * L2E, k = invT * L2E;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (8 * c < nv) {
+        float e[8];
+        raw[c].unpack(e);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) S += ex2_approx(__fmaf_rn(e[i], k, nm));
+      }
+    return __fadd_rn(m, logf(S));
+  }
+  // Residual: weights e^a (1 - e^-delta) for delta > 0, scaled by the largest
+  // e^a among them; two halves of 16 ids (registers), online merged.
+  float m = -INFINITY, S = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    if (16 * h >= nv) break;
+    Raw8<T> rz[2];
+    float4 sa[2], sb[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      if (16 * h + 8 * c < nv) {
+        rz[c].load(z, g0 + 2 * h + c);
+        sa[c] = __ldg(reinterpret_cast<const float4*>(srow) + 2 * (g0 + 2 * h + c));
+        sb[c] = __ldg(reinterpret_cast<const float4*>(srow) + 2 * (g0 + 2 * h + c) + 1);
+      }
+    float mh = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      if (16 * h + 8 * c < nv) {
+        float e[8];
+        rz[c].unpack(e);
+        const float sv[8] = {sa[c].x, sa[c].y, sa[c].z, sa[c].w, sb[c].x, sb[c].y, sb[c].z, sb[c].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float av, dt;
+          residual_terms(e[i], sv[i], invT, Lt, dL, av, dt);
+          if (dt > 0.0f) mh = fmaxf(mh, av);
+        }
+      }
+    if (mh == -INFINITY) continue;
+    float Sh = 0.0f;
+    const float nm = -mh * L2E;
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      if (16 * h + 8 * c < nv) {
+        float e[8];
+        rz[c].unpack(e);
+        const float sv[8] = {sa[c].x, sa[c].y, sa[c].z, sa[c].w, sb[c].x, sb[c].y, sb[c].z, sb[c].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float av, dt;
+          residual_terms(e[i], sv[i], invT, Lt, dL, av, dt);
+          if (dt > 0.0f) Sh += ex2_approx(__fmaf_rn(av, L2E, nm)) * -expm1f(-dt);
+        }
+      }
+    lse_merge(m, S, mh, Sh);
+  }
+  return (m == -INFINITY || !(S > 0.0f)) ? -INFINITY : __fadd_rn(m, logf(S));
+}
+
+// Stage 1 of the two-level draw over one chunk of 512 groups of the drawn row
+// (the rejected row's residual, or the bonus row's p^t): one group per thread
+// at a time.  A group's key is L_j + G(seed, r, row, RESAMPLE_GROUP, j); it can
+// beat the running best key b only if 1 - u_j < exp(L_j - b), tested as
+// fl(f + 1.001 exp(L_j - b)) >= 2 (f = 1 + (w >> 9) 2^-23), so the two
+// logarithms run only for candidates.  b is the best key any thread of the
+// CTA has reached so far (shared memory, raised with atomicMax in key_ord
+// form; a stale value is still a lower bound of the chunk's maximum).
+// Writes the chunk's (best group key, group index) partial; the emit kernel
+// merges the chunks and draws the token inside the winning group.
+template <typename T>
+__global__ void __launch_bounds__(kDrawThreads, 4)
 verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
                    const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
                    float invT, const PhiloxKeys keys, const float* __restrict__ lse_t_ws,
@@ -456,157 +547,52 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   const bool residual = n < L;
   const int row = n + 1;  // 1-based position of the drawn token
   const T* z = Z + zr.row(r, row) * V;
-  const int groups = V >> 3;
-  const int g0 = chunk * kDrawGroups, g1 = min(groups, g0 + kDrawGroups);
-  const float L2E = 1.4426950408889634f;
-  const KeyedPhilox rng(keys, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
-  // best/idx: this thread's argmax; a lane publishes its best key into the
-  // CTA's threshold whenever it beats the threshold it filtered against.
-  float best = -INFINITY;
-  int idx = 0x7fffffff;
-  const int lane = threadIdx.x & 31;
-  const int iters = (g1 - g0 + kDrawThreads - 1) / kDrawThreads;  // uniform across the CTA
+  const float* srow = scores + ((size_t)r * gamma + (residual ? row - 1 : 0)) * V;
+  float Lt = 0.0f, dL = 0.0f;
   if (residual) {
-    const float* srow = scores + ((size_t)r * gamma + (row - 1)) * V;
-    const float ld = lse[(size_t)r * gamma + (row - 1)];
-    const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
-    const float dL = __fsub_rn(Lt, ld);
-    for (int it = 0; it < iters; ++it) {
-      const int g = g0 + it * kDrawThreads + threadIdx.x;
-      const bool have = g < g1;
-      float e[8], sc[8];
-      if (have) {
-        load8(z, g, e);
-        load8(srow, g, sc);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = sc[i] = 0.0f;
+    Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+    dL = __fsub_rn(Lt, lse[(size_t)r * gamma + (row - 1)]);
+  }
+  const int n_groups = (V + kGroup - 1) / kGroup;
+  const int j1 = min(n_groups, (chunk + 1) * kDrawChunkGroups);
+  const float L2E = 1.4426950408889634f;
+  const KeyedPhilox rng(keys, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE_GROUP);
+  float best = -INFINITY;
+  int bj = 0x7fffffff;
+  for (int j = chunk * kDrawChunkGroups + threadIdx.x; j < j1; j += kDrawThreads) {
+    const int v0 = j * kGroup;
+    const float Lg = group_log_mass(z, srow, v0, min(kGroup, V - v0), residual, invT, Lt, dL);
+    if (Lg == -INFINITY) continue;
+    const uint4 q = rng.quad(keys, (uint32_t)j >> 2);
+    const int sub = j & 3;
+    const uint32_t w = sub == 0 ? q.x : sub == 1 ? q.y : sub == 2 ? q.z : q.w;
+    const float thr = ord_key(*cta_best);
+    const bool cand = thr == -INFINITY ||
+                      __uint_as_float(__funnelshift_r(w, 0x7Fu, 9)) +
+                              ex2_approx((Lg - thr) * L2E) * 1.001f >= 2.0f;
+    if (cand) {
+      const float key = __fadd_rn(Lg, gumbel(w));
+      if (better(key, j, best, bj)) {
+        best = key;
+        bj = j;
       }
-      const uint4 w0 = rng.quad(keys, 2 * g), w1 = rng.quad(keys, 2 * g + 1);
-      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-      const float thr = ord_key(*cta_best);
-      if (have) {
-        // Candidate test, conservative for the exact key residual_key(a, delta, w):
-        //   key >= b  implies  1 - u < e^(a - b) (1 - e^-delta)  (up to roundings
-        //   far below the 0.1% slack), and 1 - e^-delta <= gb =
-        //   min(delta, 1 - ex2(-delta log2 e) + 2^-20): delta is an exact upper
-        //   bound, and 2^-20 covers the approximate ex2's absolute error on [0, 1].
-        const float nb = -thr * L2E;
-        uint32_t cand = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          float a, dt;
-          residual_terms(e[i], sc[i], invT, Lt, dL, a, dt);
-          const float y = ex2_approx(__fmaf_rn(a, L2E, nb));
-          const float gb = fminf(dt, __fadd_rn(__fsub_rn(1.0f, ex2_approx(-dt * L2E)),
-                                               9.5367431640625e-07f));
-          const float om = __fsub_rn(__uint_as_float(0x3F800000u | ((~w[i]) >> 9)), 0.99999994f);
-          cand |= (dt > 0.0f && om < y * gb * 1.001f) ? (1u << i) : 0u;
-        }
-        if (cand) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (!(cand & (1u << i))) continue;
-            float a, dt;  // the same explicitly rounded a and delta as the test above
-            residual_terms(e[i], sc[i], invT, Lt, dL, a, dt);
-            const float key = residual_key(a, dt, w[i]);
-            if (better(key, 8 * g + i, best, idx)) {
-              best = key;
-              idx = 8 * g + i;
-            }
-          }
-          if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
-        }
-      }
-      __syncwarp();
-    }
-  } else {
-    const float invT_l2e = invT * L2E;
-    for (int it = 0; it < iters; ++it) {
-      const int g = g0 + it * kDrawThreads + threadIdx.x;
-      const bool have = g < g1;
-      float e[8];
-      uint32_t w[8];
-      if (have) {
-        load8(z, g, e);
-        const uint4 w0 = rng.quad(keys, 2 * g), w1 = rng.quad(keys, 2 * g + 1);
-        w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
-        w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-      }
-      float thr = __shfl_sync(0xffffffffu, ord_key(*cta_best), 0);  // one value per warp
-      if (thr == -INFINITY) {
-        // Seed the threshold with one exact key: the lane holding the warp's
-        // largest logit evaluates it.
-        float em = -INFINITY;
-        int im = 0;
-        if (have) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (e[i] > em) {
-              em = e[i];
-              im = i;
-            }
-        }
-        float wm = em;
-        int wl = lane;
-        warp_argmax(wm, wl);
-        if (lane == wl && have) {
-          uint32_t ws = w[0];
-#pragma unroll
-          for (int i = 1; i < 8; ++i)
-            if (i == im) ws = w[i];
-          const float key = __fadd_rn(em * invT, gumbel(ws));
-          if (better(key, 8 * g + im, best, idx)) {
-            best = key;
-            idx = 8 * g + im;
-          }
-          if (best < INFINITY) atomicMax(&s_best, key_ord(best));
-        }
-        thr = warp_max(best);
-      }
-      if (have) {
-        // candidate iff fl(f_i + 1.001 exp(z_i / T - b)) >= 2, f_i = 1 + (w_i >> 9) 2^-23:
-        // one rounding of f_i >= 2 - 1.001 exp(z_i / T - b), on float pairs
-        const float2 it2 = make_float2(invT_l2e, invT_l2e), c02 = make_float2(-thr * L2E, -thr * L2E);
-        const float2 k2 = make_float2(1.001f, 1.001f);
-        uint32_t cand = 0;
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float2 av = __ffma2_rn(make_float2(e[i], e[i + 1]), it2, c02);
-          const float2 y = make_float2(ex2_approx(av.x), ex2_approx(av.y));
-          const float2 f = make_float2(__uint_as_float(__funnelshift_r(w[i], 0x7Fu, 9)),
-                                       __uint_as_float(__funnelshift_r(w[i + 1], 0x7Fu, 9)));
-          const float2 d = __ffma2_rn(y, k2, f);
-          cand |= d.x >= 2.0f ? (1u << i) : 0u;
-          cand |= d.y >= 2.0f ? (2u << i) : 0u;
-        }
-        if (cand) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (!(cand & (1u << i))) continue;
-            const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
-            if (better(key, 8 * g + i, best, idx)) {
-              best = key;
-              idx = 8 * g + i;
-            }
-          }
-          if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
-        }
-      }
-      __syncwarp();
+      if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
     }
   }
-  block_argmax<kDrawThreads / 32>(best, idx, rk, ri);
+  block_argmax<kDrawThreads / 32>(best, bj, rk, ri);
   if (threadIdx.x == 0)
-    partials[(size_t)r * n_chunks + chunk] = make_float2(best, __int_as_float(idx));
+    partials[(size_t)r * n_chunks + chunk] = make_float2(best, __int_as_float(bj));
 }
 
-// Per request: merge the chunks' partials into the drawn token (for a residual
-// that is zero everywhere, draw from p^t over the whole row instead), then
-// write tokens, n_acc, n_emit and the NaN padding of c* / LSE^t beyond l.
+// Per request: merge the chunks' partials into the drawn group (for a residual
+// that is zero everywhere, draw the group from p^t over the whole row
+// instead), draw the token inside it (stage 2, warp 0: lane t keys id
+// 32 j + t with G(seed, r, row, RESAMPLE, v)), then write tokens, n_acc,
+// n_emit and the NaN padding of c* / LSE^t beyond l.
 template <typename T>
 __global__ void __launch_bounds__(kVerifyThreads)
-verify_emit_kernel(const int32_t* __restrict__ x, const T* __restrict__ Z,
+verify_emit_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
+                   const float* __restrict__ scores, const T* __restrict__ Z,
                    const int32_t* __restrict__ ell, int gamma, int V, float invT, uint64_t seed,
                    const float* __restrict__ lse_t_ws, const int* __restrict__ acc_ws,
                    const float2* __restrict__ partials, int n_chunks, int32_t* __restrict__ n_acc,
@@ -618,45 +604,72 @@ verify_emit_kernel(const int32_t* __restrict__ x, const T* __restrict__ Z,
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float rk[kWarps];
   __shared__ int ri[kWarps];
-  __shared__ int s_n;
+  __shared__ int s_n, s_tok;
   const int r = blockIdx.x;
   const int L = clamp_ell(ell, r, gamma, nullptr, false);
   if (threadIdx.x == 0) s_n = leading_accepts(acc_ws, r, gamma, L);
   __syncthreads();
   const int n = s_n;
   const int row = n + 1;
+  bool residual = n < L;
+  const T* z = Z + zr.row(r, row) * V;
   float best = -INFINITY;
-  int idx = 0x7fffffff;
+  int gj = 0x7fffffff;
   for (int c = threadIdx.x; c < n_chunks; c += kVerifyThreads) {
     const float2 p = partials[(size_t)r * n_chunks + c];
     const int pi = __float_as_int(p.y);
-    if (better(p.x, pi, best, idx)) {
+    if (better(p.x, pi, best, gj)) {
       best = p.x;
-      idx = pi;
+      gj = pi;
     }
   }
-  block_argmax<kWarps>(best, idx, rk, ri);
+  block_argmax<kWarps>(best, gj, rk, ri);
+  const int n_groups = (V + kGroup - 1) / kGroup;
   if (best == -INFINITY) {
-    // Residual zero everywhere (p^t = p^d numerically): draw from p^t.
-    const T* z = Z + zr.row(r, row) * V;
-    const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE);
-    idx = 0x7fffffff;
-    for (int g = threadIdx.x; g < (V >> 3); g += kVerifyThreads) {
-      float e[8];
-      load8(z, g, e);
-      const uint4 w0 = rng.quad(2 * g), w1 = rng.quad(2 * g + 1);
-      const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float key = __fadd_rn(e[i] * invT, gumbel(w[i]));
-        if (better(key, 8 * g + i, best, idx)) {
-          best = key;
-          idx = 8 * g + i;
-        }
+    // Residual zero everywhere (p^t = p^d numerically): draw from p^t, stage 1
+    // over every group of the row here.
+    residual = false;
+    const PhiloxStream rng(seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE_GROUP);
+    gj = 0x7fffffff;
+    for (int j = threadIdx.x; j < n_groups; j += kVerifyThreads) {
+      const int v0 = j * kGroup;
+      const float Lg = group_log_mass(z, (const float*)nullptr, v0, min(kGroup, V - v0), false, invT,
+                                      0.0f, 0.0f);
+      const float key = __fadd_rn(Lg, gumbel(rng.word((uint32_t)j)));
+      if (better(key, j, best, gj)) {
+        best = key;
+        gj = j;
       }
     }
-    block_argmax<kWarps>(best, idx, rk, ri);
+    block_argmax<kWarps>(best, gj, rk, ri);
   }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    if (gj < 0 || gj >= n_groups) gj = 0;  // NaN logits only
+    const int v = gj * kGroup + lane;
+    bool valid = v < V;
+    float lw = 0.0f;
+    if (valid) {
+      const float zv = to_f32(z[v]);
+      if (residual) {
+        const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+        const float dL = __fsub_rn(Lt, lse[(size_t)r * gamma + (row - 1)]);
+        float a, dt;
+        residual_terms(zv, scores[((size_t)r * gamma + (row - 1)) * V + v], invT, Lt, dL, a, dt);
+        valid = dt > 0.0f;
+        if (valid) lw = residual_lw(a, dt);
+      } else {
+        lw = zv * invT;
+      }
+    }
+    float key, lwb;
+    int tok;
+    group_draw_warp(lw, valid, v, seed, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE, key, tok,
+                    lwb);
+    if (lane == 0) s_tok = tok < V ? tok : gj * kGroup;
+  }
+  __syncthreads();
+  const int idx = s_tok;
   int32_t* trow = tokens + (size_t)r * (gamma + 1);
   for (int t = threadIdx.x; t < gamma + 1; t += kVerifyThreads) {
     int32_t out = -1;
@@ -726,7 +739,10 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
                         zr);
 }
 
-int verify_draw_chunks(int V) { return ((V >> 3) + kDrawGroups - 1) / kDrawGroups; }
+int verify_draw_chunks(int V) {
+  const int n_groups = (V + kGroup - 1) / kGroup;
+  return (n_groups + kDrawChunkGroups - 1) / kDrawChunkGroups;
+}
 
 cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
                                  const void* Z, int dtype, const int32_t* ell, int R, int gamma,
@@ -743,14 +759,15 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
                        acc_ws, partials, chunks, zr);
     if (e != cudaSuccess) return e;
     return launch_chained(verify_emit_kernel<__nv_bfloat16>, dim3(R), dim3(kVerifyThreads), s, x,
-                          (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                          (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
+                          lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws,
+                          acc_ws, (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t,
+                          zr);
   }
   e = launch_chained(verify_draw_kernel<float>, grid, dim3(kDrawThreads), s, lse, scores,
                      (const float*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
                      partials, chunks, zr);
   if (e != cudaSuccess) return e;
-  return launch_chained(verify_emit_kernel<float>, dim3(R), dim3(kVerifyThreads), s, x,
+  return launch_chained(verify_emit_kernel<float>, dim3(R), dim3(kVerifyThreads), s, x, lse, scores,
                         (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws,
                         (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
 }
