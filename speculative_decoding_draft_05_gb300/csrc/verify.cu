@@ -225,7 +225,10 @@ template <> struct Raw8<float> {
 // then the logit Z_j[x_j]) one pass ahead of their use.
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
+// 16-byte loads of Z per thread in flight: pass 1 (Z alone) and pass 2 (Z and
+// the scores).  Larger values spill at the 64 registers two CTAs per SM allow.
 template <typename T> constexpr int row_unroll() { return sizeof(T) == 2 ? 4 : 2; }
+template <typename T> constexpr int row_unroll2() { return sizeof(T) == 2 ? 2 : 1; }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads, 2)
@@ -308,11 +311,12 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
 
     // Pass 2: sum over the row of min(p^d, p^t) = exp(min(s - lse^d, z / T - LSE^t)).
     float acc = 0.0f;
-    for (int g0 = threadIdx.x; g0 < groups; g0 += kRowThreads * (kRowUnroll / 2)) {
-      Raw8<T> raw[kRowUnroll / 2];
-      float4 sa[kRowUnroll / 2], sb[kRowUnroll / 2];
+    constexpr int kRowUnroll2 = row_unroll2<T>();
+    for (int g0 = threadIdx.x; g0 < groups; g0 += kRowThreads * kRowUnroll2) {
+      Raw8<T> raw[kRowUnroll2];
+      float4 sa[kRowUnroll2], sb[kRowUnroll2];
 #pragma unroll
-      for (int u = 0; u < kRowUnroll / 2; ++u) {
+      for (int u = 0; u < kRowUnroll2; ++u) {
         const int g = g0 + u * kRowThreads;
         if (g < groups) {
           raw[u].load(z, g);
@@ -321,7 +325,7 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
         }
       }
 #pragma unroll
-      for (int u = 0; u < kRowUnroll / 2; ++u) {
+      for (int u = 0; u < kRowUnroll2; ++u) {
         if (g0 + u * kRowThreads >= groups) break;
         float e[8];
         raw[u].unpack(e);
