@@ -524,6 +524,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           }
         }
       }
+      if (ok_row && (idx < 0 || idx >= p.V)) {  // nothing drawn: every score of the row was NaN
+        if (sub == 0) flag_status(p.status, DSPARK_DEV_BAD_INPUT);
+        idx = 0;
+      }
       if (ok_row && slot == 0 && sub == 0) {
         const float l = m + logf(S);
         const size_t o = (size_t)arow * p.gamma + (p.k - 2);

@@ -119,6 +119,10 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
         int idx;
         group_draw_warp(s_v, valid, v, seed, (uint32_t)row, (uint32_t)(k - 1), DSPARK_PURPOSE_DRAFT, k2,
                         idx, sv);
+        if (idx < 0 || idx >= V) {  // nothing drawn: every score of the row was NaN
+          if (lane == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
+          idx = 0;
+        }
         xp = idx;
         if (lane == 0 && blockIdx.y == 0) {  // one CTA per row stores step k-1
           const float l = m + logf(S);
