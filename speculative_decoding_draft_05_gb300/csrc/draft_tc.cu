@@ -30,14 +30,19 @@
 //     M = 128, N = 128, K = 16) from shared-memory descriptors: A and W2^T both
 //     K-major, 128-byte swizzled.
 //   * warps 0..15 (epilogue): warp w reads TMEM lanes 32 (w % 4) .. +31 (its
-//     rows) and columns 32 (w / 4) .. +31 of the tile.  Per tile it TMA-loads
-//     its [32 x 32] block of U_k, computes s, stages it in swizzled shared
-//     memory and TMA-stores it, and updates per-row running statistics in
-//     registers: max / sum-exp (online), and the Gumbel-max best key.
-//   * Gumbel filter: element v can beat the running best key b only if
-//     -ln u_v < exp(s_v - b); since -ln u >= 1 - u, the cheap test
-//     1 - u_v < exp(s_v - b) (with 0.1% slack) lets the two logarithms run only
-//     for candidates.  The decision is the exact fp32 argmax of s + G.
+//     rows) and columns 32 (w / 4) .. +31 of the tile.  The four warps of a
+//     row quarter share its U_k tile (32 rows x 128 columns, two TMA boxes with
+//     128-byte rows, loaded by the quarter's column-group-0 warp once all four
+//     have read the previous one).  Each warp computes s, stages it in
+//     swizzled shared memory and stores it (coalesced st.global for several
+//     row tiles, TMA for one), and updates per-row running statistics in
+//     registers: max / sum-exp (online), and stage 1 of the two-level draw.
+//   * Two-level draw: each warp's 32 columns of a row are one group; its key
+//     L_j + G(DRAFT_GROUP, j) can beat the running best key b only if
+//     -ln u < exp(L_j - b); since -ln u >= 1 - u, the cheap test
+//     1 - u < exp(L_j - b) (with 0.1% slack) lets the two logarithms run only
+//     for candidates.  Stage 2 (an id inside the drawn group) runs in the next
+//     step's prologue, or in the combine after the last step.
 //   * Every mbarrier wait is bounded (about 2 s of SM clocks); on expiry the
 //     CTA flags DSPARK_DEV_TIMEOUT in the status word, stops issuing work,
 //     drains what it issued, frees TMEM and returns.
@@ -67,14 +72,15 @@ constexpr uint32_t kTmemCols = 256;
 
 constexpr int kAChunkBytes = kTileM * kChunkK * 2;  // 16 KB
 constexpr int kBChunkBytes = kChunkK * kTileN * 2;  // 16 KB (two 64-column boxes)
-constexpr int kUBoxBytes = 32 * 32 * 2;             // 2 KB per epilogue warp
+constexpr int kUBoxBytes = 32 * 64 * 2;             // 4 KB: 32 rows x 64 columns of U
+constexpr int kUQuarterBytes = 2 * kUBoxBytes;      // 8 KB: a row quarter's 128 columns
 constexpr int kSBoxBytes = 32 * 32 * 4;             // 4 KB per epilogue warp
 
 // Shared memory layout (offsets from a 1024-aligned base).
 constexpr int kOffA = 0;                                            // 4 x 16 KB
 constexpr int kOffB = kOffA + (kMaxRank / kChunkK) * kAChunkBytes;  // 64 KB
 constexpr int kOffU = kOffB + kStages * kBChunkBytes;               // 112 KB
-constexpr int kOffS = kOffU + kEpiWarps * kUBoxBytes;               // 144 KB
+constexpr int kOffS = kOffU + 4 * kUQuarterBytes;                   // 144 KB
 constexpr int kOffMerge = kOffS + kEpiWarps * kSBoxBytes;           // 208 KB
 constexpr int kMergeBytes = 5 * 4 * kTileM * 4;                     // 10 KB
 constexpr int kOffRowBest = kOffMerge + kMergeBytes;                // [128 rows][4 groups] fp32
@@ -257,7 +263,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
   uint64_t* bar_empty = bars + 1 + kStages;       // [kStages] W2 chunk consumed
   uint64_t* bar_acc_full = bars + 1 + 2 * kStages;   // [2] accumulator ready
   uint64_t* bar_acc_empty = bar_acc_full + 2;        // [2] accumulator drained
-  uint64_t* bar_u = bar_acc_empty + 2;               // [kEpiWarps] U block loaded
+  uint64_t* bar_u = bar_acc_empty + 2;               // [4] quarter's U tile loaded, [4..7] read
   uint64_t* bar_drain = bar_u + kEpiWarps;           // MMA drain at exit
   uint32_t* tmem_slot = (uint32_t*)(bars + kNumBars);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
@@ -281,7 +287,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       mbar_init(&bar_acc_full[b], 1);
       mbar_init(&bar_acc_empty[b], kEpiWarps);
     }
-    for (int w = 0; w < kEpiWarps; ++w) mbar_init(&bar_u[w], 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&bar_u[q], 1);      // U tile of quarter q loaded
+      mbar_init(&bar_u[4 + q], 4);  // read by the quarter's four warps
+    }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -384,7 +393,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     const int row_local = quarter * 32 + lane;
     const int row = m_tile * kTileM + row_local;
     const bool row_ok = row < p.R;
-    uint8_t* ubox = smem + kOffU + warp * kUBoxBytes;
+    // The quarter's U tile: 32 rows x 128 columns as two 64-column boxes (128-byte rows,
+    // 128-byte swizzle), loaded by the quarter's column-group-0 warp, read by all four.
+    uint8_t* uq = smem + kOffU + quarter * kUQuarterBytes;
     uint8_t* sbox = smem + kOffS + warp * kSBoxBytes;
     const int row0 = m_tile * kTileM + quarter * 32;
     const int kpos = p.k - 1;
@@ -399,9 +410,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (slot == 0 && cgrp == 0 && row_ok) p.gthr_next[row] = 0u;
 
-    if (lane == 0 && n_units > 0) {
-      mbar_expect_tx(&bar_u[warp], kUBoxBytes);
-      tma_load_3d(ubox, &tmU, slot * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
+    if (cgrp == 0 && lane == 0 && n_units > 0) {
+      mbar_expect_tx(&bar_u[quarter], kUQuarterBytes);
+      tma_load_3d(uq, &tmU, slot * kTileN, kpos, row0, &bar_u[quarter]);
+      tma_load_3d(uq + kUBoxBytes, &tmU, slot * kTileN + 64, kpos, row0, &bar_u[quarter]);
     }
     // U loads of this warp issued so far and those waited for (equal on exit
     // unless a wait failed: the one in flight must land before the CTA exits).
@@ -572,19 +584,20 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       // The row's best key over all CTAs of this step so far, read early (L2).
       const uint32_t gkey = row_ok ? __ldcg(p.gthr_cur + row) : 0u;
 
-      // U block of this warp: row `lane`, 32 bf16 (64-byte rows, 64-byte swizzle).
+      // U of this warp: row `lane`, its 32 columns of the quarter's tile.
       // Waits are decided warp-wide; on a failed one the warp leaves the loop
       // (every epilogue warp still reaches the merge barrier below).
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_u[warp], u & 1, abort_flag, p.wait_budget)))
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_u[quarter], u & 1, abort_flag, p.wait_budget)))
         break;
       u_landed = u + 1;
       uint32_t upk[16];
       {
-        const uint32_t* rowp = (const uint32_t*)(ubox + lane * 64);
+        // this warp's 32 columns: chunks 4 (cgrp & 1) .. +3 of box cgrp >> 1, row `lane`
+        const uint8_t* rowp = uq + (cgrp >> 1) * kUBoxBytes + lane * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int pc = c ^ ((lane >> 1) & 3);
-          const uint4 q = *(const uint4*)(rowp + pc * 4);
+          const int pc = (4 * (cgrp & 1) + c) ^ (lane & 7);
+          const uint4 q = *(const uint4*)(rowp + pc * 16);
           upk[4 * c + 0] = q.x;
           upk[4 * c + 1] = q.y;
           upk[4 * c + 2] = q.z;
@@ -592,11 +605,18 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         }
       }
       __syncwarp();
-      if (u + 1 < n_units) {
+      if (lane == 0) mbar_arrive(&bar_u[4 + quarter]);
+      if (u + 1 < n_units && cgrp == 0) {
+        // the next tile may overwrite the buffer once all four warps have read it
+        const bool freed = __all_sync(0xffffffffu, mbar_wait(&bar_u[4 + quarter], u & 1, abort_flag,
+                                                               p.wait_budget));
+        if (!freed) break;
         if (lane == 0) {
           fence_proxy_async();
-          mbar_expect_tx(&bar_u[warp], kUBoxBytes);
-          tma_load_3d(ubox, &tmU, (n + p.slots) * kTileN + cgrp * 32, kpos, row0, &bar_u[warp]);
+          mbar_expect_tx(&bar_u[quarter], kUQuarterBytes);
+          tma_load_3d(uq, &tmU, (n + p.slots) * kTileN, kpos, row0, &bar_u[quarter]);
+          tma_load_3d(uq + kUBoxBytes, &tmU, (n + p.slots) * kTileN + 64, kpos, row0,
+                      &bar_u[quarter]);
         }
         u_issued = u + 2;
       }
@@ -746,7 +766,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       p.pindex[o] = bi;
     }
     if (lane == 0) {
-      if (u_issued > u_landed) mbar_drain(&bar_u[warp], (uint32_t)(u_issued - 1) & 1u, p.wait_budget);
+      if (cgrp == 0 && u_issued > u_landed)
+        mbar_drain(&bar_u[quarter], (uint32_t)(u_issued - 1) & 1u, p.wait_budget);
       bulk_wait0();
     }
   }
@@ -873,9 +894,9 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, 
   {
     const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)gamma, (cuuint64_t)R};
     const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)gamma * V * 2};
-    const cuuint32_t box[3] = {32, 1, 32};
+    const cuuint32_t box[3] = {64, 1, 32};
     if (!encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, U, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_64B))
+                CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
