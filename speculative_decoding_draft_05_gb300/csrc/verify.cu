@@ -404,7 +404,6 @@ struct KeyedPhilox {
 };
 
 constexpr int kDrawThreads = 256;
-constexpr int kDrawChunkGroups = 512;  // 32-id groups per draw CTA (16384 ids)
 
 // The residual row of the rejection draw, element by element.  With
 // a = z/T - LSE^t = ln p^t(v) and delta = ln p^t(v) - ln p^d(v) written as
@@ -425,47 +424,99 @@ __device__ __forceinline__ float residual_lw(float a, float delta) {
   return __fadd_rn(a, logf(-expm1f(-delta)));
 }
 
-// Log-mass of one 32-id group of the drawn row: log sum_v e^{lw(v)} over its
-// ids (the last group of a row may hold fewer: nv, a multiple of 8), with lw
-// = z/T (bonus draw, and the residual-free fallback) or the residual's
-// log-weight.  -inf when every weight of the group is zero.  The raw loads of
-// the group stay in registers and are unpacked twice (the maximum, then the
-// sum), so the group needs no array of its values.
+// max of two packed bf16 pairs, lane by lane (exact: a comparison).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// The raw loads of one 32-id group of a target row (the last group of a row may
+// hold fewer ids: nv, a multiple of 8; the missing ones read as -inf), and its
+// log-mass log sum_v e^{z_v / T}: the maximum first -- on packed bf16 pairs,
+// before any unpacking -- then the sum of exp on float pairs, one unpack per id.
+template <typename T> struct GroupZ;
+template <> struct GroupZ<__nv_bfloat16> {
+  static constexpr uint32_t kNegInf2 = 0xff80ff80u;  // two bf16 -inf
+  uint4 q[4];
+  __device__ __forceinline__ void load(const __nv_bfloat16* __restrict__ z, int g0, int nv) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      q[c] = 8 * c < nv ? __ldg(reinterpret_cast<const uint4*>(z) + g0 + c)
+                        : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+  }
+  __device__ __forceinline__ float log_mass(float invT) const {
+    const float L2E = 1.4426950408889634f;
+    uint32_t m4[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) m4[c] = bmax2(bmax2(q[c].x, q[c].y), bmax2(q[c].z, q[c].w));
+    const uint32_t m2 = bmax2(bmax2(m4[0], m4[1]), bmax2(m4[2], m4[3]));
+    const float mz = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xffff0000u));
+    if (mz == -INFINITY) return -INFINITY;
+    const float m = mz * invT;  // T > 0: the largest z/T is the largest z, scaled
+    const float2 k2 = make_float2(invT * L2E, invT * L2E), n2 = make_float2(-m * L2E, -m * L2E);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 e2 = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+        const float2 a2 = __ffma2_rn(e2, k2, n2);
+        acc = __fadd2_rn(acc, make_float2(ex2_approx(a2.x), ex2_approx(a2.y)));
+      }
+    }
+    return __fadd_rn(m, logf(acc.x + acc.y));
+  }
+};
+template <> struct GroupZ<float> {
+  float4 q[8];
+  __device__ __forceinline__ void load(const float* __restrict__ z, int g0, int nv) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      q[c] = 4 * c < nv ? __ldg(reinterpret_cast<const float4*>(z) + 2 * g0 + c)
+                        : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+  __device__ __forceinline__ float log_mass(float invT) const {
+    const float L2E = 1.4426950408889634f;
+    float mz = fmax3(q[0].x, q[0].y, q[0].z);
+    mz = fmax3(mz, q[0].w, q[1].x);
+    mz = fmax3(mz, q[1].y, q[1].z);
+    mz = fmaxf(mz, q[1].w);
+#pragma unroll
+    for (int c = 2; c < 8; ++c) mz = fmax3(fmax3(mz, q[c].x, q[c].y), q[c].z, q[c].w);
+    if (mz == -INFINITY) return -INFINITY;
+    const float m = mz * invT;
+    const float2 k2 = make_float2(invT * L2E, invT * L2E), n2 = make_float2(-m * L2E, -m * L2E);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float2 lo = __ffma2_rn(make_float2(q[c].x, q[c].y), k2, n2);
+      const float2 hi = __ffma2_rn(make_float2(q[c].z, q[c].w), k2, n2);
+      acc = __fadd2_rn(acc, make_float2(ex2_approx(lo.x), ex2_approx(lo.y)));
+      acc = __fadd2_rn(acc, make_float2(ex2_approx(hi.x), ex2_approx(hi.y)));
+    }
+    return __fadd_rn(m, logf(acc.x + acc.y));
+  }
+};
+
+// Log-mass of one 32-id group of the rejected row's residual: log sum_v of
+// e^a (1 - e^-delta) over the ids with delta > 0 (see residual_terms), -inf
+// when there is none.  Two halves of 16 ids, each scaled by its largest e^a
+// and merged online; the raw loads of a half are unpacked twice (the maximum,
+// then the sum), so the group needs no array of its values.
 template <typename T>
-__device__ __forceinline__ float group_log_mass(const T* __restrict__ z, const float* __restrict__ srow,
-                                                int v0, int nv, bool residual, float invT, float Lt,
-                                                float dL) {
+__device__ __forceinline__ float residual_group_log_mass(const T* __restrict__ z,
+                                                         const float* __restrict__ srow, int v0,
+                                                         int nv, float invT, float Lt, float dL) {
   const float L2E = 1.4426950408889634f;
   const int g0 = v0 >> 3;  // first 8-id chunk
-  if (!residual) {
-    Raw8<T> raw[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (8 * c < nv) raw[c].load(z, g0 + c);
-    float m = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (8 * c < nv) {
-        float e[8];
-        raw[c].unpack(e);
-        m = fmaxf(m, fmaxf(fmaxf(fmaxf(e[0], e[1]), fmaxf(e[2], e[3])),
-                           fmaxf(fmaxf(e[4], e[5]), fmaxf(e[6], e[7]))));
-      }
-    m *= invT;  // T > 0: the largest z/T is the largest z, scaled
-    float S = 0.0f;
-    const float nm = -m * L2E, k = invT * L2E;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (8 * c < nv) {
-        float e[8];
-        raw[c].unpack(e);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) S += ex2_approx(__fmaf_rn(e[i], k, nm));
-      }
-    return __fadd_rn(m, logf(S));
-  }
-  // Residual: weights e^a (1 - e^-delta) for delta > 0, scaled by the largest
-  // e^a among them; two halves of 16 ids (registers), online merged.
   float m = -INFINITY, S = 0.0f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -514,23 +565,27 @@ __device__ __forceinline__ float group_log_mass(const T* __restrict__ z, const f
   return (m == -INFINITY || !(S > 0.0f)) ? -INFINITY : __fadd_rn(m, logf(S));
 }
 
-// Stage 1 of the two-level draw over one chunk of 512 groups of the drawn row
-// (the rejected row's residual, or the bonus row's p^t): one group per thread
-// at a time.  A group's key is L_j + G(seed, r, row, RESAMPLE_GROUP, j); it can
-// beat the running best key b only if 1 - u_j < exp(L_j - b), tested as
-// fl(f + 1.001 exp(L_j - b)) >= 2 (f = 1 + (w >> 9) 2^-23), so the two
-// logarithms run only for candidates.  b is the best key any thread of the
-// CTA has reached so far (shared memory, raised with atomicMax in key_ord
-// form; a stale value is still a lower bound of the chunk's maximum).
-// Writes the chunk's (best group key, group index) partial; the emit kernel
-// merges the chunks and draws the token inside the winning group.
+// Stage 1 of the two-level draw over one chunk of 256 gpt groups of the drawn
+// row (the rejected row's residual, or the bonus row's p^t): each thread takes
+// gpt consecutive groups (4: they share one Philox quad, word j & 3 keying
+// group j; 1 when there are too few requests to fill the GPU otherwise), one
+// after another; for a bf16 bonus row the next group's loads are issued
+// before the current group is summed.  A group's key is
+// L_j + G(seed, r, row, RESAMPLE_GROUP, j); it can beat the running best key
+// b only if 1 - u_j < exp(L_j - b), tested as fl(f + 1.001 exp(L_j - b)) >= 2
+// (f = 1 + (w >> 9) 2^-23), so the two logarithms run only for candidates.  b
+// is the best key any thread of the CTA has reached so far (shared memory,
+// raised with atomicMax in key_ord form; a stale value is still a lower bound
+// of the chunk's maximum).  Writes the chunk's (best group key, group index)
+// partial; the emit kernel merges the chunks and draws the token inside the
+// winning group.
 template <typename T>
 __global__ void __launch_bounds__(kDrawThreads, 4)
 verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scores,
                    const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
                    float invT, const PhiloxKeys keys, const float* __restrict__ lse_t_ws,
                    const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks,
-                   ZRows zr) {
+                   int gpt, ZRows zr) {
   // Launched as a programmatic dependent of the previous kernel: wait for it
   // before anything else, then let the next kernel's launch begin.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -558,18 +613,11 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
     dL = __fsub_rn(Lt, lse[(size_t)r * gamma + (row - 1)]);
   }
   const int n_groups = (V + kGroup - 1) / kGroup;
-  const int j1 = min(n_groups, (chunk + 1) * kDrawChunkGroups);
   const float L2E = 1.4426950408889634f;
-  const KeyedPhilox rng(keys, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE_GROUP);
   float best = -INFINITY;
   int bj = 0x7fffffff;
-  for (int j = chunk * kDrawChunkGroups + threadIdx.x; j < j1; j += kDrawThreads) {
-    const int v0 = j * kGroup;
-    const float Lg = group_log_mass(z, srow, v0, min(kGroup, V - v0), residual, invT, Lt, dL);
-    if (Lg == -INFINITY) continue;
-    const uint4 q = rng.quad(keys, (uint32_t)j >> 2);
-    const int sub = j & 3;
-    const uint32_t w = sub == 0 ? q.x : sub == 1 ? q.y : sub == 2 ? q.z : q.w;
+  auto consider = [&](float Lg, int j, uint32_t w) {
+    if (Lg == -INFINITY) return;
     const float thr = ord_key(*cta_best);
     const bool cand = thr == -INFINITY ||
                       __uint_as_float(__funnelshift_r(w, 0x7Fu, 9)) +
@@ -581,6 +629,44 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
         bj = j;
       }
       if (best > thr && best < INFINITY) atomicMax(&s_best, key_ord(best));
+    }
+  };
+  const int j0 = (chunk * kDrawThreads + threadIdx.x) * gpt;  // gpt = 1 or 4: 4 | j0
+  if (j0 < n_groups) {
+    const KeyedPhilox rng(keys, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE_GROUP);
+    const uint4 q = rng.quad(keys, (uint32_t)j0 >> 2);
+    auto word = [&](int g) {
+      const int t = (j0 + g) & 3;
+      return t == 0 ? q.x : t == 1 ? q.y : t == 2 ? q.z : q.w;
+    };
+    const int ng = min(gpt, n_groups - j0);
+    if (!residual && sizeof(T) == 2) {
+      GroupZ<T> cur, nxt;
+      cur.load(z, j0 * (kGroup / 8), min(kGroup, V - j0 * kGroup));
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (g >= ng) break;
+        const int j = j0 + g;
+        if (g + 1 < ng) nxt.load(z, (j + 1) * (kGroup / 8), min(kGroup, V - (j + 1) * kGroup));
+        consider(cur.log_mass(invT), j, word(g));
+        cur = nxt;
+      }
+    } else if (!residual) {  // fp32 rows: 128 bytes a group, no second group in flight
+#pragma unroll 1
+      for (int g = 0; g < ng; ++g) {
+        const int j = j0 + g;
+        GroupZ<T> cur;
+        cur.load(z, j * (kGroup / 8), min(kGroup, V - j * kGroup));
+        consider(cur.log_mass(invT), j, word(g));
+      }
+    } else {
+#pragma unroll 1
+      for (int g = 0; g < ng; ++g) {
+        const int j = j0 + g;
+        consider(residual_group_log_mass(z, srow, j * kGroup, min(kGroup, V - j * kGroup), invT, Lt,
+                                         dL),
+                 j, word(g));
+      }
     }
   }
   block_argmax<kDrawThreads / 32>(best, bj, rk, ri);
@@ -637,8 +723,9 @@ verify_emit_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
     gj = 0x7fffffff;
     for (int j = threadIdx.x; j < n_groups; j += kVerifyThreads) {
       const int v0 = j * kGroup;
-      const float Lg = group_log_mass(z, (const float*)nullptr, v0, min(kGroup, V - v0), false, invT,
-                                      0.0f, 0.0f);
+      GroupZ<T> gz;
+      gz.load(z, v0 >> 3, min(kGroup, V - v0));
+      const float Lg = gz.log_mass(invT);
       const float key = __fadd_rn(Lg, gumbel(rng.word((uint32_t)j)));
       if (better(key, j, best, gj)) {
         best = key;
@@ -743,10 +830,21 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
                         zr);
 }
 
-int verify_draw_chunks(int V) {
-  const int n_groups = (V + kGroup - 1) / kGroup;
-  return (n_groups + kDrawChunkGroups - 1) / kDrawChunkGroups;
+// Groups per thread of the draw: 4 when four-group chunks still give at least
+// two waves of draw CTAs (four per SM), else 1.
+static int draw_gpt(int R, int V) {
+  const long long n_groups = (V + kGroup - 1) / kGroup;
+  const long long chunks4 = (n_groups + 4 * kDrawThreads - 1) / (4 * kDrawThreads);
+  return (long long)R * chunks4 >= 2LL * 4 * verify_sm_count() ? 4 : 1;
 }
+
+static int draw_chunks(int V, int gpt) {
+  const int n_groups = (V + kGroup - 1) / kGroup;
+  return (n_groups + gpt * kDrawThreads - 1) / (gpt * kDrawThreads);
+}
+
+// Partials per request the workspace holds: the larger count (one group per thread).
+int verify_draw_chunks(int V) { return draw_chunks(V, 1); }
 
 cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
                                  const void* Z, int dtype, const int32_t* ell, int R, int gamma,
@@ -754,13 +852,14 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
                                  const int* acc_ws, float2* partials, int32_t* n_acc,
                                  int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
                                  ZRows zr, cudaStream_t s) {
-  const int chunks = verify_draw_chunks(V);
+  const int gpt = draw_gpt(R, V);
+  const int chunks = draw_chunks(V, gpt);
   dim3 grid(chunks, R);
   cudaError_t e;
   if (dtype == DSPARK_BF16) {
     e = launch_chained(verify_draw_kernel<__nv_bfloat16>, grid, dim3(kDrawThreads), s, lse, scores,
                        (const __nv_bfloat16*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws,
-                       acc_ws, partials, chunks, zr);
+                       acc_ws, partials, chunks, gpt, zr);
     if (e != cudaSuccess) return e;
     return launch_chained(verify_emit_kernel<__nv_bfloat16>, dim3(R), dim3(kVerifyThreads), s, x,
                           lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws,
@@ -769,7 +868,7 @@ cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float
   }
   e = launch_chained(verify_draw_kernel<float>, grid, dim3(kDrawThreads), s, lse, scores,
                      (const float*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
-                     partials, chunks, zr);
+                     partials, chunks, gpt, zr);
   if (e != cudaSuccess) return e;
   return launch_chained(verify_emit_kernel<float>, dim3(R), dim3(kVerifyThreads), s, x, lse, scores,
                         (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws,
