@@ -382,7 +382,7 @@ def verify_rows_bytes(w: workload.Workload, rows: int) -> int:
 
 
 def verify_draw_bytes(w: workload.Workload, residual_rows: int) -> int:
-    """Algorithmic bytes of the draw (+ emit): one target row per request, plus the
+    """Algorithmic bytes of the draw (stage 1): one target row per request, plus the
     draft scores of the rows drawn from a residual."""
     e = 4 if w.dtype == "f32" else 2
     return w.R * w.V * e + residual_rows * w.V * 4
@@ -403,8 +403,11 @@ def kernel_rooflines(w, prof, rows_per_round: int, residual_per_round: float, hb
                          achieved_gbs=nbytes / t / 1e9, frac=nbytes / t / 1e9 / hbm_peak, bound="hbm")
 
     entry("verify_rows", verify_rows_bytes(w, rows_per_round), {"rows": rows_per_round})
-    entry("verify_finish", verify_draw_bytes(w, residual_per_round),
+    entry("verify_draw", verify_draw_bytes(w, residual_per_round),
           {"residual_rows": residual_per_round, "bonus_rows": w.R - residual_per_round})
+    ms, n = prof.get("verify_emit", (0.0, 0))
+    if n > 0:  # one CTA per request: latency-bound, reported as time only
+        out["verify_emit"] = {"us_per_launch": ms / n * 1e3, "bound": "latency"}
     if rnn:
         # h_{k-1} read, h_k written (fp32), the A rows written (bf16), Wh, Q_k
         e = 2

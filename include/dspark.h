@@ -380,9 +380,10 @@ enum {
   DSPARK_KERNEL_DRAFT_COMBINE = 2,  /* per-row combine + next gather (gamma launches) */
   DSPARK_KERNEL_SCHEDULE = 3,
   DSPARK_KERNEL_VERIFY_ROWS = 4,
-  DSPARK_KERNEL_VERIFY_FINISH = 5,
+  DSPARK_KERNEL_VERIFY_DRAW = 5,    /* stage 1 of the residual / bonus draw */
   DSPARK_KERNEL_RNN_STATE = 6,      /* RNN head: state update (gamma launches) */
-  DSPARK_KERNEL_KINDS = 7
+  DSPARK_KERNEL_VERIFY_EMIT = 7,    /* stage 2 of the draw, emitted tokens */
+  DSPARK_KERNEL_KINDS = 8
 };
 int dspark_profile_start(void);
 int dspark_profile_stop(double* ms_by_kind, int* launches_by_kind, int* timed_launches);

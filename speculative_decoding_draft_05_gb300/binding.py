@@ -350,8 +350,8 @@ def dspark_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     return int(out.value)
 
 
-KERNEL_KINDS = ["prepare", "draft_tile", "draft_combine", "schedule", "verify_rows", "verify_finish",
-                "rnn_state"]
+KERNEL_KINDS = ["prepare", "draft_tile", "draft_combine", "schedule", "verify_rows", "verify_draw",
+                "rnn_state", "verify_emit"]
 
 
 def dspark_stream_probe(inp, out, stream=None) -> None:

@@ -433,9 +433,14 @@ static int verify_enqueue(const int32_t* x, const float* logp, const float* lse,
                          status, zr, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, what);
-  prof_begin(kKindVerifyFinish, s);
-  e = launch_verify_finish(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                           partials, n_acc, tokens, n_emit, cstar, lse_t, zr, s);
+  prof_begin(kKindVerifyDraw, s);
+  e = launch_verify_draw(lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
+                         partials, status, zr, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  prof_begin(kKindVerifyEmit, s);
+  e = launch_verify_emit(x, lse, scores, Z, dtype, ell, R, gamma, V, invT, seed, lse_t_ws, acc_ws,
+                         partials, n_acc, tokens, n_emit, cstar, lse_t, zr, s);
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return DSPARK_OK;

@@ -117,12 +117,16 @@ cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float*
 
 // The drawn token: verify_draw over vocab chunks, then verify_emit per request.
 int verify_draw_chunks(int V);
-cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
-                                 const void* Z, int dtype, const int32_t* ell, int R, int gamma,
-                                 int V, float invT, uint64_t seed, const float* lse_t_ws,
-                                 const int* acc_ws, float2* partials, int32_t* n_acc,
-                                 int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
-                                 ZRows zr, cudaStream_t s);
+cudaError_t launch_verify_draw(const float* lse, const float* scores, const void* Z, int dtype,
+                               const int32_t* ell, int R, int gamma, int V, float invT,
+                               uint64_t seed, const float* lse_t_ws, const int* acc_ws,
+                               float2* partials, int* status, ZRows zr, cudaStream_t s);
+cudaError_t launch_verify_emit(const int32_t* x, const float* lse, const float* scores,
+                               const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
+                               float invT, uint64_t seed, const float* lse_t_ws, const int* acc_ws,
+                               const float2* partials, int32_t* n_acc, int32_t* tokens,
+                               int32_t* n_emit, float* cstar, float* lse_t, ZRows zr,
+                               cudaStream_t s);
 
 // Sequential temperature scaling: workspace (byte offsets, 256-aligned) of the
 // chosen grid index, the [G, M] fixed-point bins, the running survival [N]
@@ -147,9 +151,10 @@ enum KernelKind {
   kKindDraftCombine = 2,
   kKindSchedule = 3,  // both scheduler launches
   kKindVerifyRows = 4,
-  kKindVerifyFinish = 5,
-  kKindRnnState = 6,  // RNN head: state update before each draft step
-  kKindCount = 7
+  kKindVerifyDraw = 5,  // stage 1 of the residual / bonus draw
+  kKindRnnState = 6,    // RNN head: state update before each draft step
+  kKindVerifyEmit = 7,  // stage 2 of the draw and the emitted tokens
+  kKindCount = 8
 };
 
 }  // namespace dspark

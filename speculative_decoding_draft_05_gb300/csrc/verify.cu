@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "kernels.h"
 
 namespace dspark {
@@ -424,6 +425,27 @@ __device__ __forceinline__ float residual_lw(float a, float delta) {
   return __fadd_rn(a, logf(-expm1f(-delta)));
 }
 
+// One contiguous global -> shared copy by the bulk-copy engine, completing on
+// `bar` (16-byte aligned addresses, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bounded wait on a warp's own copy barrier: false after `budget` SM clocks.
+__device__ __forceinline__ bool bar_wait_bounded(uint64_t* bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > budget) return false;
+  return true;
+}
+
+constexpr int kDrawWarpBytes = 32 * 4 * 32 * 2;  // a warp's four groups per lane of bf16 Z: 8 KB
+constexpr int kDrawSmemBytes = (kDrawThreads / 32) * kDrawWarpBytes + (kDrawThreads / 32) * 8;
+
 // max of two packed bf16 pairs, lane by lane (exact: a comparison).
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -451,6 +473,16 @@ template <> struct GroupZ<__nv_bfloat16> {
       q[c] = 8 * c < nv ? __ldg(reinterpret_cast<const uint4*>(z) + g0 + c)
                         : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
   }
+  // From a shared-memory copy of the group: piece pc is read at step c = pc - rot
+  // (mod 4), so that lanes spread over the banks; pieces past nv read as -inf.
+  __device__ __forceinline__ void load_shared(const uint8_t* g, int nv, int rot) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int pc = (c + rot) & 3;
+      q[c] = 8 * pc < nv ? *(const uint4*)(g + pc * 16)
+                         : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+    }
+  }
   __device__ __forceinline__ float log_mass(float invT) const {
     const float L2E = 1.4426950408889634f;
     uint32_t m4[4];
@@ -477,6 +509,7 @@ template <> struct GroupZ<__nv_bfloat16> {
 };
 template <> struct GroupZ<float> {
   float4 q[8];
+  __device__ __forceinline__ void load_shared(const uint8_t*, int, int) {}  // bf16 rows only
   __device__ __forceinline__ void load(const float* __restrict__ z, int g0, int nv) {
 #pragma unroll
     for (int c = 0; c < 8; ++c)
@@ -569,8 +602,10 @@ __device__ __forceinline__ float residual_group_log_mass(const T* __restrict__ z
 // row (the rejected row's residual, or the bonus row's p^t): each thread takes
 // gpt consecutive groups (4: they share one Philox quad, word j & 3 keying
 // group j; 1 when there are too few requests to fill the GPU otherwise), one
-// after another; for a bf16 bonus row the next group's loads are issued
-// before the current group is summed.  A group's key is
+// after another.  For a bf16 bonus row at gpt = 4 each warp first brings its
+// 8 KB of Z into shared memory with one bulk copy (dynamic shared memory of
+// kDrawSmemBytes), so that the loads are whole-line requests rather than 32
+// scattered 16-byte pieces per instruction.  A group's key is
 // L_j + G(seed, r, row, RESAMPLE_GROUP, j); it can beat the running best key
 // b only if 1 - u_j < exp(L_j - b), tested as fl(f + 1.001 exp(L_j - b)) >= 2
 // (f = 1 + (w >> 9) 2^-23), so the two logarithms run only for candidates.  b
@@ -585,7 +620,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
                    const T* __restrict__ Z, const int32_t* __restrict__ ell, int gamma, int V,
                    float invT, const PhiloxKeys keys, const float* __restrict__ lse_t_ws,
                    const int* __restrict__ acc_ws, float2* __restrict__ partials, int n_chunks,
-                   int gpt, ZRows zr) {
+                   int gpt, int* __restrict__ status, ZRows zr) {
   // Launched as a programmatic dependent of the previous kernel: wait for it
   // before anything else, then let the next kernel's launch begin.
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -632,6 +667,29 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
     }
   };
   const int j0 = (chunk * kDrawThreads + threadIdx.x) * gpt;  // gpt = 1 or 4: 4 | j0
+  // bf16 bonus rows at four groups per thread: the warp's 8 KB of Z (four
+  // groups per lane) come by one bulk copy into shared memory, issued by lane 0
+  // for the whole warp (the warp's ids from s0 up to the row's end).
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long s0 = (long long)(j0 - gpt * lane) * kGroup;  // the warp's first id
+  const bool staged = sizeof(T) == 2 && !residual && gpt == 4;
+  extern __shared__ __align__(128) uint8_t draw_smem[];
+  uint8_t* wbuf = draw_smem + warp * kDrawWarpBytes;
+  if (staged && s0 < V) {
+    uint64_t* wbar = (uint64_t*)(draw_smem + (kDrawThreads / 32) * kDrawWarpBytes) + warp;
+    if (lane == 0) {
+      mbar_init(wbar, 1);
+      fence_barrier_init();
+      const uint32_t bytes = (uint32_t)min((long long)kDrawWarpBytes, (V - s0) * 2);
+      mbar_expect_tx(wbar, bytes);
+      bulk_load(wbuf, z + s0, bytes, wbar);
+    }
+    __syncwarp();
+    if (!bar_wait_bounded(wbar, 0, kWaitBudget)) {
+      if (lane == 0) flag_status(status, DSPARK_DEV_TIMEOUT);
+      mbar_drain(wbar, 0, kWaitBudget);
+    }
+  }
   if (j0 < n_groups) {
     const KeyedPhilox rng(keys, (uint32_t)r, (uint32_t)row, DSPARK_PURPOSE_RESAMPLE_GROUP);
     const uint4 q = rng.quad(keys, (uint32_t)j0 >> 2);
@@ -640,18 +698,21 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
       return t == 0 ? q.x : t == 1 ? q.y : t == 2 ? q.z : q.w;
     };
     const int ng = min(gpt, n_groups - j0);
-    if (!residual && sizeof(T) == 2) {
-      GroupZ<T> cur, nxt;
-      cur.load(z, j0 * (kGroup / 8), min(kGroup, V - j0 * kGroup));
+    if (staged) {
+      // Lane l takes its groups in the order (g + l / 4) % 4 and each group's
+      // pieces from l % 4 on: the pieces a step reads fall in eight distinct
+      // 16-byte bank groups across the warp.
+      const uint8_t* tbuf = wbuf + lane * (4 * kGroup * 2);
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        if (g >= ng) break;
-        const int j = j0 + g;
-        if (g + 1 < ng) nxt.load(z, (j + 1) * (kGroup / 8), min(kGroup, V - (j + 1) * kGroup));
-        consider(cur.log_mass(invT), j, word(g));
-        cur = nxt;
+        const int G = (g + (lane >> 2)) & 3;
+        if (G >= ng) continue;
+        const int j = j0 + G;
+        GroupZ<T> gz;
+        gz.load_shared(tbuf + G * kGroup * 2, min(kGroup, V - j * kGroup), lane);
+        consider(gz.log_mass(invT), j, word(G));
       }
-    } else if (!residual) {  // fp32 rows: 128 bytes a group, no second group in flight
+    } else if (!residual) {  // loads straight from global memory
 #pragma unroll 1
       for (int g = 0; g < ng; ++g) {
         const int j = j0 + g;
@@ -794,11 +855,12 @@ int verify_sm_count() {
 // Launch `kernel` as a programmatic dependent of the stream's previous kernel
 // (the kernel waits for it with griddepcontrol.wait at entry).
 template <typename... Params, typename... Args>
-cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t s,
-                           Args... args) {
+cudaError_t launch_chained_smem(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -806,6 +868,12 @@ cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, cud
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t s,
+                           Args... args) {
+  return launch_chained_smem(kernel, grid, block, 0, s, args...);
 }
 
 cudaError_t launch_verify_rows(const int32_t* x, const float* logp, const float* lse,
@@ -846,33 +914,49 @@ static int draw_chunks(int V, int gpt) {
 // Partials per request the workspace holds: the larger count (one group per thread).
 int verify_draw_chunks(int V) { return draw_chunks(V, 1); }
 
-cudaError_t launch_verify_finish(const int32_t* x, const float* lse, const float* scores,
-                                 const void* Z, int dtype, const int32_t* ell, int R, int gamma,
-                                 int V, float invT, uint64_t seed, const float* lse_t_ws,
-                                 const int* acc_ws, float2* partials, int32_t* n_acc,
-                                 int32_t* tokens, int32_t* n_emit, float* cstar, float* lse_t,
-                                 ZRows zr, cudaStream_t s) {
+// Draw CTAs per request of this launch (both launches below must agree).
+int verify_draw_launch_chunks(int R, int V) { return draw_chunks(V, draw_gpt(R, V)); }
+
+cudaError_t launch_verify_draw(const float* lse, const float* scores, const void* Z, int dtype,
+                               const int32_t* ell, int R, int gamma, int V, float invT,
+                               uint64_t seed, const float* lse_t_ws, const int* acc_ws,
+                               float2* partials, int* status, ZRows zr, cudaStream_t s) {
   const int gpt = draw_gpt(R, V);
   const int chunks = draw_chunks(V, gpt);
   dim3 grid(chunks, R);
-  cudaError_t e;
   if (dtype == DSPARK_BF16) {
-    e = launch_chained(verify_draw_kernel<__nv_bfloat16>, grid, dim3(kDrawThreads), s, lse, scores,
-                       (const __nv_bfloat16*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws,
-                       acc_ws, partials, chunks, gpt, zr);
-    if (e != cudaSuccess) return e;
+    static bool smem_set = false;  // the staged bonus draw's shared memory (> 48 KB: opt in)
+    if (!smem_set) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          verify_draw_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          kDrawSmemBytes);
+      if (e != cudaSuccess) return e;
+      smem_set = true;
+    }
+    return launch_chained_smem(verify_draw_kernel<__nv_bfloat16>, grid, dim3(kDrawThreads),
+                               gpt == 4 ? (size_t)kDrawSmemBytes : 0, s, lse, scores,
+                               (const __nv_bfloat16*)Z, ell, gamma, V, invT, philox_keys(seed),
+                               lse_t_ws, acc_ws, partials, chunks, gpt, status, zr);
+  }
+  return launch_chained(verify_draw_kernel<float>, grid, dim3(kDrawThreads), s, lse, scores,
+                        (const float*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
+                        partials, chunks, gpt, status, zr);
+}
+
+cudaError_t launch_verify_emit(const int32_t* x, const float* lse, const float* scores,
+                               const void* Z, int dtype, const int32_t* ell, int R, int gamma, int V,
+                               float invT, uint64_t seed, const float* lse_t_ws, const int* acc_ws,
+                               const float2* partials, int32_t* n_acc, int32_t* tokens,
+                               int32_t* n_emit, float* cstar, float* lse_t, ZRows zr,
+                               cudaStream_t s) {
+  const int chunks = verify_draw_launch_chunks(R, V);
+  if (dtype == DSPARK_BF16)
     return launch_chained(verify_emit_kernel<__nv_bfloat16>, dim3(R), dim3(kVerifyThreads), s, x,
                           lse, scores, (const __nv_bfloat16*)Z, ell, gamma, V, invT, seed, lse_t_ws,
-                          acc_ws, (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t,
-                          zr);
-  }
-  e = launch_chained(verify_draw_kernel<float>, grid, dim3(kDrawThreads), s, lse, scores,
-                     (const float*)Z, ell, gamma, V, invT, philox_keys(seed), lse_t_ws, acc_ws,
-                     partials, chunks, gpt, zr);
-  if (e != cudaSuccess) return e;
+                          acc_ws, partials, chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
   return launch_chained(verify_emit_kernel<float>, dim3(R), dim3(kVerifyThreads), s, x, lse, scores,
-                        (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws,
-                        (const float2*)partials, chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
+                        (const float*)Z, ell, gamma, V, invT, seed, lse_t_ws, acc_ws, partials,
+                        chunks, n_acc, tokens, n_emit, cstar, lse_t, zr);
 }
 
 }  // namespace dspark

@@ -53,10 +53,11 @@ def test_our_arm_line():
     assert d["gpu_launches"] > 0
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     kr = d["kernels_roofline"]
-    for k in ("verify_rows", "verify_finish"):  # full blocks at this workload: both run
+    for k in ("verify_rows", "verify_draw"):  # full blocks at this workload: both run
         assert kr[k]["bytes_per_launch"] > 0 and kr[k]["us_per_launch"] > 0
         assert abs(kr[k]["frac"] - kr[k]["achieved_gbs"] / rf["peak"]) < 1e-9
     assert kr["verify_rows"]["rows"] == 8 * 4
+    assert kr["verify_emit"]["us_per_launch"] > 0
     vp = d["verify_rows_probe"]
     assert vp["requests"] == 8 and vp["rows"] == 32 and vp["bytes_per_launch"] == 32 * 151936 * 6
     assert vp["us_per_launch"] > 0 and vp["frac"] > 0
