@@ -108,6 +108,37 @@ def test_verify_parity_on_oracle_draft(R, gamma, V):
         assert ov["n_acc"].sum() > 0 and (ov["n_acc"] < ell).any()  # both outcomes exercised
 
 
+@pytest.mark.parametrize("R,V", [(1300, 1000), (700, 40008)], ids=["r1300_v1000", "r700_v40008"])
+def test_verify_draw_four_groups_per_thread(R, V):
+    # Enough requests that the draw takes four 32-id groups per thread (and, on
+    # bonus rows, stages each warp's bf16 target rows in shared memory with one
+    # bulk copy), with V % 32 = 8: the last group of a row holds 8 ids and the
+    # last warp's copy is short.  gamma = 1 and a random schedule in {0, 1} mix
+    # bonus draws from row 1 and row 2 with residual draws from row 1.
+    w = QWEN.resized(name="draw_gpt4", R=R, gamma=1, V=V, r=64)
+    seed = 11
+    inp = workload.generate(w, seed=seed, device="cpu")
+    W1, W2 = f64(inp["W1"]), f64(inp["W2"])
+    od = oracle.draft(f64(inp["U"]), W1, W2, inp["x0"].numpy(), w.T, seed)
+    bias = oracle_target_bias(W1, W2, inp["x0"].numpy(), od["x"])
+    Z = workload.target_logits(w, inp["U"], seed, bias_rows=lambda i: torch.from_numpy(bias[i]))
+    ell = np.random.default_rng(1).integers(0, 2, size=w.R).astype(np.int32)
+    ov = oracle.verify(od["x"], od["logp"], od["lse"], od["scores"], f64(Z), ell, w.T, seed)
+    dev = torch.device("cuda")
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    gv = dspark.dspark_verify(t(od["x"], torch.int32), t(od["logp"], torch.float32),
+                              t(od["lse"], torch.float32), t(od["scores"], torch.float32), Z.to(dev),
+                              t(ell, torch.int32), w.T, seed)
+    torch.cuda.synchronize()
+    assert dspark.dspark_read_device_status(gv["workspace"]) == 0
+    gv = {k: v.cpu().numpy() for k, v in gv.items() if isinstance(v, torch.Tensor) and k != "workspace"}
+    ex = compare_verify(gv, ov, ell, w.dtype)
+    assert len(ex) <= max(1, R // 200), ex
+    # both draws exercised (a short last group read past the copied bytes
+    # would carry garbage mass and win stage 1 far more often than the oracle)
+    assert (ov["n_acc"] < ell).any() and (ov["n_acc"] == ell).any()
+
+
 @pytest.mark.parametrize("name", workload.ORDER)
 def test_schedule_parity_full_size(name):
     w = W[name]
