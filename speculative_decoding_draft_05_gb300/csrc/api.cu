@@ -36,8 +36,8 @@ DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype)
   w.index = align256(w.stats + (size_t)R * tiles * sizeof(float4));
   w.stats2 = align256(w.index + (size_t)R * tiles * sizeof(int));
   w.index2 = align256(w.stats2 + (size_t)R * tiles * sizeof(float4));
-  w.gthr = align256(w.index2 + (size_t)R * tiles * sizeof(int));  // uint32 [2, R]
-  w.w2t = align256(w.gthr + 2 * (size_t)R * sizeof(uint32_t));     // bf16 W2^T [V, r]
+  w.gbest = align256(w.index2 + (size_t)R * tiles * sizeof(int));  // uint64 [3, R]
+  w.w2t = align256(w.gbest + 3 * (size_t)R * sizeof(unsigned long long));  // bf16 W2^T [V, r]
   w.total = align256(w.w2t + (dtype == DSPARK_BF16 ? (size_t)V * r * 2 : 0));
   return w;
 }
@@ -167,13 +167,13 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
     DraftTcPlan plan;
     e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
     if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
-    uint32_t* gthr = (uint32_t*)(ws + L.gthr);
-    e = cudaMemsetAsync(gthr, 0, 2 * (size_t)R * sizeof(uint32_t), s);
+    unsigned long long* gbest = (unsigned long long*)(ws + L.gbest);
+    e = cudaMemsetAsync(gbest, 0, 3 * (size_t)R * sizeof(unsigned long long), s);
     if (e != cudaSuccess) return cuda_fail(e, "draft key reset");
     const DraftPartials buf[2] = {p, p2};
     for (int k = 1; k <= gamma; ++k) {
       prof_begin(kKindDraftTile, s);
-      e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], gthr, x,
+      e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], gbest, x,
                                logp, lse, status, s);
       prof_end(s);
       if (e != cudaSuccess) return cuda_fail(e, "draft_step");
@@ -261,8 +261,8 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
   DraftTcPlan plan;
   e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
   if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
-  uint32_t* gthr = (uint32_t*)(ws + L.gthr);
-  e = cudaMemsetAsync(gthr, 0, 2 * (size_t)R * sizeof(uint32_t), s);
+  unsigned long long* gbest = (unsigned long long*)(ws + L.gbest);
+  e = cudaMemsetAsync(gbest, 0, 3 * (size_t)R * sizeof(unsigned long long), s);
   if (e != cudaSuccess) return cuda_fail(e, "draft key reset");
   const DraftPartials buf[2] = {p, p2};
   for (int k = 1; k <= gamma; ++k) {
@@ -273,7 +273,7 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "rnn_state");
     prof_begin(kKindDraftTile, s);
-    e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], gthr, x,
+    e = launch_draft_step_tc(plan, k, invT, seed, x0, W1, buf[(k + 1) & 1], buf[k & 1], gbest, x,
                              logp, lse, status, s, A);
     prof_end(s);
     if (e != cudaSuccess) return cuda_fail(e, "draft_step");
@@ -617,14 +617,14 @@ int dspark_selftest_draft_timeout(const void* U, const void* W1, const void* W2,
   const int n_parts = draft_tc_parts(R, V);
   DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index), n_parts};
   DraftPartials p2{(float4*)(ws + L.stats2), (int*)(ws + L.index2), n_parts};
-  uint32_t* gthr = (uint32_t*)(ws + L.gthr);
+  unsigned long long* gbest = (unsigned long long*)(ws + L.gbest);
   cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(gthr, 0, 2 * (size_t)R * sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(gbest, 0, 3 * (size_t)R * sizeof(unsigned long long), s);
   if (e != cudaSuccess) return cuda_fail(e, "selftest reset");
   DraftTcPlan plan;
   e = prepare_draft_tc(&plan, U, ws + L.w2t, R, gamma, V, r, scores);
   if (e != cudaSuccess) return cuda_fail(e, "selftest tensor maps");
-  e = launch_draft_step_tc(plan, 1, 1.0f, 0, x0, W1, p2, p, gthr, x, logp, lse, status, s, nullptr,
+  e = launch_draft_step_tc(plan, 1, 1.0f, 0, x0, W1, p2, p, gbest, x, logp, lse, status, s, nullptr,
                            wait_cycles, true);
   if (e != cudaSuccess) return cuda_fail(e, "selftest draft_step");
   return DSPARK_OK;

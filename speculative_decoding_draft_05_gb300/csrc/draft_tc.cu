@@ -84,7 +84,8 @@ constexpr int kOffS = kOffU + 4 * kUQuarterBytes;                   // 144 KB
 constexpr int kOffMerge = kOffS + kEpiWarps * kSBoxBytes;           // 208 KB
 constexpr int kMergeBytes = 5 * 4 * kTileM * 4;                     // 10 KB
 constexpr int kOffRowBest = kOffMerge + kMergeBytes;                // [128 rows][4 groups] fp32
-constexpr int kOffBar = kOffRowBest + kTileM * 4 * 4;
+constexpr int kOffDrawn = kOffRowBest + kTileM * 4 * 4;  // [128] x_{k-1}, then [128] its score
+constexpr int kOffBar = kOffDrawn + kTileM * 8;
 constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + kEpiWarps + 1;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + slack for 1024 alignment
 
@@ -239,9 +240,14 @@ struct Params {
   const int* prev_index;
   float4* pstats;                // this step's partials
   int* pindex;
-  uint32_t* gthr_cur;            // [R] best key per row reached by any CTA of this step (key_ord)
-  uint32_t* gthr_next;           // [R] zeroed here for step k+1
-  int32_t* x;                    // step k-1 outputs, written by the slot-0 CTAs
+  // [R] per row, the best (group key, group) any CTA of a step has reached,
+  // packed as key_ord(key) << 32 | ~group (so that the u64 maximum takes the
+  // larger key, then the smaller group): step k-1's (read by the prologue),
+  // this step's (raised with atomicMax), and step k+1's (zeroed here).
+  const unsigned long long* gbest_prev;
+  unsigned long long* gbest_cur;
+  unsigned long long* gbest_next;
+  int32_t* x;                    // step k-1 outputs: each row by one CTA of its row tile
   float* logp;
   float* lse;
   int* status;
@@ -408,7 +414,7 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     // Everything below reads or writes what the previous step (launched as this
     // grid's programmatic primary) wrote or reads: wait for its completion.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (slot == 0 && cgrp == 0 && row_ok) p.gthr_next[row] = 0u;
+    if (slot == 0 && cgrp == 0 && row_ok) p.gbest_next[row] = 0ull;
 
     if (cgrp == 0 && lane == 0 && n_units > 0) {
       mbar_expect_tx(&bar_u[quarter], kUQuarterBytes);
@@ -437,44 +443,13 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         xps[i] = arow < p.R ? p.x0[arow] : 0;
       }
     } else {
-      constexpr int kMergeBatch = 5;
+      // The row's drawn group of step k-1: the packed best that step's CTAs
+      // raised (the larger key, ties to the smaller group).
       const int sub = lane & 3;
       const int arow = m_tile * kTileM + warp * 8 + (lane >> 2);
       const bool ok_row = arow < p.R;
-      float m = -INFINITY, S = 0.0f, key = -INFINITY;
-      int gj = 0x7fffffff;
-      for (int t0 = sub; t0 < p.n_parts; t0 += 4 * kMergeBatch) {
-        float4 q[kMergeBatch];
-        int qi[kMergeBatch];
-#pragma unroll
-        for (int b = 0; b < kMergeBatch; ++b) {
-          const int t = t0 + 4 * b;
-          const bool ld = ok_row && t < p.n_parts;
-          q[b] = ld ? p.prev_stats[(size_t)arow * p.n_parts + t]
-                    : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-          qi[b] = ld ? p.prev_index[(size_t)arow * p.n_parts + t] : 0x7fffffff;
-        }
-#pragma unroll
-        for (int b = 0; b < kMergeBatch; ++b) {
-          lse_merge(m, S, q[b].x, q[b].y);
-          if (better(q[b].z, qi[b], key, gj)) {
-            key = q[b].z;
-            gj = qi[b];
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {  // the row's four lanes
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-        lse_merge(m, S, m2, s2);
-        const float k2 = __shfl_xor_sync(0xffffffffu, key, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, gj, o);
-        if (better(k2, i2, key, gj)) {
-          key = k2;
-          gj = i2;
-        }
-      }
+      const unsigned long long pb = ok_row ? __ldcg(p.gbest_prev + arow) : 0ull;
+      const int gj = (pb >> 32) ? (int)~(uint32_t)pb : 0x7fffffff;
       // Stage 2: x_{k-1} inside group gj, from step k-1's stored scores.  The
       // row's four lanes take 8 ids each; each lane keys its largest score
       // exactly, filters the other seven against it (the draft epilogue's
@@ -540,12 +515,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         if (sub == 0) flag_status(p.status, DSPARK_DEV_BAD_INPUT);
         idx = 0;
       }
-      if (ok_row && slot == 0 && sub == 0) {
-        const float l = m + logf(S);
-        const size_t o = (size_t)arow * p.gamma + (p.k - 2);
-        p.x[o] = idx;
-        p.logp[o] = sv - l;
-        p.lse[o] = l;
+      if (sub == 0) {  // for the row's x, logp, lse of step k-1, written after the A tile
+        const int q = warp * 8 + (lane >> 2);
+        ((int*)(smem + kOffDrawn))[q] = idx;
+        ((float*)(smem + kOffDrawn))[kTileM + q] = sv;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) xps[i] = __shfl_sync(0xffffffffu, idx, 4 * i);
@@ -576,13 +549,42 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_a);
+    if (p.k >= 2 && !p.A_src) {
+      // x, logp and lse of step k-1 for the rows q = slot, slot + slots, ... of
+      // this row tile (each row by one CTA), while the first tile's contraction
+      // runs: the row's log-normaliser merged from its partials (one warp per
+      // row, lanes over the partials), its drawn token and score from above.
+      named_barrier(2, kEpiWarps * 32);  // every warp's drawn rows are in shared memory
+      for (int q = slot + warp * p.slots; q < kTileM; q += kEpiWarps * p.slots) {
+        const int arow = m_tile * kTileM + q;
+        if (arow >= p.R) break;
+        float m = -INFINITY, S = 0.0f;
+        for (int t = lane; t < p.n_parts; t += 32) {
+          const float4 st = p.prev_stats[(size_t)arow * p.n_parts + t];
+          lse_merge(m, S, st.x, st.y);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+          lse_merge(m, S, m2, s2);
+        }
+        if (lane == 0) {
+          const float l = m + logf(S);
+          const size_t o = (size_t)arow * p.gamma + (p.k - 2);
+          p.x[o] = ((const int*)(smem + kOffDrawn))[q];
+          p.logp[o] = ((const float*)(smem + kOffDrawn))[kTileM + q] - l;
+          p.lse[o] = l;
+        }
+      }
+    }
     for (int u = 0; u < n_units; ++u) {
       const int n = slot + u * p.slots;
       const int buf = u & 1;
       const uint32_t acc_phase = (u >> 1) & 1;
       const int col0 = n * kTileN + cgrp * 32;
       // The row's best key over all CTAs of this step so far, read early (L2).
-      const uint32_t gkey = row_ok ? __ldcg(p.gthr_cur + row) : 0u;
+      const uint32_t gkey = row_ok ? (uint32_t)(__ldcg(p.gbest_cur + row) >> 32) : 0u;
 
       // U of this warp: row `lane`, its 32 columns of the quarter's tile.
       // Waits are decided warp-wide; on a failed one the warp leaves the loop
@@ -728,16 +730,23 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
         // key yet the group is keyed exactly.
         const bool cand = thr == -INFINITY ||
                           unit_float(wg) + ex2_approx((Lg - thr) * L2E) * 1.001f >= 2.0f;
+        bool raised = false;
         if (cand) {
           const float key = __fadd_rn(Lg, gumbel(wg));
           if (better(key, gj, best, best_j)) {
             best = key;
             best_j = gj;
+            raised = true;
           }
         }
-        if (best > thr) {  // publish for the row's other groups and CTAs
+        // Publish for the row's other groups and CTAs.  A key equal to the
+        // threshold is published too, so that the packed maximum ends on the
+        // smaller of two groups with equal keys, as the partials' merge would.
+        if (raised && best >= thr) {
           rowbest[cgrp] = best;
-          if (best < INFINITY) atomicMax(p.gthr_cur + row, key_ord(best));
+          if (best < INFINITY)
+            atomicMax(p.gbest_cur + row,
+                      ((unsigned long long)key_ord(best) << 32) | (unsigned long long)~(uint32_t)best_j);
         }
       }
     }
@@ -933,9 +942,9 @@ cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStr
 
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
-                                 const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s, const void* A_src,
-                                 long long wait_budget, bool withhold_w2) {
+                                 const DraftPartials& cur, unsigned long long* gbest, int32_t* x,
+                                 float* logp, float* lse, int* status, cudaStream_t s,
+                                 const void* A_src, long long wait_budget, bool withhold_w2) {
   const int Mt = (plan.R + kTileM - 1) / kTileM;
   const int n_tiles = (plan.V + kTileN - 1) / kTileN;
   const int slots = draft_tc_parts(plan.R, plan.V);
@@ -959,8 +968,9 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.prev_index = prev.index;
   p.pstats = cur.stats;
   p.pindex = cur.index;
-  p.gthr_cur = gthr + (size_t)(k & 1) * plan.R;
-  p.gthr_next = gthr + (size_t)((k + 1) & 1) * plan.R;
+  p.gbest_prev = gbest + (size_t)((k + 2) % 3) * plan.R;  // step k-1's
+  p.gbest_cur = gbest + (size_t)(k % 3) * plan.R;
+  p.gbest_next = gbest + (size_t)((k + 1) % 3) * plan.R;
   p.x = x;
   p.logp = logp;
   p.lse = lse;

@@ -22,8 +22,8 @@ constexpr int kDraftTileN = 128;  // vocab columns per tile (both contraction pa
 
 // Workspace layout of dspark_draft_sample (byte offsets, 256-aligned).
 struct DraftWorkspace {
-  // two partial buffers; gthr: [2][R] per-row best keys shared by a step's CTAs
-  size_t status, a_rows, stats, index, stats2, index2, gthr, w2t, total;
+  // two partial buffers; gbest: [3][R] per-row packed best (key, group) of a step's CTAs
+  size_t status, a_rows, stats, index, stats2, index2, gbest, w2t, total;
 };
 DraftWorkspace draft_workspace_layout(int R, int gamma, int V, int r, int dtype);
 
@@ -45,15 +45,17 @@ struct DraftTcPlan {
 cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, int R, int gamma,
                              int V, int r, float* scores);
 cudaError_t launch_transpose_w2(const void* W2, int r, int V, void* W2T, cudaStream_t s);
-// Step k (1-based): gathers A from x0 (k = 1) or from the combine of `prev`
-// (step k-1's partials, whose x/logp/lse it stores), writes `cur`.  gthr is
-// the [2][R] array of per-row best keys (key_ord form): step k reads and raises
-// row k & 1 and zeroes row (k + 1) & 1 for the next step; row 1 must be zero
-// before step 1.
+// Step k (1-based): gathers A from x0 (k = 1) or from step k-1's drawn
+// tokens (its packed per-row best, then the token inside that group; the
+// partials `prev` give step k-1's lse, which it stores with x and logp),
+// writes `cur`.  gbest is the [3][R] array of per-row packed bests
+// (key_ord(key) << 32 | ~group): step k reads row (k - 1) % 3, raises row
+// k % 3 and zeroes row (k + 1) % 3 for the next step; rows 1 and 2 must be
+// zero before step 1.
 cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uint64_t seed,
                                  const int32_t* x0, const void* W1, const DraftPartials& prev,
-                                 const DraftPartials& cur, uint32_t* gthr, int32_t* x, float* logp,
-                                 float* lse, int* status, cudaStream_t s,
+                                 const DraftPartials& cur, unsigned long long* gbest, int32_t* x,
+                                 float* logp, float* lse, int* status, cudaStream_t s,
                                  const void* A_src = nullptr, long long wait_budget = 0,
                                  bool withhold_w2 = false);
 // RNN head, step k: x_{k-1} (anchor for k = 1, else the merge of `prev`, whose
