@@ -413,6 +413,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     int best_j = 0x7fffffff;
     // Everything below reads or writes what the previous step (launched as this
     // grid's programmatic primary) wrote or reads: wait for its completion.
+    // Its outputs are read with coherent loads (plain or ld.global.cg), never
+    // the non-coherent path: this grid may have started while that step ran.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (slot == 0 && cgrp == 0 && row_ok) p.gbest_next[row] = 0ull;
 

@@ -67,11 +67,14 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
   float2 q = make_float2(0.0f, 0.0f);
   if (row < R) q = *(const float2*)(Q + ((size_t)row * gamma + (k - 1)) * r + j);
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // What the previous draft step and state update wrote (state, partials,
+  // scores) is read through L2 (ld.global.cg), never the non-coherent path:
+  // this grid may have started while the previous step still ran.
 #pragma unroll
   for (int u = 0; u < kLoads; ++u) {
     const int v = threadIdx.x + u * kRnnThreads;
     const int i = v / r, hrow = row0 + i;  // previous states of the CTA's rows
-    hv[u] = (v < kRnnRows * r && k > 1 && hrow < R) ? h_prev[(size_t)hrow * r + (v - i * r)] : 0.0f;
+    hv[u] = (v < kRnnRows * r && k > 1 && hrow < R) ? __ldcg(h_prev + (size_t)hrow * r + (v - i * r)) : 0.0f;
   }
   // The previous step's partials of this warp's row (at most 2 per lane issued at once).
   float4 ps[2];
@@ -80,8 +83,8 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
   for (int u = 0; u < 2; ++u) {
     const int t = lane + 32 * u;
     const bool use = k > 1 && row < R && t < n_parts;
-    ps[u] = use ? prev_stats[(size_t)row * n_parts + t] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-    pi[u] = use ? prev_index[(size_t)row * n_parts + t] : 0x7fffffff;
+    ps[u] = use ? __ldcg(prev_stats + (size_t)row * n_parts + t) : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+    pi[u] = use ? __ldcg(prev_index + (size_t)row * n_parts + t) : 0x7fffffff;
   }
 #pragma unroll
   for (int u = 0; u < kLoads; ++u) {
@@ -101,8 +104,8 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
         int gj = 0x7fffffff;
         for (int t = lane; t < n_parts; t += 32) {
           const int u = (t - lane) >> 5;
-          const float4 qs = u < 2 ? ps[u] : prev_stats[(size_t)row * n_parts + t];
-          const int qi = u < 2 ? pi[u] : prev_index[(size_t)row * n_parts + t];
+          const float4 qs = u < 2 ? ps[u] : __ldcg(prev_stats + (size_t)row * n_parts + t);
+          const int qi = u < 2 ? pi[u] : __ldcg(prev_index + (size_t)row * n_parts + t);
           lse_merge(m, S, qs.x, qs.y);
           if (better(qs.z, qi, key, gj)) {
             key = qs.z;
@@ -114,7 +117,7 @@ rnn_state_kernel(int k, const int32_t* __restrict__ x0, const __nv_bfloat16* __r
         if (gj < 0 || gj >= (V + kGroup - 1) / kGroup) gj = 0;  // NaN scores: flagged below
         const int v = gj * kGroup + lane;
         const bool valid = v < V;
-        const float s_v = valid ? scores[((size_t)row * gamma + (k - 2)) * V + v] : 0.0f;
+        const float s_v = valid ? __ldcg(scores + ((size_t)row * gamma + (k - 2)) * V + v) : 0.0f;
         float k2, sv;
         int idx;
         group_draw_warp(s_v, valid, v, seed, (uint32_t)row, (uint32_t)(k - 1), DSPARK_PURPOSE_DRAFT, k2,

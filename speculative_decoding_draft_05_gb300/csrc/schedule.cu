@@ -209,7 +209,8 @@ __device__ __forceinline__ long long stage_and_prefix(const unsigned long long* 
                                                       unsigned long long (&k)[kPerThread]) {
   const int tid = threadIdx.x, base = tid * kPerThread;
 #pragma unroll
-  for (int i = tid; i < kMaxCandidates; i += kSchedThreads) stage[skew(i)] = i < n ? sorted[i] : ~0ull;
+  for (int i = tid; i < kMaxCandidates; i += kSchedThreads)
+    stage[skew(i)] = i < n ? __ldcg(sorted + i) : ~0ull;  // L2 (see the scan kernel)
   __syncthreads();
   long long local = 0;
 #pragma unroll
@@ -253,7 +254,10 @@ __global__ void __launch_bounds__(kSchedThreads)
 schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double* __restrict__ sps,
                      int R, int gamma, int32_t* __restrict__ ell, double* __restrict__ diag,
                      int* __restrict__ status) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // launched as the rank kernel's dependent
+  // Launched as the rank kernel's programmatic dependent: the sorted keys it
+  // writes are read after this wait, through L2 (ld.global.cg), never the
+  // non-coherent path, since this grid may start while the rank kernel runs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ long long warp_tot[kSchedThreads / 32];
   __shared__ int stop_at;
   const int tid = threadIdx.x;
@@ -405,7 +409,7 @@ schedule_topk_kernel(const unsigned long long* __restrict__ sorted, const int32_
   }
   if (k > n) k = n;
   for (int i = threadIdx.x; i < k; i += kSchedThreads)
-    atomicAdd(&ell[(int)(sorted[i] & 0xffffu)], 1);
+    atomicAdd(&ell[(int)(__ldcg(sorted + i) & 0xffffu)], 1);
 }
 
 int sm_count_sched() {

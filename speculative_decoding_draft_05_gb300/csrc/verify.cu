@@ -246,16 +246,20 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
   __shared__ float rm[kRowWarps], rs[kRowWarps];
   __shared__ float s_ld;
   constexpr int kRowUnroll = row_unroll<T>();  // 64 bytes of Z per thread in flight
-  const int n_rows = *count;
+  // What the kernels before this one in the chain wrote (the row list and its
+  // count here; LSE^t, the accept flags and the draw partials further on) is
+  // read through L2 (ld.global.cg), never through the non-coherent path: a
+  // programmatic dependent may start while the kernel before it still runs.
+  const int n_rows = __ldcg(count);
   const int groups = V >> 3;
   // Equal waves: with w = ceil(rows / grid) rows per CTA, only the first
   // ceil(rows / w) CTAs take rows, so every working CTA takes w or w - 1 and no
   // last wave runs part-empty (1088 rows on 304 CTAs: 272 CTAs x 4 rows).
   const int waves = n_rows > 0 ? (n_rows + (int)gridDim.x - 1) / (int)gridDim.x : 1;
   const int stride = (n_rows + waves - 1) / waves;
-  uint32_t item = (int)blockIdx.x < n_rows ? list[blockIdx.x] : 0u;
+  uint32_t item = (int)blockIdx.x < n_rows ? __ldcg(list + blockIdx.x) : 0u;
   for (int i = blockIdx.x; i < n_rows && (int)blockIdx.x < stride; i += stride) {
-    const uint32_t item_next = i + stride < n_rows ? list[i + stride] : 0u;
+    const uint32_t item_next = i + stride < n_rows ? __ldcg(list + i + stride) : 0u;
     const int r = (int)(item / (uint32_t)gamma), j = (int)(item - (uint32_t)r * gamma) + 1;
     const size_t rj = (size_t)r * gamma + (j - 1);
     const T* z = Z + zr.row(r, j) * V;
@@ -351,7 +355,7 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
 __device__ __forceinline__ int leading_accepts(const int* __restrict__ acc_ws, int r, int gamma,
                                                int L) {
   int n = 0;
-  while (n < L && acc_ws[(size_t)r * gamma + n]) ++n;
+  while (n < L && __ldcg(acc_ws + (size_t)r * gamma + n)) ++n;
   return n;
 }
 
@@ -644,7 +648,7 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   const float* srow = scores + ((size_t)r * gamma + (residual ? row - 1 : 0)) * V;
   float Lt = 0.0f, dL = 0.0f;
   if (residual) {
-    Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+    Lt = __ldcg(lse_t_ws + (size_t)r * (gamma + 1) + (row - 1));
     dL = __fsub_rn(Lt, lse[(size_t)r * gamma + (row - 1)]);
   }
   const int n_groups = (V + kGroup - 1) / kGroup;
@@ -767,7 +771,7 @@ verify_emit_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
   float best = -INFINITY;
   int gj = 0x7fffffff;
   for (int c = threadIdx.x; c < n_chunks; c += kVerifyThreads) {
-    const float2 p = partials[(size_t)r * n_chunks + c];
+    const float2 p = __ldcg(partials + (size_t)r * n_chunks + c);
     const int pi = __float_as_int(p.y);
     if (better(p.x, pi, best, gj)) {
       best = p.x;
@@ -804,7 +808,7 @@ verify_emit_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
     if (valid) {
       const float zv = to_f32(z[v]);
       if (residual) {
-        const float Lt = lse_t_ws[(size_t)r * (gamma + 1) + (row - 1)];
+        const float Lt = __ldcg(lse_t_ws + (size_t)r * (gamma + 1) + (row - 1));
         const float dL = __fsub_rn(Lt, lse[(size_t)r * gamma + (row - 1)]);
         float a, dt;
         residual_terms(zv, scores[((size_t)r * gamma + (row - 1)) * V + v], invT, Lt, dL, a, dt);
@@ -831,7 +835,7 @@ verify_emit_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
     if (t < gamma && t >= L) cstar[(size_t)r * gamma + t] = __int_as_float(0x7fc00000);
     if (lse_t_out)
       lse_t_out[(size_t)r * (gamma + 1) + t] =
-          t < L ? lse_t_ws[(size_t)r * (gamma + 1) + t] : __int_as_float(0x7fc00000);
+          t < L ? __ldcg(lse_t_ws + (size_t)r * (gamma + 1) + t) : __int_as_float(0x7fc00000);
   }
   if (threadIdx.x == 0) {
     n_acc[r] = n;
