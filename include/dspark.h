@@ -90,7 +90,10 @@ enum {
 /* Ids per group of the two-level Gumbel-max draw. */
 enum { DSPARK_GROUP = 32 };
 
-/* Device status word bits (OR-ed together). */
+/* Device status word bits (OR-ed together).  DSPARK_DEV_TIMEOUT: a bounded
+ * device-side wait gave up (the tensor-core draft's pipeline barriers; the
+ * verify draw's wait for its bulk copy of a target row); the outputs of that
+ * call are then not valid, and the context stays usable. */
 enum { DSPARK_DEV_BAD_INPUT = 1, DSPARK_DEV_TIMEOUT = 2 };
 
 /* Text of a status code; static storage. */
