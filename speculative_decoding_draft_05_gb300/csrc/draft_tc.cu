@@ -16,11 +16,12 @@
 //     that share a vocab tile stream the same W2 tile at about the same time,
 //     so W2 comes from HBM about once per step.
 //   * The A tile is gathered by the epilogue warps at the start: for step 1
-//     from the anchors, for step k > 1 by first merging step k-1's per-slot
-//     partials of each row (its local normaliser and Gumbel-max argmax), which
-//     also yields step k-1's x, logp and lse (stored by the slot-0 CTAs).  So
-//     consecutive steps need no separate combine launch; one combine follows
-//     the last step.
+//     from the anchors, for step k > 1 from step k-1's drawn tokens (each
+//     row's packed best (key, group) that step's CTAs raised, then the token
+//     inside that group).  Each CTA then writes step k-1's x, logp and lse for
+//     its share of the row tile's rows, merging those rows' per-slot partials
+//     for the lse.  So consecutive steps need no separate combine launch; one
+//     combine follows the last step.
 //   * warp 16 (producer): TMA of W2^T chunks [128 vocab rows x 64 K] into a
 //     3-stage ring.  W2^T (K-major) is written once per draft call by
 //     transpose_w2_kernel, so each vocab tile's B operand is one contiguous
@@ -428,12 +429,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     int u_issued = n_units > 0 ? 1 : 0, u_landed = 0;
     // A tile: rows m_tile*128 + 8 warp .. +7 get W1[x_{k-1}], written straight into
     // the K-major 128-byte-swizzled layout the MMA reads (zero rows past R).
-    // x_{k-1} is the anchor for k = 1, else the combine of step k-1's partials;
-    // the slot-0 CTA of each row tile also stores step k-1's x, logp, lse.
-    // Lanes 4i .. 4i+3 merge row i of the warp's 8: lane 4i + s holds parts
-    // s, s + 4, s + 8, ..., loaded kMergeBatch at a time so that each batch is
-    // in flight at once (two memory round trips for up to 40 parts, where
-    // holding every part of every row at once would need too many registers).
+    // x_{k-1} is the anchor for k = 1, else step k-1's draw: its packed
+    // per-row best gives the group, and lanes 4i .. 4i+3 (row i of the warp's
+    // 8) draw the token inside it (stage 2).
     int xps[8];
     if (p.A_src) {  // the A rows come precomputed (RNN head); x_{k-1} is stored elsewhere
 #pragma unroll
