@@ -30,6 +30,8 @@
 //     accumulators) and issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
 //     M = 128, N = 128, K = 16) from shared-memory descriptors: A and W2^T both
 //     K-major, 128-byte swizzled.
+//   * warp 18 (finalization, steps k > 1): writes step k-1's x, logp and lse
+//     for its share of the row tile's rows, beside the pipeline.
 //   * warps 0..15 (epilogue): warp w reads TMEM lanes 32 (w % 4) .. +31 (its
 //     rows) and columns 32 (w / 4) .. +31 of the tile.  The four warps of a
 //     row quarter share its U_k tile (32 rows x 128 columns, two TMA boxes with
@@ -65,9 +67,10 @@ constexpr int kTileN = kDraftTileN;  // 128
 constexpr int kChunkK = 64;          // 128 bytes of bf16: one swizzle atom row
 constexpr int kStages = 3;
 constexpr int kEpiWarps = 16;
-constexpr int kThreads = (kEpiWarps + 2) * 32;
+constexpr int kThreads = (kEpiWarps + 3) * 32;
 constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kFinWarp = kEpiWarps + 2;  // step k-1's x, logp, lse, beside the pipeline
 constexpr int kMaxRank = 256;
 constexpr uint32_t kTmemCols = 256;
 
@@ -227,6 +230,11 @@ __device__ __forceinline__ float unit_float(uint32_t w) {
 
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Arrive on a named barrier without waiting for it.
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 
@@ -393,6 +401,40 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       tc_commit(bar_drain);
       mbar_drain(bar_drain, 0, p.wait_budget);
     }
+  } else if (warp == kFinWarp) {
+    // ------------------------------------------------------------ finalization
+    // x, logp and lse of step k-1 for the rows q = slot, slot + slots, ... of
+    // this row tile (each row by one CTA), beside the pipeline: the row's
+    // log-normaliser merged from its partials (lanes over the partials), its
+    // drawn token and score from the epilogue warps' prologue (shared memory,
+    // behind named barrier 2).
+    if (p.k >= 2 && !p.A_src) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      named_barrier(2, (kEpiWarps + 1) * 32);
+      const int m_row0 = m_tile * kTileM;
+      for (int q = slot; q < kTileM; q += p.slots) {
+        const int arow = m_row0 + q;
+        if (arow >= p.R) break;
+        float m = -INFINITY, S = 0.0f;
+        for (int t = lane; t < p.n_parts; t += 32) {
+          const float4 st = p.prev_stats[(size_t)arow * p.n_parts + t];
+          lse_merge(m, S, st.x, st.y);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+          lse_merge(m, S, m2, s2);
+        }
+        if (lane == 0) {
+          const float l = m + logf(S);
+          const size_t o = (size_t)arow * p.gamma + (p.k - 2);
+          p.x[o] = ((const int*)(smem + kOffDrawn))[q];
+          p.logp[o] = ((const float*)(smem + kOffDrawn))[kTileM + q] - l;
+          p.lse[o] = l;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
@@ -549,35 +591,8 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_a);
-    if (p.k >= 2 && !p.A_src) {
-      // x, logp and lse of step k-1 for the rows q = slot, slot + slots, ... of
-      // this row tile (each row by one CTA), while the first tile's contraction
-      // runs: the row's log-normaliser merged from its partials (one warp per
-      // row, lanes over the partials), its drawn token and score from above.
-      named_barrier(2, kEpiWarps * 32);  // every warp's drawn rows are in shared memory
-      for (int q = slot + warp * p.slots; q < kTileM; q += kEpiWarps * p.slots) {
-        const int arow = m_tile * kTileM + q;
-        if (arow >= p.R) break;
-        float m = -INFINITY, S = 0.0f;
-        for (int t = lane; t < p.n_parts; t += 32) {
-          const float4 st = p.prev_stats[(size_t)arow * p.n_parts + t];
-          lse_merge(m, S, st.x, st.y);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-          const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-          lse_merge(m, S, m2, s2);
-        }
-        if (lane == 0) {
-          const float l = m + logf(S);
-          const size_t o = (size_t)arow * p.gamma + (p.k - 2);
-          p.x[o] = ((const int*)(smem + kOffDrawn))[q];
-          p.logp[o] = ((const float*)(smem + kOffDrawn))[kTileM + q] - l;
-          p.lse[o] = l;
-        }
-      }
-    }
+    // The drawn rows are in shared memory: the finalization warp may go on.
+    if (p.k >= 2 && !p.A_src) named_arrive(2, (kEpiWarps + 1) * 32);
     for (int u = 0; u < n_units; ++u) {
       const int n = slot + u * p.slots;
       const int buf = u & 1;
