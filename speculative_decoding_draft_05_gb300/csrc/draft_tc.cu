@@ -117,6 +117,22 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// L2 eviction priority for TMA loads whose lines should stay (evict_last).
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
                                              int z) {
   asm volatile(
@@ -263,6 +279,10 @@ struct Params {
   float* scores;           // [R, gamma, V]: stored by the epilogue (kStg), read by stage 2
   long long wait_budget;  // SM clocks each bounded wait may take
   int withhold_w2;        // diagnostic: the producer issues no W2 loads, so the waits run out
+  // W2^T kept in L2 across the steps (it fits); the last step hands its lines
+  // back to the normal eviction order when done.
+  int w2_keep;
+  const __nv_bfloat16* w2t;
 };
 
 template <bool kStg>
@@ -326,6 +346,9 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
+      // W2^T is read again by the next step: where it fits in L2, its loads mark
+      // it to be kept (evict_last) over the streamed U and scores.
+      const uint64_t pol_w2 = l2_policy_keep();
       bool ok = true;
       for (int u = 0; u < n_units && ok; ++u) {
         const int n = slot + u * p.slots;
@@ -337,7 +360,10 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
           uint8_t* dst = smem + kOffB + stage * kBChunkBytes;
           mbar_expect_tx(&bar_full[stage], kBChunkBytes);
           // W2^T rows n*128 .. +127, K columns c*64 .. +63 (one contiguous 64 KB block per tile)
-          tma_load_2d(dst, &tmW2, c * kChunkK, n * kTileN, &bar_full[stage]);
+          if (p.w2_keep)
+            tma_load_2d_hint(dst, &tmW2, c * kChunkK, n * kTileN, &bar_full[stage], pol_w2);
+          else
+            tma_load_2d(dst, &tmW2, c * kChunkK, n * kTileN, &bar_full[stage]);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -789,6 +815,21 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
       p.pstats[o] = make_float4(m, S, bk, 0.0f);
       p.pindex[o] = bi;
     }
+    if (p.w2_keep && p.k == p.gamma) {
+      // Last step: the W2^T rows of this CTA's vocab tiles (128-byte lines)
+      // go back to the normal eviction order, so that what runs after the
+      // draft gets the L2; the Mt CTAs that share the tiles split the lines.
+      const int lines_per_row = p.r * 2 / 128;
+      const int lines = n_units * kTileN * lines_per_row;
+      for (int i = threadIdx.x + m_tile * kEpiWarps * 32; i < lines; i += p.Mt * kEpiWarps * 32) {
+        const int u = i / (kTileN * lines_per_row), rest = i - u * (kTileN * lines_per_row);
+        const size_t vrow = (size_t)(slot + u * p.slots) * kTileN + rest / lines_per_row;
+        if (vrow < (size_t)p.V) {
+          const char* a = (const char*)(p.w2t + vrow * p.r) + (rest % lines_per_row) * 128;
+          asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(a) : "memory");
+        }
+      }
+    }
     if (lane == 0) {
       if (cgrp == 0 && u_issued > u_landed)
         mbar_drain(&bar_u[quarter], (uint32_t)(u_issued - 1) & 1u, p.wait_budget);
@@ -874,6 +915,18 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
   return r == CUDA_SUCCESS;
 }
 
+// L2 size of the current device (bytes), once.
+static size_t l2_bytes() {
+  static size_t n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev);
+    n = v > 0 ? (size_t)v : 1;
+  }
+  return n;
+}
+
 int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -942,6 +995,7 @@ cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, 
   }();
   if (attr_err != cudaSuccess) return attr_err;
   plan->scores = scores;
+  plan->w2t = W2T;
   plan->R = R;
   plan->gamma = gamma;
   plan->V = V;
@@ -993,6 +1047,10 @@ cudaError_t launch_draft_step_tc(const DraftTcPlan& plan, int k, float invT, uin
   p.scores = plan.scores;
   p.wait_budget = wait_budget > 0 ? wait_budget : kWaitBudget;
   p.withhold_w2 = withhold_w2 ? 1 : 0;
+  p.w2t = (const __nv_bfloat16*)plan.w2t;
+  // (rows of whole 128-byte lines, r % 64 == 0, so that each line the last
+  // step hands back starts on a line boundary)
+  p.w2_keep = plan.r % 64 == 0 && (size_t)plan.V * plan.r * 2 <= l2_bytes() / 4 * 3 ? 1 : 0;
   // Score stores: coalesced st.global when several row tiles share each W2
   // tile (the TMA unit then carries U and W2 for up to Mt CTAs' worth of
   // stores), TMA stores for a single row tile (R <= 128), where W2 dominates.

@@ -40,6 +40,7 @@ cudaError_t launch_draft_tile_simt(const void* U, const void* A, const void* W2,
 struct DraftTcPlan {
   alignas(64) unsigned char maps[3][128];
   float* scores;
+  const void* w2t;  // W2^T [V, r] bf16, read by every step
   int R, gamma, V, r;
 };
 cudaError_t prepare_draft_tc(DraftTcPlan* plan, const void* U, const void* W2T, int R, int gamma,
