@@ -36,7 +36,8 @@
 //     rows) and columns 32 (w / 4) .. +31 of the tile.  The four warps of a
 //     row quarter share its U_k tile (32 rows x 128 columns, two TMA boxes with
 //     128-byte rows, loaded by the quarter's column-group-0 warp once all four
-//     have read the previous one).  Each warp computes s, stages it in
+//     have read the previous one; the first, and the next few into L2, before
+//     the wait on the previous step).  Each warp computes s, stages it in
 //     swizzled shared memory and stores it (coalesced st.global for several
 //     row tiles, TMA for one), and updates per-row running statistics in
 //     registers: max / sum-exp (online), and stage 1 of the two-level draw.
@@ -72,6 +73,9 @@ constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr int kFinWarp = kEpiWarps + 2;  // step k-1's x, logp, lse, beside the pipeline
 constexpr int kMaxRank = 256;
+// U tiles of the CTA's next units fetched into L2 before the step's wait (see
+// the epilogue); more than a few competed with the previous step's last tiles.
+constexpr int kUPrefetch = 4;
 constexpr uint32_t kTmemCols = 256;
 
 constexpr int kAChunkBytes = kTileM * kChunkK * 2;  // 16 KB
@@ -106,6 +110,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Fetch a U box into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
@@ -480,18 +491,25 @@ draft_step_tc_kernel(const __grid_constant__ CUtensorMap tmW2,
     const PhiloxStream rng(p.seed, (uint32_t)row, (uint32_t)p.k, DSPARK_PURPOSE_DRAFT_GROUP);
     float run_m = -INFINITY, run_s = 0.0f, best = -INFINITY;
     int best_j = 0x7fffffff;
+    // The first U tile, and the next few into L2: U is an input of the call
+    // that no kernel of the draft writes, so it loads before the wait below,
+    // while the previous step's last CTAs still run and HBM has room.
+    if (cgrp == 0 && lane == 0 && n_units > 0) {
+      mbar_expect_tx(&bar_u[quarter], kUQuarterBytes);
+      tma_load_3d(uq, &tmU, slot * kTileN, kpos, row0, &bar_u[quarter]);
+      tma_load_3d(uq + kUBoxBytes, &tmU, slot * kTileN + 64, kpos, row0, &bar_u[quarter]);
+      for (int u = 1; u <= kUPrefetch && u < n_units; ++u) {
+        const int n = slot + u * p.slots;
+        tma_prefetch_3d(&tmU, n * kTileN, kpos, row0);
+        tma_prefetch_3d(&tmU, n * kTileN + 64, kpos, row0);
+      }
+    }
     // Everything below reads or writes what the previous step (launched as this
     // grid's programmatic primary) wrote or reads: wait for its completion.
     // Its outputs are read with coherent loads (plain or ld.global.cg), never
     // the non-coherent path: this grid may have started while that step ran.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (slot == 0 && cgrp == 0 && row_ok) p.gbest_next[row] = 0ull;
-
-    if (cgrp == 0 && lane == 0 && n_units > 0) {
-      mbar_expect_tx(&bar_u[quarter], kUQuarterBytes);
-      tma_load_3d(uq, &tmU, slot * kTileN, kpos, row0, &bar_u[quarter]);
-      tma_load_3d(uq + kUBoxBytes, &tmU, slot * kTileN + 64, kpos, row0, &bar_u[quarter]);
-    }
     // U loads of this warp issued so far and those waited for (equal on exit
     // unless a wait failed: the one in flight must land before the CTA exits).
     int u_issued = n_units > 0 ? 1 : 0, u_landed = 0;
