@@ -5,7 +5,11 @@ One step = one full round (dspark_draft_sample -> dspark_schedule ->
 dspark_verify) over one batch of synthetic input already resident in HBM.
 Metric: draft+verify positions/s = R * gamma / round time (whole job over all
 ranks).  Default workload: R = 512 requests, gamma = 16, V = 151936, r = 256,
-bf16 inputs (verify_r512_g16_v151936).
+bf16 inputs (verify_r512_g16_v151936).  The draft head's weights stay fixed
+across rounds, so its W2 is transposed once at setup into the layout the
+tensor-core draft reads (dspark_transpose_w2) and every round calls
+dspark_draft_sample_w2t; --w2-layout plain passes W2 as stored instead and each
+round's draft call transposes it (a read and a write of r V bf16).
 
 Also reported on the same JSON line:
   roofline      the dominant kernel (the draft contraction + epilogue) timed with
@@ -204,7 +208,7 @@ class Round:
     """Device buffers of one round and the three C-ABI calls on one stream."""
 
     def __init__(self, w: workload.Workload, seed: int, device, scheduler: str = "alg1",
-                 verify_layout: str = "padded", head: str = "markov"):
+                 verify_layout: str = "padded", head: str = "markov", w2_layout: str = "transposed"):
         import speculative_decoding_draft_05_gb300 as dspark
 
         self.dspark = dspark
@@ -214,6 +218,13 @@ class Round:
         self.rnn = workload.rnn_inputs(w, seed=seed, device=device) if head == "rnn" else None
         inp = workload.generate(w, seed=seed, device=device)
         self.inp = inp
+        # The head's second factor in the tensor cores' K-major layout, written once
+        # here as the weights are loaded (they stay fixed across rounds); each round's
+        # draft then reads it as is.  w2_layout "plain": every draft call transposes W2.
+        self.w2t = None
+        if (w2_layout == "transposed" and w.dtype == "bf16" and w.r % 64 == 0 and w.r <= 256
+                and w.V % 8 == 0):
+            self.w2t = dspark.dspark_transpose_w2(inp["W2"])
         R, g, V = w.R, w.gamma, w.V
         f32, i32 = torch.float32, torch.int32
         self.x = torch.empty(R, g, dtype=i32, device=device)
@@ -287,19 +298,27 @@ class Round:
         torch.cuda.synchronize(self.device)
 
     def draft(self, seed=None, U=None, W1=None, W2=None, x0=None, Wh=None, Q=None):
+        """The draft call; W2 is the head's second factor in this round's layout
+        (W2^T [V, r] where it was transposed at setup, else W2 [r, V])."""
         i = self.inp
         seed = self.seed if seed is None else seed
         U = i["U"] if U is None else U
         W1 = i["W1"] if W1 is None else W1
-        W2 = i["W2"] if W2 is None else W2
+        W2 = (self.w2t if self.w2t is not None else i["W2"]) if W2 is None else W2
         x0 = i["x0"] if x0 is None else x0
         kw = dict(x=self.x, logp=self.logp, lse=self.lse, scores=self.scores, workspace=self.ws_d)
+        d = self.dspark
         if self.rnn is not None:
             Wh = self.rnn["Wh"] if Wh is None else Wh
             Q = self.rnn["Q"] if Q is None else Q
-            self.dspark.dspark_draft_sample_rnn(U, W1, W2, Wh, Q, x0, self.w.T, seed, **kw)
+            if self.w2t is not None:
+                d.dspark_draft_sample_rnn_w2t(U, W1, W2, Wh, Q, x0, self.w.T, seed, **kw)
+            else:
+                d.dspark_draft_sample_rnn(U, W1, W2, Wh, Q, x0, self.w.T, seed, **kw)
+        elif self.w2t is not None:
+            d.dspark_draft_sample_w2t(U, W1, W2, x0, self.w.T, seed, **kw)
         else:
-            self.dspark.dspark_draft_sample(U, W1, W2, x0, self.w.T, seed, **kw)
+            d.dspark_draft_sample(U, W1, W2, x0, self.w.T, seed, **kw)
 
     def schedule(self, conf=None, sps=None):
         d = self.dspark
@@ -342,7 +361,7 @@ class Round:
 
     def input_tensors(self):
         i = self.inp
-        ins = [i["U"], i["W1"], i["W2"], i["x0"], i["conf"], i["sps"]]
+        ins = [i["U"], i["W1"], i["W2"] if self.w2t is None else self.w2t, i["x0"], i["conf"], i["sps"]]
         ins += [self.Zp, self.offsets] if self.packed else [self.Z]
         if self.rnn is not None:
             ins += [self.rnn["Wh"], self.rnn["Q"]]
@@ -359,13 +378,14 @@ def draft_tile_bytes(w: workload.Workload) -> int:
     return w.R * w.V * (e + 4) + w.r * w.V * e + w.R * w.r * e
 
 
-def round_bytes(w: workload.Workload, ell) -> int:
-    """Algorithmic HBM bytes of one round: the W2 transpose (read + write), gamma
-    draft steps, and verify -- the Z rows of the scheduled positions and of the
-    drawn token (sum(l) + R rows) and the draft scores of the scheduled rows."""
+def round_bytes(w: workload.Workload, ell, transpose: bool = True) -> int:
+    """Algorithmic HBM bytes of one round: the W2 transpose (read + write) where the
+    round does it, gamma draft steps, and verify -- the Z rows of the scheduled
+    positions and of the drawn token (sum(l) + R rows) and the draft scores of the
+    scheduled rows."""
     e = 4 if w.dtype == "f32" else 2
     rows = int(ell.sum().item())
-    return (2 * w.r * w.V * e + w.gamma * draft_tile_bytes(w)
+    return ((2 * w.r * w.V * e if transpose else 0) + w.gamma * draft_tile_bytes(w)
             + (rows + w.R) * w.V * e + rows * w.V * 4)
 
 
@@ -551,7 +571,8 @@ def run_seeds(args, w, rank, world, local):
     init_dist(world, "nccl")
     dspark.binding.load()
     stream = torch.cuda.current_stream(device)
-    rnd = Round(w, 0, device, scheduler=args.scheduler, verify_layout="padded", head=args.head)
+    rnd = Round(w, 0, device, scheduler=args.scheduler, verify_layout="padded", head=args.head,
+                w2_layout=args.w2_layout)
     for i in range(args.warmup):
         rnd.step(0)
     torch.cuda.synchronize(device)
@@ -584,6 +605,7 @@ def run_seeds(args, w, rank, world, local):
                 "mode": f"seeds 0..{len(per_seed) - 1}, one round each on its own inputs",
                 "config": dict(workload.describe(w), seeds=len(per_seed), scheduler=args.scheduler,
                                head=args.head, weights_seed=0,
+                               w2_layout="transposed at setup" if rnd.w2t is not None else "plain",
                                l2="inputs larger than L2 (regenerated between rounds)"),
                 "accepted_tokens_per_s": accepted, "emitted_tokens": emitted,
                 "ms_per_round": {"min": min(per_seed), "median": statistics.median(per_seed),
@@ -608,7 +630,7 @@ def run_ours(args, w, rank, world, local):
     dspark.binding.load()
     stream = torch.cuda.current_stream(device)
     rnd = Round(w, args.seed, device, scheduler=args.scheduler, verify_layout=args.verify_layout,
-                head=args.head)
+                head=args.head, w2_layout=args.w2_layout)
     seeds = [args.seed + i for i in range(args.steps)]  # one Philox key per round
     for i in range(args.warmup):
         rnd.step(args.seed + i)
@@ -769,7 +791,7 @@ def run_ours(args, w, rank, world, local):
         vprobe = {"requests": n, "rows": n * w.gamma, "bytes_per_launch": nb, "us_per_launch": t_r * 1e6,
                   "achieved_gbs": nb / t_r / 1e9, "frac": nb / t_r / 1e9 / hbm_peak, "peak": hbm_peak,
                   "note": "extra call outside the timed regions; not part of value"}
-    rb = round_bytes(w, rnd.ell)
+    rb = round_bytes(w, rnd.ell, transpose=rnd.w2t is None and w.dtype == "bf16")
     round_roof = {"bound": "hbm", "algorithmic_bytes": rb,
                   "achieved": rb / (ms_max / args.steps / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                   "frac": rb / (ms_max / args.steps / 1e3) / 1e9 / hbm_peak}
@@ -789,6 +811,7 @@ def run_ours(args, w, rank, world, local):
                 if w.dtype == "bf16" else "f32", "data": "synthetic",
                 "config": dict(workload.describe(w), seed=args.seed, scheduler=args.scheduler,
                                verify_layout=args.verify_layout, head=args.head,
+                               w2_layout="transposed at setup" if rnd.w2t is not None else "plain",
                                parallelism="replicas" if world > 1 else "single",
                                l2="inputs larger than L2 (U %.2f GB, scores %.2f GB, Z %.2f GB > 129 MB)" % (
                                    w.R * w.gamma * w.V * (2 if w.dtype == "bf16" else 4) / 1e9,
@@ -824,6 +847,10 @@ def main(argv=None):
                     help="draft head: markov (default) or the RNN head")
     ap.add_argument("--verify-layout", choices=["padded", "packed"], default="padded",
                     help="target logits padded [R, gamma+1, V] (default) or packed rows + offsets")
+    ap.add_argument("--w2-layout", choices=["transposed", "plain"], default="transposed",
+                    help="the head's W2: transposed once at setup into the tensor cores' layout "
+                         "(default; weights stay fixed across rounds) or passed as stored, "
+                         "each draft call transposing it")
     ap.add_argument("--R", type=int, default=None, help="override the workload's request count")
     ap.add_argument("--gamma", type=int, default=None, help="override the workload's draft length")
     ap.add_argument("--seeds", type=int, default=0,

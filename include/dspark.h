@@ -136,6 +136,31 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dspark_transpose_w2 -- the Markov head's second factor in the layout the
+ * tensor-core draft reads: W2T[v][a] = W2[a][v], so that each block of 128
+ * vocabulary ids is one contiguous 128 x r block (K-major operand).  The bf16
+ * dspark_draft_sample does this itself on every call (a read and a write of
+ * r V bf16); a caller whose head weights stay fixed across rounds does it once
+ * and passes W2T to dspark_draft_sample_w2t / dspark_draft_sample_rnn_w2t.
+ *
+ * W2   [r, V]  bf16   in;  W2T  [V, r]  bf16   out (caller-allocated)
+ * r a multiple of 64, at most 256; V a multiple of 8 (else
+ * DSPARK_ERR_UNSUPPORTED); W2 and W2T 16-byte aligned (else
+ * DSPARK_ERR_INVALID_ARG).  Enqueued on `stream`; no host synchronisation.
+ * ---------------------------------------------------------------------- */
+int dspark_transpose_w2(const void* W2, int r, int V, void* W2T, void* stream);
+
+/* dspark_draft_sample_w2t -- dspark_draft_sample, bf16, with the second factor
+ * given as dspark_transpose_w2's W2T [V, r] instead of W2 [r, V]; the same
+ * computation and outputs (bit for bit), without the per-call transpose.
+ * Shapes the tensor-core draft does not take return DSPARK_ERR_UNSUPPORTED.
+ * workspace: >= dspark_draft_workspace_bytes(R, gamma, V, r, DSPARK_BF16). */
+int dspark_draft_sample_w2t(const void* U, const void* W1, const void* W2T, const int32_t* x0,
+                            int R, int gamma, int V, int r, float temperature, uint64_t seed,
+                            int32_t* x, float* logp, float* lse, float* scores, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * dspark_draft_sample_rnn -- the draft with the RNN head instead of the Markov
  * head ([summary] §3.1: the alternative sequential head keeps a state across
  * the block and also takes the backbone's hidden state).  Read as an Elman
@@ -159,6 +184,14 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
                             int r, float temperature, uint64_t seed, int32_t* x, float* logp,
                             float* lse, float* scores, void* workspace, size_t workspace_bytes,
                             void* stream);
+/* dspark_draft_sample_rnn_w2t -- dspark_draft_sample_rnn with W2 given as
+ * dspark_transpose_w2's W2T [V, r] (bf16); same outputs, no per-call transpose.
+ * workspace: >= dspark_draft_rnn_workspace_bytes(R, gamma, V, r). */
+int dspark_draft_sample_rnn_w2t(const void* U, const void* W1, const void* W2T, const void* Wh,
+                                const float* Q, const int32_t* x0, int R, int gamma, int V, int r,
+                                float temperature, uint64_t seed, int32_t* x, float* logp,
+                                float* lse, float* scores, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * dspark_schedule -- hardware-aware prefix scheduler, Algorithm 1

@@ -9,6 +9,9 @@ from .binding import (  # noqa: F401
     DSparkError,
     dspark_draft_sample,
     dspark_draft_sample_rnn,
+    dspark_draft_sample_rnn_w2t,
+    dspark_draft_sample_w2t,
+    dspark_transpose_w2,
     draft_rnn_workspace_bytes,
     dspark_profile_start,
     dspark_profile_stop,
@@ -30,6 +33,9 @@ from .binding import (  # noqa: F401
 __all__ = [
     "dspark_draft_sample",
     "dspark_draft_sample_rnn",
+    "dspark_draft_sample_rnn_w2t",
+    "dspark_draft_sample_w2t",
+    "dspark_transpose_w2",
     "draft_rnn_workspace_bytes",
     "dspark_schedule",
     "dspark_schedule_capacity",

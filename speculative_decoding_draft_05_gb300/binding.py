@@ -57,6 +57,13 @@ def load() -> ctypes.CDLL:
     L.dspark_draft_rnn_workspace_bytes.restype = SZ
     L.dspark_draft_sample_rnn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, U64, P, P, P, P, P, SZ, P]
     L.dspark_draft_sample_rnn.restype = I
+    L.dspark_transpose_w2.argtypes = [P, I, I, P, P]
+    L.dspark_transpose_w2.restype = I
+    L.dspark_draft_sample_w2t.argtypes = [P, P, P, P, I, I, I, I, F, U64, P, P, P, P, P, SZ, P]
+    L.dspark_draft_sample_w2t.restype = I
+    L.dspark_draft_sample_rnn_w2t.argtypes = [P, P, P, P, P, P, I, I, I, I, F, U64, P, P, P, P, P,
+                                              SZ, P]
+    L.dspark_draft_sample_rnn_w2t.restype = I
     L.dspark_schedule_workspace_bytes.argtypes = [I, I]
     L.dspark_schedule_workspace_bytes.restype = SZ
     L.dspark_sts_workspace_bytes.argtypes = [I, I, I]
@@ -205,6 +212,40 @@ def dspark_draft_sample(U, W1, W2, x0, temperature: float, seed: int, *, x=None,
     return dict(x=x, logp=logp, lse=lse, scores=scores, workspace=ws)
 
 
+def dspark_transpose_w2(W2, W2T=None, *, stream=None):
+    """W2 [r, V] bf16 -> W2T [V, r] bf16, the layout dspark_draft_sample_w2t reads."""
+    L = load()
+    r, V = W2.shape
+    W2T = torch.empty(V, r, dtype=torch.bfloat16, device=W2.device) if W2T is None else W2T
+    st = L.dspark_transpose_w2(_dev(W2, "W2", torch.bfloat16, (r, V)), r, V,
+                               _dev(W2T, "W2T", torch.bfloat16, (V, r)), _stream(stream))
+    _check("dspark_transpose_w2", st)
+    return W2T
+
+
+def dspark_draft_sample_w2t(U, W1, W2T, x0, temperature: float, seed: int, *, x=None, logp=None,
+                            lse=None, scores=None, workspace=None, stream=None) -> dict:
+    """dspark_draft_sample (bf16) with W2 given as W2T [V, r] from dspark_transpose_w2."""
+    L = load()
+    R, g, V = U.shape
+    r = W1.shape[1]
+    dt = torch.bfloat16
+    dev = U.device
+    x = torch.empty(R, g, dtype=torch.int32, device=dev) if x is None else x
+    logp = torch.empty(R, g, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(R, g, dtype=torch.float32, device=dev) if lse is None else lse
+    scores = torch.empty(R, g, V, dtype=torch.float32, device=dev) if scores is None else scores
+    ws = _workspace(draft_workspace_bytes(R, g, V, r, dt), dev, workspace)
+    st = L.dspark_draft_sample_w2t(
+        _dev(U, "U", dt), _dev(W1, "W1", dt, (V, r)), _dev(W2T, "W2T", dt, (V, r)),
+        _dev(x0, "x0", torch.int32, (R,)), R, g, V, r, float(temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(x, "x", torch.int32, (R, g)),
+        _dev(logp, "logp", torch.float32, (R, g)), _dev(lse, "lse", torch.float32, (R, g)),
+        _dev(scores, "scores", torch.float32, (R, g, V)), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check("dspark_draft_sample_w2t", st)
+    return dict(x=x, logp=logp, lse=lse, scores=scores, workspace=ws)
+
+
 def draft_rnn_workspace_bytes(R: int, gamma: int, V: int, r: int) -> int:
     return int(load().dspark_draft_rnn_workspace_bytes(R, gamma, V, r))
 
@@ -231,6 +272,31 @@ def dspark_draft_sample_rnn(U, W1, W2, Wh, Q, x0, temperature: float, seed: int,
         _dev(logp, "logp", torch.float32, (R, g)), _dev(lse, "lse", torch.float32, (R, g)),
         _dev(scores, "scores", torch.float32, (R, g, V)), ws.data_ptr(), ws.numel(), _stream(stream))
     _check("dspark_draft_sample_rnn", st)
+    return dict(x=x, logp=logp, lse=lse, scores=scores, workspace=ws)
+
+
+def dspark_draft_sample_rnn_w2t(U, W1, W2T, Wh, Q, x0, temperature: float, seed: int, *, x=None,
+                                logp=None, lse=None, scores=None, workspace=None,
+                                stream=None) -> dict:
+    """dspark_draft_sample_rnn with W2 given as W2T [V, r] from dspark_transpose_w2."""
+    L = load()
+    R, g, V = U.shape
+    r = W1.shape[1]
+    dt = torch.bfloat16
+    dev = U.device
+    x = torch.empty(R, g, dtype=torch.int32, device=dev) if x is None else x
+    logp = torch.empty(R, g, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(R, g, dtype=torch.float32, device=dev) if lse is None else lse
+    scores = torch.empty(R, g, V, dtype=torch.float32, device=dev) if scores is None else scores
+    ws = _workspace(draft_rnn_workspace_bytes(R, g, V, r), dev, workspace)
+    st = L.dspark_draft_sample_rnn_w2t(
+        _dev(U, "U", dt), _dev(W1, "W1", dt, (V, r)), _dev(W2T, "W2T", dt, (V, r)),
+        _dev(Wh, "Wh", dt, (r, r)), _dev(Q, "Q", torch.float32, (R, g, r)),
+        _dev(x0, "x0", torch.int32, (R,)), R, g, V, r, float(temperature),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(x, "x", torch.int32, (R, g)),
+        _dev(logp, "logp", torch.float32, (R, g)), _dev(lse, "lse", torch.float32, (R, g)),
+        _dev(scores, "scores", torch.float32, (R, g, V)), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check("dspark_draft_sample_rnn_w2t", st)
     return dict(x=x, logp=logp, lse=lse, scores=scores, workspace=ws)
 
 

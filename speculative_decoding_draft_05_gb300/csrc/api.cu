@@ -125,10 +125,24 @@ size_t dspark_draft_workspace_bytes(int R, int gamma, int V, int r, int dtype) {
   return draft_workspace_layout(R, gamma, V, r, dtype).total;
 }
 
-int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int32_t* x0,
-                        int dtype, int R, int gamma, int V, int r, float temperature,
-                        uint64_t seed, int32_t* x, float* logp, float* lse, float* scores,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+int dspark_transpose_w2(const void* W2, int r, int V, void* W2T, void* stream) {
+  if (!W2 || !W2T || r <= 0 || V <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (r > 256 || r % 64 != 0 || V % 8 != 0) return DSPARK_ERR_UNSUPPORTED;
+  if (!aligned16(W2) || !aligned16(W2T)) return DSPARK_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  prof_begin(kKindPrepare, s);
+  const cudaError_t e = launch_transpose_w2(W2, r, V, W2T, s);
+  prof_end(s);
+  if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
+  return DSPARK_OK;
+}
+
+// The Markov-head draft; W2 is [r, V] as stored, or (w2t) the K-major W2^T
+// [V, r] that dspark_transpose_w2 wrote, which the tensor-core steps read.
+static int draft_markov(const void* U, const void* W1, const void* W2, bool w2t,
+                        const int32_t* x0, int dtype, int R, int gamma, int V, int r,
+                        float temperature, uint64_t seed, int32_t* x, float* logp, float* lse,
+                        float* scores, void* workspace, size_t workspace_bytes, void* stream) {
   if (!U || !W1 || !W2 || !x0 || !x || !logp || !lse || !scores) return DSPARK_ERR_INVALID_ARG;
   if (r <= 0) return DSPARK_ERR_INVALID_ARG;
   int st = check_common(R, gamma, V, temperature, dtype);
@@ -144,6 +158,7 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   int* status = (int*)(ws + L.status);
   void* A = ws + L.a_rows;
   const bool tc = dtype == DSPARK_BF16 && draft_tc_supported(R, V, r);
+  if (w2t && !tc) return DSPARK_ERR_UNSUPPORTED;  // W2^T feeds the tensor-core steps only
   const int n_parts = tc ? draft_tc_parts(R, V) : (V + kDraftTileN - 1) / kDraftTileN;
   DraftPartials p{(float4*)(ws + L.stats), (int*)(ws + L.index), n_parts};
   DraftPartials p2{(float4*)(ws + L.stats2), (int*)(ws + L.index2), n_parts};
@@ -159,11 +174,14 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   if (tc) {
     // Tensor-core path: each step gathers its A tile itself; partials alternate
     // between two buffers; one combine after the last step.
-    void* W2T = ws + L.w2t;
-    prof_begin(kKindPrepare, s);
-    e = launch_transpose_w2(W2, r, V, W2T, s);
-    prof_end(s);
-    if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
+    const void* W2T = W2;
+    if (!w2t) {
+      W2T = ws + L.w2t;
+      prof_begin(kKindPrepare, s);
+      e = launch_transpose_w2(W2, r, V, ws + L.w2t, s);
+      prof_end(s);
+      if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
+    }
     DraftTcPlan plan;
     e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
     if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
@@ -203,6 +221,22 @@ int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int
   return DSPARK_OK;
 }
 
+int dspark_draft_sample(const void* U, const void* W1, const void* W2, const int32_t* x0,
+                        int dtype, int R, int gamma, int V, int r, float temperature,
+                        uint64_t seed, int32_t* x, float* logp, float* lse, float* scores,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return draft_markov(U, W1, W2, false, x0, dtype, R, gamma, V, r, temperature, seed, x, logp,
+                      lse, scores, workspace, workspace_bytes, stream);
+}
+
+int dspark_draft_sample_w2t(const void* U, const void* W1, const void* W2T, const int32_t* x0,
+                            int R, int gamma, int V, int r, float temperature, uint64_t seed,
+                            int32_t* x, float* logp, float* lse, float* scores, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return draft_markov(U, W1, W2T, true, x0, DSPARK_BF16, R, gamma, V, r, temperature, seed, x,
+                      logp, lse, scores, workspace, workspace_bytes, stream);
+}
+
 // The RNN head's extra scratch after the draft workspace: the state h [2][R, r]
 // fp32 (double-buffered across steps) and the A rows [R padded to 128, r] bf16.
 struct RnnWorkspace {
@@ -221,11 +255,10 @@ size_t dspark_draft_rnn_workspace_bytes(int R, int gamma, int V, int r) {
   return rnn_workspace_layout(R, gamma, V, r).total;
 }
 
-int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const void* Wh,
-                            const float* Q, const int32_t* x0, int dtype, int R, int gamma, int V,
-                            int r, float temperature, uint64_t seed, int32_t* x, float* logp,
-                            float* lse, float* scores, void* workspace, size_t workspace_bytes,
-                            void* stream) {
+static int draft_rnn(const void* U, const void* W1, const void* W2, bool w2t, const void* Wh,
+                     const float* Q, const int32_t* x0, int dtype, int R, int gamma, int V, int r,
+                     float temperature, uint64_t seed, int32_t* x, float* logp, float* lse,
+                     float* scores, void* workspace, size_t workspace_bytes, void* stream) {
   if (!U || !W1 || !W2 || !Wh || !Q || !x0 || !x || !logp || !lse || !scores)
     return DSPARK_ERR_INVALID_ARG;
   if (r <= 0) return DSPARK_ERR_INVALID_ARG;
@@ -253,11 +286,14 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
   if (e == cudaSuccess)  // A's rows past R stay zero: the contraction reads whole 128-row tiles
     e = cudaMemsetAsync(A, 0, ((size_t)R + 127) / 128 * 128 * r * 2, s);
   if (e != cudaSuccess) return cuda_fail(e, "draft_rnn reset");
-  void* W2T = ws + L.w2t;
-  prof_begin(kKindPrepare, s);
-  e = launch_transpose_w2(W2, r, V, W2T, s);
-  prof_end(s);
-  if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
+  const void* W2T = W2;
+  if (!w2t) {
+    W2T = ws + L.w2t;
+    prof_begin(kKindPrepare, s);
+    e = launch_transpose_w2(W2, r, V, ws + L.w2t, s);
+    prof_end(s);
+    if (e != cudaSuccess) return cuda_fail(e, "transpose_w2");
+  }
   DraftTcPlan plan;
   e = prepare_draft_tc(&plan, U, W2T, R, gamma, V, r, scores);
   if (e != cudaSuccess) return cuda_fail(e, "draft tensor maps");
@@ -284,6 +320,24 @@ int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const
   prof_end(s);
   if (e != cudaSuccess) return cuda_fail(e, "draft_combine");
   return DSPARK_OK;
+}
+
+int dspark_draft_sample_rnn(const void* U, const void* W1, const void* W2, const void* Wh,
+                            const float* Q, const int32_t* x0, int dtype, int R, int gamma, int V,
+                            int r, float temperature, uint64_t seed, int32_t* x, float* logp,
+                            float* lse, float* scores, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  return draft_rnn(U, W1, W2, false, Wh, Q, x0, dtype, R, gamma, V, r, temperature, seed, x, logp,
+                   lse, scores, workspace, workspace_bytes, stream);
+}
+
+int dspark_draft_sample_rnn_w2t(const void* U, const void* W1, const void* W2T, const void* Wh,
+                                const float* Q, const int32_t* x0, int R, int gamma, int V, int r,
+                                float temperature, uint64_t seed, int32_t* x, float* logp,
+                                float* lse, float* scores, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return draft_rnn(U, W1, W2T, true, Wh, Q, x0, DSPARK_BF16, R, gamma, V, r, temperature, seed, x,
+                   logp, lse, scores, workspace, workspace_bytes, stream);
 }
 
 size_t dspark_schedule_workspace_bytes(int R, int gamma) {

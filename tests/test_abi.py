@@ -133,3 +133,43 @@ def test_rnn_draft_rejects_bad_arguments_on_the_host(lib):
     assert _draft_rnn(lib, Q=8) == 1
     assert _draft_rnn(lib, ws=None) == 3
     assert _draft_rnn(lib, wsb=16) == 3
+
+
+def test_transposed_w2_calls_reject_bad_arguments_on_the_host(lib):
+    # transpose_w2(W2, r, V, W2T, stream)
+    assert lib.dspark_transpose_w2(None, 64, 1024, 16, None) == 1
+    assert lib.dspark_transpose_w2(16, 64, 1024, None, None) == 1
+    assert lib.dspark_transpose_w2(16, 48, 1024, 16, None) == 2
+    assert lib.dspark_transpose_w2(16, 320, 1024, 16, None) == 2
+    assert lib.dspark_transpose_w2(16, 64, 1001, 16, None) == 2
+    assert lib.dspark_transpose_w2(8, 64, 1024, 16, None) == 1  # not 16-byte aligned
+
+    def draft_w2t(**kw):
+        a = dict(U=16, W1=16, W2T=16, x0=16, R=4, gamma=4, V=1024, r=64, T=1.0, seed=0, x=16,
+                 logp=16, lse=16, scores=16, ws=256, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return lib.dspark_draft_sample_w2t(a["U"], a["W1"], a["W2T"], a["x0"], a["R"], a["gamma"],
+                                           a["V"], a["r"], a["T"], a["seed"], a["x"], a["logp"],
+                                           a["lse"], a["scores"], a["ws"], a["wsb"], a["stream"])
+
+    assert draft_w2t(W2T=None) == 1
+    assert draft_w2t(R=0) == 1
+    assert draft_w2t(T=-1.0) == 1
+    assert draft_w2t(r=48) == 2
+    assert draft_w2t(V=1001) == 2
+    assert draft_w2t(W2T=8) == 1
+    assert draft_w2t(ws=None) == 3
+
+    def rnn_w2t(**kw):
+        a = dict(U=16, W1=16, W2T=16, Wh=16, Q=16, x0=16, R=4, gamma=4, V=1024, r=64, T=1.0,
+                 seed=0, x=16, logp=16, lse=16, scores=16, ws=256, wsb=1 << 30, stream=None)
+        a.update(kw)
+        return lib.dspark_draft_sample_rnn_w2t(a["U"], a["W1"], a["W2T"], a["Wh"], a["Q"], a["x0"],
+                                               a["R"], a["gamma"], a["V"], a["r"], a["T"],
+                                               a["seed"], a["x"], a["logp"], a["lse"], a["scores"],
+                                               a["ws"], a["wsb"], a["stream"])
+
+    assert rnn_w2t(W2T=None) == 1
+    assert rnn_w2t(Wh=None) == 1
+    assert rnn_w2t(r=96) == 2
+    assert rnn_w2t(wsb=16) == 3

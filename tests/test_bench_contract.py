@@ -43,6 +43,8 @@ def test_our_arm_line():
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3 and d["value"] > 0
     assert d["scaling"] == "weak" and d["vs_baseline"] is None
     assert d["config"]["workload"].startswith("qwen3_r64_g16_v151936") and "l2" in d["config"]
+    assert d["config"]["w2_layout"] == "transposed at setup"
+    assert "prepare" not in d["kernels"]  # no per-round transpose
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
@@ -70,3 +72,12 @@ def test_seeds_mode_line():
     assert d["steps"] == 3 and d["config"]["seeds"] == 3 and d["value"] > 0
     assert d["accepted_tokens_per_s"] > 0 and 3 * 16 <= d["emitted_tokens"] <= 3 * 16 * 17
     assert d["ms_per_round"]["min"] <= d["ms_per_step"] <= d["ms_per_round"]["max"] + 1e-9
+
+
+@pytest.mark.gpu
+def test_plain_w2_layout_line():
+    # W2 passed as stored: every round's draft call transposes it itself.
+    d = _run(["--workload", "qwen3_r64_g16_v151936", "--R", "8", "--gamma", "4", "--steps", "3", "--warmup", "3",
+              "--no-cpu-baseline", "--w2-layout", "plain"], 600)
+    assert d["config"]["w2_layout"] == "plain" and d["value"] > 0
+    assert d["kernels"]["prepare"]["launches"] == 3
