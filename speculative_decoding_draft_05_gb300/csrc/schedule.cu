@@ -7,21 +7,27 @@
 // SPS the engine's measured step-rate table.  Algorithm 1 extends prefixes in
 // survival order and stops at the first candidate that does not improve Theta.
 //
-// Two launches, every step exact or IEEE-rounded in a fixed order, so the
-// result is bit-reproducible on any device:
-//   schedule_rank  (up to one CTA per SM) each CTA builds the sort key of every
-//                  candidate in shared memory.  Survival is non-increasing along
+// Every step is exact or IEEE-rounded in a fixed order, so the result is
+// bit-reproducible on any device.  Each kernel runs in CTAs of 128 threads with
+// at most 56 registers and no dynamic shared memory: one fits on an SM beside
+// a tensor-core draft step's CTA, so a schedule issued on a side stream next
+// to the draft takes no SM from it (CTAs of 1024 threads with the keys staged
+// in shared memory had waited for SMs between draft steps and delayed them).
+//   schedule_keys  one thread per request: the sequential products and the
+//                  sort key of each of its gamma candidates, to global memory.
+//   schedule_rank  one thread per candidate.  Survival is non-increasing along
 //                  a request, so every request's gamma keys are already sorted;
 //                  a candidate's place in the global order is the sum over
 //                  requests of how many of their keys are smaller (a binary
-//                  search of <= 64 keys each), split across the CTA's warps.
-//                  Keys are unique, so these ranks are a permutation: each
-//                  candidate is written to its slot of the sorted array.
+//                  search of <= 64 keys each, the lists streamed through a
+//                  3 KB shared-memory window).  Keys are unique, so these ranks
+//                  are a permutation: each candidate is written to its slot of
+//                  the sorted array.
 //   schedule_scan  (one CTA) exact int64 prefix sum of the fixed-point
-//                  survivals in sorted order, the Theta test of every prefix in
-//                  parallel (an exact integer comparison of the products
-//                  tau * SPS, no floating point), a block-wide minimum for the
-//                  first non-improvement, and the per-request counts l_r.
+//                  survivals in sorted order, the Theta test of every prefix
+//                  (an exact integer comparison of the products tau * SPS, no
+//                  floating point), a block-wide minimum for the first
+//                  non-improvement, and the per-request counts l_r.
 //
 // Zero-overhead scheduling (same summary, §5.2): the capacity K comes from
 // confidences two steps old without the early stop -- schedule_capacity is
@@ -35,9 +41,11 @@ namespace dspark {
 
 namespace {
 
-constexpr int kSchedThreads = 1024;
+constexpr int kSchedThreads = 128;
 constexpr int kMaxCandidates = 16384;
-constexpr int kPerThread = kMaxCandidates / kSchedThreads;  // 16
+constexpr int kChunkKeys = 384;  // schedule_rank's shared-memory window: 3 KB of keys
+// (128 threads, at least 9 CTAs' worth of registers per SM: <= 56 registers)
+#define SCHED_BOUNDS __launch_bounds__(kSchedThreads, 9)
 
 __device__ __forceinline__ unsigned long long sort_key(float a, int j, int r) {
   // a >= 0: its bit pattern orders like the value.  Complementing it sorts by a
@@ -122,104 +130,86 @@ __device__ __forceinline__ bool greater_packed(long long ta, unsigned long long 
   return greater_split(ta, ra & kM, (int)(ra >> 53) - 1075, tb, rb & kM, (int)(rb >> 53) - 1075);
 }
 
-__global__ void __launch_bounds__(kSchedThreads)
-schedule_rank_kernel(const float* __restrict__ conf, int R, int gamma,
-                     unsigned long long* __restrict__ sorted, int* __restrict__ status) {
-  // The kernel after this one (scan, capacity or top-K) may be launched now; it
-  // waits for this grid's completion before reading anything.
+__global__ void SCHED_BOUNDS
+schedule_keys_kernel(const float* __restrict__ conf, int R, int gamma,
+                     unsigned long long* __restrict__ keys, int* __restrict__ status) {
+  // The rank kernel may be launched now; it waits for this grid before reading.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  extern __shared__ unsigned long long keys[];  // [R][gamma], ascending along each request
-  const int tid = threadIdx.x;
-  const int n = R * gamma;
-  // The confidences first, coalesced, into shared memory behind the keys (one
-  // memory round trip), then each request's sequential products from there.
-  float* cst = reinterpret_cast<float*>(keys + n);
-#pragma unroll 4
-  for (int i = tid; i < n; i += kSchedThreads) cst[i] = conf[i];
-  __syncthreads();
-  for (int r = tid; r < R; r += kSchedThreads) {
-    float a = 1.0f;
-    for (int j = 0; j < gamma; ++j) {
-      float c = cst[r * gamma + j];
-      if (!(c >= 0.0f) || c > 1.0f) {
-        if (blockIdx.x == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
-        c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
-      }
-      a = (j == 0) ? c : __fmul_rn(a, c);
-      const float av = (a == 0.0f) ? 0.0f : a;  // canonical +0
-      keys[r * gamma + j] = sort_key(av, j, r);
+  const int r = blockIdx.x * kSchedThreads + threadIdx.x;
+  if (r >= R) return;
+  float a = 1.0f;
+  for (int j = 0; j < gamma; ++j) {
+    float c = conf[(size_t)r * gamma + j];
+    if (!(c >= 0.0f) || c > 1.0f) {
+      flag_status(status, DSPARK_DEV_BAD_INPUT);
+      c = (c > 1.0f) ? 1.0f : 0.0f;  // NaN and negatives -> 0
     }
-  }
-  __syncthreads();
-  // Blocks of 32 candidates, one per lane; warp w counts, for every lane's
-  // candidate, the keys below it in the lists of requests r = w, w + 32, ...
-  // (all lanes probe the same list at once: no bank conflicts).  Each count is
-  // a branch-free lower bound with the same number of steps for every lane
-  // (ceil(log2 gamma)), four lists interleaved so that their probes overlap.
-  __shared__ int part[kSchedThreads / 32][33];
-  const int lane = tid & 31, warp = tid >> 5;
-  const int blocks = (n + 31) / 32;
-  constexpr int kW = kSchedThreads / 32;
-  for (int blk = blockIdx.x; blk < blocks; blk += gridDim.x) {
-    const int e = blk * 32 + lane;
-    const unsigned long long key = e < n ? keys[e] : ~0ull;
-    int below = 0;
-    for (int r0 = warp; r0 < R; r0 += 4 * kW) {
-      int pos[4];  // list start + running base, per list
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = r0 + q * kW;
-        pos[q] = (r < R ? r : r0) * gamma;
-      }
-      for (int len = gamma; len > 1;) {  // the answer lies in [base, base + len]
-        const int half = len >> 1;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) pos[q] += keys[pos[q] + half] < key ? half : 0;
-        len -= half;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int r = r0 + q * kW;
-        if (r < R) below += pos[q] - r * gamma + (keys[pos[q]] < key ? 1 : 0);
-      }
-    }
-    part[warp][lane] = below;
-    __syncthreads();
-    if (warp == 0) {
-      int rank = 0;
-#pragma unroll 8
-      for (int w = 0; w < kSchedThreads / 32; ++w) rank += part[w][lane];
-      if (e < n) sorted[rank] = key;
-    }
-    __syncthreads();
+    a = (j == 0) ? c : __fmul_rn(a, c);
+    const float av = (a == 0.0f) ? 0.0f : a;  // canonical +0
+    keys[(size_t)r * gamma + j] = sort_key(av, j, r);
   }
 }
 
-// Shared-memory slot of element i: one pad slot after every 16 elements, so
-// that thread t reading its 16 consecutive 8-byte elements 16t + e hits banks
-// 2(t + e) mod 32 -- at most two lanes of a warp per bank pair.
-__device__ __forceinline__ int skew(int i) { return i + (i >> 4); }
-constexpr int kStageSlots = kMaxCandidates + kMaxCandidates / 16 + 2;  // 8-byte slots
-
-// Exclusive prefix of the fixed-point survivals of this thread's kPerThread
-// sorted keys (staged coalesced in shared memory, then read into registers).
-__device__ __forceinline__ long long stage_and_prefix(const unsigned long long* __restrict__ sorted,
-                                                      int n, unsigned long long* stage,
-                                                      long long* warp_tot,
-                                                      unsigned long long (&k)[kPerThread]) {
-  const int tid = threadIdx.x, base = tid * kPerThread;
+__global__ void SCHED_BOUNDS
+schedule_rank_kernel(const unsigned long long* __restrict__ keys, int R, int gamma,
+                     unsigned long long* __restrict__ sorted) {
+  // The kernel after this one (scan, capacity or top-K) may be launched now; it
+  // waits for this grid's completion before reading anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The keys come from the kernel before (this grid's programmatic primary):
+  // read after its completion, through L2 (ld.global.cg), never the
+  // non-coherent path, since this grid may start while that kernel runs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ unsigned long long chunk[kChunkKeys];
+  const int n = R * gamma;
+  const int e = blockIdx.x * kSchedThreads + threadIdx.x;  // this thread's candidate
+  const bool valid = e < n;
+  const unsigned long long key = valid ? __ldcg(keys + e) : 0ull;
+  // The requests' lists pass through shared memory a few at a time (each key
+  // is read from L2 once per CTA); every thread counts the keys below its own
+  // in each list, a branch-free lower bound with the same number of steps
+  // (ceil(log2 gamma)) for all lanes, four lists interleaved.  All lanes probe
+  // the same list at once: its gamma keys span the banks once.
+  const int per = kChunkKeys / gamma;  // whole lists per chunk (gamma <= 64)
+  int below = 0;
+  for (int r0 = 0; r0 < R; r0 += per) {
+    const int nl = min(per, R - r0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nl * gamma; i += kSchedThreads)
+      chunk[i] = __ldcg(keys + (size_t)r0 * gamma + i);
+    __syncthreads();
+    if (!valid) continue;
+    int l = 0;
+    for (; l + 4 <= nl; l += 4) {
+      int pos[4];
 #pragma unroll
-  for (int i = tid; i < kMaxCandidates; i += kSchedThreads)
-    stage[skew(i)] = i < n ? __ldcg(sorted + i) : ~0ull;  // L2 (see the scan kernel)
-  __syncthreads();
-  long long local = 0;
+      for (int q = 0; q < 4; ++q) pos[q] = (l + q) * gamma;
+      for (int len = gamma; len > 1;) {  // the answer lies in [base, base + len]
+        const int half = len >> 1;
 #pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    k[e] = stage[skew(base + e)];
-    if (base + e < n) local += fixed_survival(k[e]);
+        for (int q = 0; q < 4; ++q) pos[q] += chunk[pos[q] + half] < key ? half : 0;
+        len -= half;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) below += pos[q] - (l + q) * gamma + (chunk[pos[q]] < key ? 1 : 0);
+    }
+    for (; l < nl; ++l) {
+      int pos = l * gamma;
+      for (int len = gamma; len > 1;) {
+        const int half = len >> 1;
+        pos += chunk[pos + half] < key ? half : 0;
+        len -= half;
+      }
+      below += pos - l * gamma + (chunk[pos] < key ? 1 : 0);
+    }
   }
-  const int lane = tid & 31, warp = tid >> 5;
-  long long incl = local;
+  if (valid) sorted[below] = key;
+}
+
+// Exclusive prefix over the block of one int64 per thread (kSchedThreads).
+__device__ __forceinline__ long long block_exclusive_sum(long long v, long long* warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const long long y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -227,30 +217,26 @@ __device__ __forceinline__ long long stage_and_prefix(const unsigned long long* 
   }
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    long long t = warp_tot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    warp_tot[lane] = t;
-  }
-  __syncthreads();
-  return (incl - local) + (warp > 0 ? warp_tot[warp - 1] : 0ll);
+  long long before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  return before + incl - v;
 }
 
-// The step rates sps[R + i], i = 0 .. n, packed (pack_rate) into the same
-// shared memory, skewed like the keys, once every thread holds its keys in
-// registers.
-__device__ __forceinline__ void stage_rates(const double* __restrict__ sps, int R, int n,
-                                            unsigned long long* st) {
-  __syncthreads();
-  for (int i = threadIdx.x; i <= n; i += kSchedThreads) st[skew(i)] = pack_rate(sps[R + i]);
-  __syncthreads();
+// This thread's contiguous share [b0, b1) of the n sorted candidates, and the
+// exact exclusive prefix of their fixed-point survivals.  The sorted keys are
+// the rank kernel's output: read through L2 (see the scan kernel).
+__device__ __forceinline__ long long share_prefix(const unsigned long long* __restrict__ sorted,
+                                                  int n, int& b0, int& b1, long long* warp_tot) {
+  const int per = (n + kSchedThreads - 1) / kSchedThreads;
+  b0 = min(n, (int)threadIdx.x * per);
+  b1 = min(n, b0 + per);
+  long long local = 0;
+#pragma unroll 8
+  for (int i = b0; i < b1; ++i) local += fixed_survival(__ldcg(sorted + i));
+  return block_exclusive_sum(local, warp_tot);
 }
 
-__global__ void __launch_bounds__(kSchedThreads)
+__global__ void SCHED_BOUNDS
 schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double* __restrict__ sps,
                      int R, int gamma, int32_t* __restrict__ ell, double* __restrict__ diag,
                      int* __restrict__ status) {
@@ -260,53 +246,40 @@ schedule_scan_kernel(const unsigned long long* __restrict__ sorted, const double
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ long long warp_tot[kSchedThreads / 32];
   __shared__ int stop_at;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int n = R * gamma;
-  const int base = tid * kPerThread;
-  const int lane = tid & 31;
   for (int r = tid; r < R; r += kSchedThreads) ell[r] = 0;
   if (tid == 0) stop_at = n + 1;
-
-  // Coalesced load of the sorted keys into shared memory, then 16 contiguous
-  // keys per thread and their exclusive prefix; then the step rates.
-  extern __shared__ unsigned long long stage[];  // [kStageSlots]
-  unsigned long long k[kPerThread];
-  const long long run0 = stage_and_prefix(sorted, n, stage, warp_tot, k);
-  const unsigned long long* sv = stage;
-  stage_rates(sps, R, n, stage);
+  int b0, b1;
+  const long long run0 = share_prefix(sorted, n, b0, b1, warp_tot);
 
   // Theta test of every candidate (0-based index i, 1-based number i + 1):
   // before it B = R + i and tau = R + P_i; after it B = R + i + 1.
   const long long tau0 = (long long)R << 48;
   long long run = run0;
   int first_fail = n + 1;  // this thread's first non-improving candidate (1-based)
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int i = base + e;
-    if (i < n) {
-      const long long tau_prev = tau0 + run;
-      run += fixed_survival(k[e]);
-      if (!greater_packed(tau0 + run, sv[skew(i + 1)], tau_prev, sv[skew(i)], status))
-        first_fail = min(first_fail, i + 1);
-    }
+  unsigned long long rate_before = b0 < b1 ? pack_rate(sps[R + b0]) : 0ull;
+#pragma unroll 4
+  for (int i = b0; i < b1; ++i) {
+    const long long tau_prev = tau0 + run;
+    run += fixed_survival(__ldcg(sorted + i));
+    const unsigned long long rate_after = pack_rate(sps[R + i + 1]);
+    if (!greater_packed(tau0 + run, rate_after, tau_prev, rate_before, status))
+      first_fail = min(first_fail, i + 1);
+    rate_before = rate_after;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) first_fail = min(first_fail, __shfl_xor_sync(0xffffffffu, first_fail, o));
   if (lane == 0 && first_fail <= n) atomicMin(&stop_at, first_fail);  // one per warp
   __syncthreads();
   const int taken = stop_at - 1;  // candidates 0..taken-1 were taken
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e)
-    if (base + e < taken) atomicAdd(&ell[(int)(k[e] & 0xffffu)], 1);
+  for (int i = b0; i < min(b1, taken); ++i) atomicAdd(&ell[(int)(__ldcg(sorted + i) & 0xffffu)], 1);
   if (diag) {
-    // tau after the taken candidates: the owner of index taken-1 finishes its chunk's sum.
-    const bool owner =
-        (taken == 0) ? (tid == 0) : (base <= taken - 1 && taken - 1 < base + kPerThread);
+    // tau after the taken candidates: the owner of index taken-1 finishes its share's sum.
+    const bool owner = (taken == 0) ? (tid == 0) : (b0 <= taken - 1 && taken - 1 < b1);
     if (owner) {
       long long tau = tau0 + (taken == 0 ? 0ll : run0);
-#pragma unroll
-      for (int e = 0; e < kPerThread; ++e)
-        if (taken > 0 && base + e < taken) tau += fixed_survival(k[e]);
+      for (int i = b0; i < taken; ++i) tau += fixed_survival(__ldcg(sorted + i));
       diag[0] = (double)(R + taken);
       diag[1] = __ll2double_rn(tau) * 0x1p-48;
       diag[2] = __dmul_rn(__ll2double_rn(tau) * 0x1p-48, sps[R + taken]);
@@ -329,7 +302,7 @@ __device__ __forceinline__ void better_theta(long long& t, int& k, unsigned long
   }
 }
 
-__global__ void __launch_bounds__(kSchedThreads)
+__global__ void SCHED_BOUNDS
 schedule_capacity_kernel(const unsigned long long* __restrict__ sorted,
                          const double* __restrict__ sps, int R, int gamma,
                          int32_t* __restrict__ K_out, double* __restrict__ diag,
@@ -339,25 +312,19 @@ schedule_capacity_kernel(const unsigned long long* __restrict__ sorted,
   __shared__ long long red_t[kSchedThreads / 32];
   __shared__ int red_k[kSchedThreads / 32];
   __shared__ unsigned long long red_s[kSchedThreads / 32];
-  extern __shared__ unsigned long long stage[];  // [kMaxCandidates]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = R * gamma, base = tid * kPerThread;
-  unsigned long long k[kPerThread];
-  long long run = stage_and_prefix(sorted, n, stage, warp_tot, k);
+  const int n = R * gamma;
+  int b0, b1;
+  long long run = share_prefix(sorted, n, b0, b1, warp_tot);
   const long long tau0 = (long long)R << 48;
-  const unsigned long long* sv = stage;
-  stage_rates(sps, R, n, stage);
   // this thread's best prefix; thread 0 also holds the empty one (k = 0)
   long long bt = tau0;
   int bk = tid == 0 ? 0 : -1;
-  unsigned long long bs = sv[skew(0)];  // sps[R], thread 0's empty prefix
-#pragma unroll
-  for (int e = 0; e < kPerThread; ++e) {
-    const int i = base + e;
-    if (i < n) {
-      run += fixed_survival(k[e]);
-      better_theta(bt, bk, bs, tau0 + run, i + 1, sv[skew(i + 1)], status);
-    }
+  unsigned long long bs = pack_rate(sps[R]);  // thread 0's empty prefix
+#pragma unroll 4
+  for (int i = b0; i < b1; ++i) {
+    run += fixed_survival(__ldcg(sorted + i));
+    better_theta(bt, bk, bs, tau0 + run, i + 1, pack_rate(sps[R + i + 1]), status);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -372,37 +339,26 @@ schedule_capacity_kernel(const unsigned long long* __restrict__ sorted,
     red_s[warp] = bs;
   }
   __syncthreads();
-  if (warp == 0) {
-    bt = red_t[lane];
-    bk = red_k[lane];
-    bs = red_s[lane];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const long long t2 = __shfl_xor_sync(0xffffffffu, bt, o);
-      const int k2 = __shfl_xor_sync(0xffffffffu, bk, o);
-      const unsigned long long s2 = __shfl_xor_sync(0xffffffffu, bs, o);
-      better_theta(bt, bk, bs, t2, k2, s2, status);
-    }
-    if (lane == 0) {
-      K_out[0] = bk;
-      if (diag) {
-        diag[0] = (double)(R + bk);
-        diag[1] = __ll2double_rn(bt) * 0x1p-48;
-        diag[2] = __dmul_rn(__ll2double_rn(bt) * 0x1p-48, sps[R + bk]);
-        diag[3] = (double)bk;
-      }
+  if (tid == 0) {
+    for (int w = 1; w < kSchedThreads / 32; ++w) better_theta(bt, bk, bs, red_t[w], red_k[w], red_s[w], status);
+    K_out[0] = bk;
+    if (diag) {
+      diag[0] = (double)(R + bk);
+      diag[1] = __ll2double_rn(bt) * 0x1p-48;
+      diag[2] = __dmul_rn(__ll2double_rn(bt) * 0x1p-48, sps[R + bk]);
+      diag[3] = (double)bk;
     }
   }
 }
 
-__global__ void __launch_bounds__(kSchedThreads)
+__global__ void SCHED_BOUNDS
 schedule_topk_kernel(const unsigned long long* __restrict__ sorted, const int32_t* __restrict__ K,
                      int R, int gamma, int32_t* __restrict__ ell, int* __restrict__ status) {
   asm volatile("griddepcontrol.wait;" ::: "memory");  // launched as the rank kernel's dependent
   const int n = R * gamma;
   for (int r = threadIdx.x; r < R; r += kSchedThreads) ell[r] = 0;
   __syncthreads();
-  int k = *K;
+  int k = __ldcg(K);
   if (k < 0) {
     if (threadIdx.x == 0) flag_status(status, DSPARK_DEV_BAD_INPUT);
     k = 0;
@@ -412,25 +368,14 @@ schedule_topk_kernel(const unsigned long long* __restrict__ sorted, const int32_
     atomicAdd(&ell[(int)(__ldcg(sorted + i) & 0xffffu)], 1);
 }
 
-int sm_count_sched() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
-// Launch as a programmatic dependent of the kernel before it on the stream
-// (the rank kernel), so that its launch overlaps that kernel's end.
+// Launch as a programmatic dependent of the kernel before it on the stream,
+// so that its launch overlaps that kernel's end.
 template <typename... Params, typename... Args>
-cudaError_t launch_after_rank(void (*kernel)(Params...), size_t smem, cudaStream_t s, Args... args) {
+cudaError_t launch_dependent(void (*kernel)(Params...), int grid, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kSchedThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -440,60 +385,69 @@ cudaError_t launch_after_rank(void (*kernel)(Params...), size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
+// The scheduler's kernels ask for the largest shared-memory carveout, the one
+// the draft steps run with, so that an SM can hold a CTA of each at once (an
+// SM changes its carveout only when idle).  Once per process.
+cudaError_t set_carveouts() {
+  static const cudaError_t err = [] {
+    const int kMax = (int)cudaSharedmemCarveoutMaxShared;
+    cudaError_t e = cudaFuncSetAttribute(schedule_keys_kernel,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout, kMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(schedule_rank_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(schedule_scan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(schedule_capacity_kernel,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, kMax);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(schedule_topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMax);
+    return e;
+  }();
+  return err;
+}
+
 }  // namespace
 
+// The sorted keys, then the keys in candidate order.
 size_t schedule_sorted_bytes(int R, int gamma) {
-  return (size_t)R * gamma * sizeof(unsigned long long);
+  return 2 * (size_t)R * gamma * sizeof(unsigned long long);
 }
 
 cudaError_t launch_schedule_rank(const float* conf, int R, int gamma, unsigned long long* sorted,
                                  int* status, cudaStream_t s) {
   const int n = R * gamma;
   if (n > kMaxCandidates) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)n * (sizeof(unsigned long long) + sizeof(float));  // keys + conf
-  // Once per process (thread-safe initialisation of a function-local static).
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(schedule_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(kMaxCandidates * (sizeof(unsigned long long) + sizeof(float))));
-  if (attr_err != cudaSuccess) return attr_err;
-  int blocks = (n + 31) / 32;  // 32 candidates per CTA pass
-  const int sms = sm_count_sched();
-  if (blocks > sms) blocks = sms;
-  if (blocks < 1) blocks = 1;
-  schedule_rank_kernel<<<blocks, kSchedThreads, smem, s>>>(conf, R, gamma, sorted, status);
-  return cudaGetLastError();
+  unsigned long long* keys = sorted + n;
+  cudaError_t e = set_carveouts();
+  if (e != cudaSuccess) return e;
+  schedule_keys_kernel<<<(R + kSchedThreads - 1) / kSchedThreads, kSchedThreads, 0, s>>>(
+      conf, R, gamma, keys, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = (n + kSchedThreads - 1) / kSchedThreads;
+  return launch_dependent(schedule_rank_kernel, grid, s, (const unsigned long long*)keys, R, gamma,
+                          sorted);
 }
 
 cudaError_t launch_schedule_scan(const unsigned long long* sorted, const double* sps, int R,
                                  int gamma, int32_t* ell, double* diag, int* status,
                                  cudaStream_t s) {
   if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
-  const size_t smem = kStageSlots * sizeof(unsigned long long);
-  // Once per process (thread-safe initialisation of a function-local static).
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(schedule_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (attr_err != cudaSuccess) return attr_err;
-  return launch_after_rank(schedule_scan_kernel, smem, s, sorted, sps, R, gamma, ell, diag, status);
+  return launch_dependent(schedule_scan_kernel, 1, s, sorted, sps, R, gamma, ell, diag, status);
 }
 
 cudaError_t launch_schedule_capacity(const unsigned long long* sorted, const double* sps, int R,
                                      int gamma, int32_t* K, double* diag, int* status,
                                      cudaStream_t s) {
   if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
-  const size_t smem = kStageSlots * sizeof(unsigned long long);
-  // Once per process (thread-safe initialisation of a function-local static).
-  static const cudaError_t attr_err =
-      cudaFuncSetAttribute(schedule_capacity_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-  if (attr_err != cudaSuccess) return attr_err;
-  return launch_after_rank(schedule_capacity_kernel, smem, s, sorted, sps, R, gamma, K, diag, status);
+  return launch_dependent(schedule_capacity_kernel, 1, s, sorted, sps, R, gamma, K, diag, status);
 }
 
 cudaError_t launch_schedule_topk(const unsigned long long* sorted, const int32_t* K, int R,
                                  int gamma, int32_t* ell, int* status, cudaStream_t s) {
   if (R * gamma > kMaxCandidates) return cudaErrorInvalidValue;
-  return launch_after_rank(schedule_topk_kernel, 0, s, sorted, K, R, gamma, ell, status);
+  return launch_dependent(schedule_topk_kernel, 1, s, sorted, K, R, gamma, ell, status);
 }
 
 }  // namespace dspark
