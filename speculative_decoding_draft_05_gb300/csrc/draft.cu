@@ -130,6 +130,10 @@ __global__ void draft_combine_kernel(const float4* __restrict__ pstats,
                                      const float* __restrict__ scores, uint64_t seed,
                                      int32_t* __restrict__ x, float* __restrict__ logp,
                                      float* __restrict__ lse, int V, int* __restrict__ status) {
+  // Launched as a programmatic dependent of the draft step before it: wait for
+  // that step, then read its partials and scores through L2 (ld.global.cg),
+  // never the non-coherent path, since this grid may start while it runs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= R) return;
@@ -138,9 +142,9 @@ __global__ void draft_combine_kernel(const float4* __restrict__ pstats,
   float m = -INFINITY, S = 0.0f, key = -INFINITY, unused = 0.0f;
   int gj = 0x7fffffff;
   for (int t = lane; t < n_tiles; t += 32) {
-    const float4 q = ps[t];
+    const float4 q = __ldcg(ps + t);
     lse_merge(m, S, q.x, q.y);
-    const int qi = pi[t];
+    const int qi = __ldcg(pi + t);
     if (better(q.z, qi, key, gj)) {
       key = q.z;
       gj = qi;
@@ -155,7 +159,7 @@ __global__ void draft_combine_kernel(const float4* __restrict__ pstats,
   }
   const int v = gj * kGroup + lane;
   const bool valid = v < V;
-  const float sv = valid ? scores[((size_t)row * gamma + (k - 1)) * V + v] : 0.0f;
+  const float sv = valid ? __ldcg(scores + ((size_t)row * gamma + (k - 1)) * V + v) : 0.0f;
   float k2, s_x;
   int idx;
   group_draw_warp(sv, valid, v, seed, (uint32_t)row, (uint32_t)k, DSPARK_PURPOSE_DRAFT, k2, idx, s_x);
@@ -207,16 +211,25 @@ cudaError_t launch_draft_combine(DraftPartials p, int R, int gamma, int V, int r
                                  uint64_t seed, int32_t* x, float* logp, float* lse, int* status,
                                  cudaStream_t s) {
   const int warps = 8;
-  dim3 grid((R + warps - 1) / warps);
+  // A programmatic dependent of the draft step before it (the kernel waits for
+  // that step at entry), so that its launch overlaps the step's end.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((R + warps - 1) / warps);
+  cfg.blockDim = dim3(warps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (dtype == DSPARK_BF16)
-    draft_combine_kernel<__nv_bfloat16><<<grid, warps * 32, 0, s>>>(
-        p.stats, p.index, p.n_parts, R, gamma, r, k, (const __nv_bfloat16*)W1,
-        (__nv_bfloat16*)A_next, scores, seed, x, logp, lse, V, status);
-  else
-    draft_combine_kernel<float><<<grid, warps * 32, 0, s>>>(
-        p.stats, p.index, p.n_parts, R, gamma, r, k, (const float*)W1, (float*)A_next, scores, seed,
-        x, logp, lse, V, status);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, draft_combine_kernel<__nv_bfloat16>, (const float4*)p.stats,
+                              (const int*)p.index, p.n_parts, R, gamma, r, k,
+                              (const __nv_bfloat16*)W1, (__nv_bfloat16*)A_next, (const float*)scores,
+                              seed, x, logp, lse, V, status);
+  return cudaLaunchKernelEx(&cfg, draft_combine_kernel<float>, (const float4*)p.stats,
+                            (const int*)p.index, p.n_parts, R, gamma, r, k, (const float*)W1,
+                            (float*)A_next, (const float*)scores, seed, x, logp, lse, V, status);
 }
 
 }  // namespace dspark
