@@ -408,6 +408,51 @@ def verify_draw_bytes(w: workload.Workload, residual_rows: int) -> int:
     return w.R * w.V * e + residual_rows * w.V * 4
 
 
+def draft_step_period(rnd, w, device, seed, hbm_peak, reps: int = 10) -> dict:
+    """Per-step period of the draft in a whole draft call, from CUDA events around
+    the call at gamma and at 2 positions: (t_gamma - t_2) / (gamma - 2).  The two
+    calls share the call's fixed costs (resets, the final combine)."""
+    d = rnd.dspark
+    R, V, r = w.R, w.V, w.r
+    U2 = rnd.inp["U"][:, :2, :].contiguous()
+    out2 = dict(x=torch.empty(R, 2, dtype=torch.int32, device=device),
+                logp=torch.empty(R, 2, dtype=torch.float32, device=device),
+                lse=torch.empty(R, 2, dtype=torch.float32, device=device),
+                scores=torch.empty(R, 2, V, dtype=torch.float32, device=device),
+                workspace=torch.empty(d.draft_workspace_bytes(R, 2, V, r, torch.bfloat16),
+                                      dtype=torch.uint8, device=device))
+    i = rnd.inp
+
+    def call2():
+        if rnd.w2t is not None:
+            d.dspark_draft_sample_w2t(U2, i["W1"], rnd.w2t, i["x0"], w.T, seed, **out2)
+        else:
+            d.dspark_draft_sample(U2, i["W1"], i["W2"], i["x0"], w.T, seed, **out2)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps / 1e3
+
+    t_full = timed(lambda: rnd.draft(seed))
+    t_two = timed(call2)
+    del U2, out2
+    step = (t_full - t_two) / (w.gamma - 2)
+    nbytes = draft_tile_bytes(w)
+    return {"method": "draft call alone with CUDA events at gamma and at 2 positions; "
+                      "per step = difference / (gamma - 2); not part of value",
+            "draft_call_us": t_full * 1e6, "draft_call_us_at_2": t_two * 1e6,
+            "per_step_us": step * 1e6, "achieved": nbytes / step / 1e9,
+            "frac": nbytes / step / 1e9 / hbm_peak}
+
+
 def kernel_rooflines(w, prof, rows_per_round: int, residual_per_round: float, hbm_peak: float,
                      rnn: bool):
     """Per-kernel algorithmic bytes per launch / event-timed launch / measured HBM
@@ -765,6 +810,12 @@ def run_ours(args, w, rank, world, local):
                                     "gbs": 6 * n_el / t_probe / 1e9,
                                     "draft_step_us": avg_tile_s * 1e6,
                                     "probe_over_draft": t_probe / avg_tile_s}
+    # The draft step in its own launch configuration: consecutive steps are
+    # programmatic dependents and overlap, which per-launch events prevent.  The
+    # draft call is timed alone at gamma and at 2 positions (same R, V, weights);
+    # the difference over gamma - 2 is the period of one step inside the call.
+    if w.dtype == "bf16" and args.head == "markov" and w.gamma > 2:
+        roofline["pipelined"] = draft_step_period(rnd, w, device, args.seed, hbm_peak)
     k_roof = kernel_rooflines(w, prof, int(rnd.ell.sum().item()), residual_rows / len(seeds), hbm_peak,
                               args.head == "rnn")
     # Full-block verify over this round's own buffers, outside the timed regions:

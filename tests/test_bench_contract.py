@@ -48,6 +48,9 @@ def test_our_arm_line():
     rf = d["roofline"]
     assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    pl = rf["pipelined"]  # the draft step's period inside a whole draft call
+    assert pl["draft_call_us"] > 0 and pl["draft_call_us_at_2"] > 0
+    assert abs(pl["frac"] - pl["achieved"] / rf["peak"]) < 1e-9
     sp = rf["stream_probe"]
     assert sp["elements"] == 8 * 151936 and sp["gbs"] > 0 and sp["us"] > 0
     e = d["e2e"]
