@@ -351,12 +351,18 @@ verify_rows_stream_kernel(const int32_t* __restrict__ x, const float* __restrict
   }
 }
 
-// Leading accepts of request r (the first rejection is at row n + 1).
-__device__ __forceinline__ int leading_accepts(const int* __restrict__ acc_ws, int r, int gamma,
-                                               int L) {
-  int n = 0;
-  while (n < L && __ldcg(acc_ws + (size_t)r * gamma + n)) ++n;
-  return n;
+// Leading accepts of request r (the first rejection is at row n + 1), by one
+// warp: lanes read 32 accept flags at a time and the first zero among them
+// ends the run (one L2 round trip for gamma <= 32).
+__device__ __forceinline__ int leading_accepts_warp(const int* __restrict__ acc_ws, int r, int gamma,
+                                                    int L) {
+  const int lane = threadIdx.x & 31;
+  for (int base = 0; base < L; base += 32) {
+    const int a = base + lane < L ? __ldcg(acc_ws + (size_t)r * gamma + base + lane) : 1;
+    const unsigned zero = __ballot_sync(0xffffffffu, a == 0);
+    if (zero) return base + __ffs((int)zero) - 1;
+  }
+  return L;
 }
 
 // Philox4x32-10 round keys of one seed, passed by value as a kernel parameter:
@@ -635,9 +641,12 @@ verify_draw_kernel(const float* __restrict__ lse, const float* __restrict__ scor
   __shared__ uint32_t s_best;  // key_ord of the CTA's best key so far (0: none)
   const int r = blockIdx.y, chunk = blockIdx.x;
   const int L = clamp_ell(ell, r, gamma, nullptr, false);
-  if (threadIdx.x == 0) {
-    s_n = leading_accepts(acc_ws, r, gamma, L);
-    s_best = 0u;
+  if (threadIdx.x < 32) {
+    const int n0 = leading_accepts_warp(acc_ws, r, gamma, L);
+    if (threadIdx.x == 0) {
+      s_n = n0;
+      s_best = 0u;
+    }
   }
   __syncthreads();
   volatile uint32_t* cta_best = &s_best;
@@ -762,7 +771,10 @@ verify_emit_kernel(const int32_t* __restrict__ x, const float* __restrict__ lse,
   __shared__ int s_n, s_tok;
   const int r = blockIdx.x;
   const int L = clamp_ell(ell, r, gamma, nullptr, false);
-  if (threadIdx.x == 0) s_n = leading_accepts(acc_ws, r, gamma, L);
+  if (threadIdx.x < 32) {
+    const int n0 = leading_accepts_warp(acc_ws, r, gamma, L);
+    if (threadIdx.x == 0) s_n = n0;
+  }
   __syncthreads();
   const int n = s_n;
   const int row = n + 1;
