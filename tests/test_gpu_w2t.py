@@ -76,3 +76,19 @@ def test_rnn_draft_w2t_equals_rnn_draft():
     assert dspark.dspark_read_device_status(out["workspace"]) == 0
     for k in KEYS:
         assert torch.equal(out[k], ref[k]), k
+
+
+def test_draft_w2t_equals_draft_full_vocab():
+    # The serving workload's shapes (R = 1024 requests, V = 129,280, r = 256) at two
+    # positions: eight row tiles of 19 column slots each over 1,010 vocab tiles.
+    w = W["serving_r1024_g16_v129280"].resized(gamma=2)
+    dev = torch.device("cuda")
+    seed = 4
+    g = {k: v.to(dev) for k, v in workload.generate(w, seed=seed, device="cpu").items()}
+    ref = dspark.dspark_draft_sample(g["U"], g["W1"], g["W2"], g["x0"], w.T, seed)
+    W2T = dspark.dspark_transpose_w2(g["W2"])
+    out = dspark.dspark_draft_sample_w2t(g["U"], g["W1"], W2T, g["x0"], w.T, seed)
+    torch.cuda.synchronize()
+    assert dspark.dspark_read_device_status(out["workspace"]) == 0
+    for k in KEYS:
+        assert torch.equal(out[k], ref[k]), k
