@@ -169,7 +169,7 @@ schedule_rank_kernel(const unsigned long long* __restrict__ keys, int R, int gam
   // is read from L2 once per CTA); every thread counts the keys below its own
   // in each list, a branch-free lower bound with the same number of steps
   // (ceil(log2 gamma)) for all lanes, four lists interleaved.  All lanes probe
-  // the same list at once: its gamma keys span the banks once.
+  // the same list at once (at gamma <= 16 its keys span the banks at most once).
   const int per = kChunkKeys / gamma;  // whole lists per chunk (gamma <= 64)
   int below = 0;
   for (int r0 = 0; r0 < R; r0 += per) {
